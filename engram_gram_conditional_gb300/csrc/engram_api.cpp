@@ -1,0 +1,609 @@
+// Host side of libengram.so: the C ABI declared in include/engram.h.
+//
+// Holds the context (geometry, token map, per-layer hash parameters and bound
+// weights), the sessions (hash history), argument validation and the launch
+// of the kernels.  No compute of the forward step happens here: every step of
+// the path runs in the CUDA kernels of kernels_misc.cu and kernels_mma.cu.
+#include <cuda_runtime.h>
+#include <string.h>
+
+#include <algorithm>
+#include <new>
+#include <string>
+#include <vector>
+
+#include "../../include/engram.h"
+#include "engram_internal.h"
+
+using namespace engram;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+engram_status fail(engram_status st, const std::string& msg) {
+    g_last_error = msg;
+    return st;
+}
+engram_status ok() {
+    g_last_error.clear();
+    return ENGRAM_OK;
+}
+engram_status cuda_fail(cudaError_t e, const char* what) {
+    return fail(ENGRAM_ECUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+constexpr uint32_t kSessionMagic = 0x53474E45u;  // "ENGS"
+
+// ---- hash parameters (setup) -------------------------------------------------------
+// Deterministic Miller-Rabin for 64-bit n (bases 2..37).
+uint64_t mulmod(uint64_t a, uint64_t b, uint64_t m) {
+    return (uint64_t)((unsigned __int128)a * b % m);
+}
+uint64_t powmod(uint64_t a, uint64_t e, uint64_t m) {
+    uint64_t r = 1;
+    a %= m;
+    while (e) {
+        if (e & 1) r = mulmod(r, a, m);
+        a = mulmod(a, a, m);
+        e >>= 1;
+    }
+    return r;
+}
+bool prime64(uint64_t n) {
+    if (n < 2) return false;
+    static const uint64_t small[] = {2, 3, 5, 7, 11, 13, 17, 19, 23, 29, 31, 37};
+    for (uint64_t p : small) {
+        if (n % p == 0) return n == p;
+    }
+    uint64_t d = n - 1;
+    int s = 0;
+    while ((d & 1) == 0) {
+        d >>= 1;
+        ++s;
+    }
+    for (uint64_t a : small) {
+        uint64_t x = powmod(a, d, n);
+        if (x == 1 || x == n - 1) continue;
+        bool comp = true;
+        for (int r = 1; r < s; ++r) {
+            x = mulmod(x, x, n);
+            if (x == n - 1) {
+                comp = false;
+                break;
+            }
+        }
+        if (comp) return false;
+    }
+    return true;
+}
+
+// Philox4x32-10 (Salmon et al., SC'11), host copy for the multiplier draw.
+void philox(uint32_t c[4], uint32_t k0, uint32_t k1) {
+    for (int r = 0; r < 10; ++r) {
+        if (r) {
+            k0 += 0x9E3779B9u;
+            k1 += 0xBB67AE85u;
+        }
+        const uint64_t p0 = (uint64_t)0xD2511F53u * c[0];
+        const uint64_t p1 = (uint64_t)0xCD9E8D57u * c[2];
+        const uint32_t n0 = (uint32_t)(p1 >> 32) ^ c[1] ^ k0;
+        const uint32_t n2 = (uint32_t)(p0 >> 32) ^ c[3] ^ k1;
+        c[1] = (uint32_t)p1;
+        c[3] = (uint32_t)p0;
+        c[0] = n0;
+        c[2] = n2;
+    }
+}
+
+uint64_t layer_multiplier(uint64_t seed, uint32_t j, uint32_t vc) {
+    uint32_t c[4] = {j, 0u, 0u, 2u};
+    philox(c, (uint32_t)seed, (uint32_t)(seed >> 32));
+    const uint64_t r = (uint64_t)c[0] | ((uint64_t)c[1] << 32);
+    uint64_t half = (UINT64_MAX / vc) / 2;
+    if (half == 0) half = 1;
+    return 2 * (r % half) + 1;
+}
+
+}  // namespace
+
+struct LayerState {
+    std::vector<uint64_t> mult;    // [nb][4]
+    std::vector<uint64_t> prime;   // [nb]
+    std::vector<uint64_t> offset;  // [nb]
+    uint64_t rows = 0;
+    bool bound = false;
+    engram_layer_weights w{};
+    CUtensorMap tm_wkv{};
+};
+
+struct engram_ctx {
+    engram_ctx_desc desc{};
+    std::vector<uint64_t> seeds, bases;
+    std::vector<uint32_t> map;
+    int nb = 0, K = 0, N = 0;
+    std::vector<LayerState> layers;
+    uint32_t* d_err = nullptr;
+    int device = -1;
+    long long wait_limit_ns = 4000000000LL;
+};
+
+struct engram_session {
+    const engram_ctx* ctx;
+    uint32_t hist[3];  // c_{t-1}, c_{t-2}, c_{t-3} of the next position
+    uint64_t count;
+    uint32_t magic;
+};
+
+namespace {
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+engram_status check_layer(const engram_ctx* ctx, int layer, bool need_bound) {
+    if (!ctx) return fail(ENGRAM_EINVAL, "null context");
+    if (layer < 0 || layer >= (int)ctx->layers.size()) return fail(ENGRAM_EINVAL, "layer out of range");
+    if (need_bound && !ctx->layers[layer].bound)
+        return fail(ENGRAM_ESTATE, "layer weights not bound (engram_layer_bind)");
+    return ENGRAM_OK;
+}
+
+engram_status check_T(int64_t T) {
+    if (T < 0 || T > (int64_t)1 << 24) return fail(ENGRAM_EINVAL, "T must be in [0, 2^24]");
+    return ENGRAM_OK;
+}
+
+HashParams hash_params(const engram_ctx* ctx, int layer) {
+    HashParams hp{};
+    const LayerState& L = ctx->layers[layer];
+    for (int b = 0; b < ctx->nb; ++b) {
+        for (int j = 0; j < 4; ++j) hp.mult[b][j] = L.mult[b * 4 + j];
+        hp.prime[b] = L.prime[b];
+        hp.offset[b] = L.offset[b];
+    }
+    hp.nb = ctx->nb;
+    hp.heads = (int)ctx->desc.heads;
+    hp.min_n = (int)ctx->desc.min_n;
+    return hp;
+}
+
+Geometry geometry(const engram_ctx* ctx) {
+    Geometry g{};
+    g.nb = ctx->nb;
+    g.heads = (int)ctx->desc.heads;
+    g.min_n = (int)ctx->desc.min_n;
+    g.row_dim = (int)ctx->desc.row_dim;
+    g.K = ctx->K;
+    g.N = ctx->N;
+    g.hc = (int)ctx->desc.hc;
+    g.d = (int)ctx->desc.d;
+    g.eps = (float)ctx->desc.eps;
+    return g;
+}
+
+MmaArgs mma_args(const engram_ctx* ctx, int layer, int64_t T) {
+    MmaArgs a{};
+    const LayerState& L = ctx->layers[layer];
+    a.T = T;
+    a.K = ctx->K;
+    a.m_blocks = (int)((T + kBM - 1) / kBM);
+    a.group_m = 16;
+    a.hc = (int)ctx->desc.hc;
+    a.d = (int)ctx->desc.d;
+    a.eps = (float)ctx->desc.eps;
+    a.err = ctx->d_err;
+    a.wait_limit_ns = ctx->wait_limit_ns;
+    a.table = L.w.table;
+    a.scales = L.w.scales;
+    a.rows = L.rows;
+    a.row_dim = (int)ctx->desc.row_dim;
+    a.wq = L.w.wq;
+    a.wk = L.w.wk;
+    a.hp = hash_params(ctx, layer);
+    return a;
+}
+
+}  // namespace
+
+extern "C" {
+
+engram_status engram_ctx_create(const engram_ctx_desc* desc, const uint32_t* token_map,
+                                engram_ctx** out) {
+    if (!desc || !token_map || !out) return fail(ENGRAM_EINVAL, "null argument");
+    *out = nullptr;
+    const engram_ctx_desc& d = *desc;
+    if (d.vocab == 0 || d.vc == 0 || d.vc == 0xFFFFFFFFu) return fail(ENGRAM_EINVAL, "vocab / vc");
+    if (d.min_n < 1 || d.max_n < d.min_n || d.max_n > 4) return fail(ENGRAM_EINVAL, "n-gram orders");
+    if (d.heads < 1 || d.heads > 8) return fail(ENGRAM_EINVAL, "heads must be 1..8");
+    if (!(d.row_dim == 32 || d.row_dim == 64 || d.row_dim == 128 || d.row_dim == 256))
+        return fail(ENGRAM_EINVAL, "row_dim must be 32, 64, 128 or 256");
+    if (d.hc < 1 || d.hc > 8) return fail(ENGRAM_EINVAL, "hc must be 1..8");
+    if (d.d == 0 || d.d % kBN != 0) return fail(ENGRAM_EINVAL, "d must be a positive multiple of 256");
+    if (d.pad_cid >= d.vc) return fail(ENGRAM_EINVAL, "pad_cid must be < vc");
+    if (d.n_layers < 1 || d.n_layers > 16 || !d.layer_seeds || !d.bucket_bases)
+        return fail(ENGRAM_EINVAL, "n_layers must be 1..16 with seeds and bucket bases");
+    if (!(d.eps >= 0.0)) return fail(ENGRAM_EINVAL, "eps");
+    const int nb = (int)((d.max_n - d.min_n + 1) * d.heads);
+    const int K = nb * (int)d.row_dim;
+    if (K % kBK != 0) return fail(ENGRAM_EINVAL, "nb * row_dim must be a multiple of 64");
+    for (uint32_t v = 0; v < d.vocab; ++v)
+        if (token_map[v] >= d.vc) return fail(ENGRAM_EINVAL, "token map value >= vc");
+
+    engram_ctx* ctx = new (std::nothrow) engram_ctx;
+    if (!ctx) return fail(ENGRAM_ENOMEM, "host allocation");
+    try {
+        ctx->desc = d;
+        ctx->desc.layer_seeds = nullptr;
+        ctx->desc.bucket_bases = nullptr;
+        ctx->seeds.assign(d.layer_seeds, d.layer_seeds + d.n_layers);
+        ctx->bases.assign(d.bucket_bases, d.bucket_bases + d.n_layers);
+        ctx->map.assign(token_map, token_map + d.vocab);
+        ctx->nb = nb;
+        ctx->K = K;
+        ctx->N = (int)((d.hc + 1) * d.d);
+        ctx->layers.resize(d.n_layers);
+        // primes: layer by layer, bucket by bucket, strictly increasing above
+        // the layer's base and never reused by a later layer
+        std::vector<uint64_t> used;
+        for (uint32_t l = 0; l < d.n_layers; ++l) {
+            LayerState& L = ctx->layers[l];
+            L.mult.resize((size_t)nb * 4);
+            L.prime.resize(nb);
+            L.offset.resize(nb);
+            uint64_t cand = ctx->bases[l], sum = 0;
+            for (int b = 0; b < nb; ++b) {
+                do {
+                    ++cand;
+                } while (!prime64(cand) || std::find(used.begin(), used.end(), cand) != used.end());
+                used.push_back(cand);
+                L.prime[b] = cand;
+                L.offset[b] = sum;
+                sum += cand;
+            }
+            L.rows = sum;
+            if (sum > 0xFFFFFFFFull) {
+                delete ctx;
+                return fail(ENGRAM_EUNSUPPORTED, "layer table above 2^32 - 1 rows");
+            }
+            for (int b = 0; b < nb; ++b)
+                for (uint32_t j = 0; j < 4; ++j)
+                    L.mult[(size_t)b * 4 + j] = j < d.max_n ? layer_multiplier(ctx->seeds[l], j, d.vc) : 0;
+        }
+    } catch (...) {
+        delete ctx;
+        return fail(ENGRAM_ENOMEM, "host allocation");
+    }
+    *out = ctx;
+    return ok();
+}
+
+engram_status engram_ctx_destroy(engram_ctx* ctx) {
+    if (!ctx) return fail(ENGRAM_EINVAL, "null context");
+    if (ctx->d_err) {
+        int cur = -1;
+        cudaGetDevice(&cur);
+        if (ctx->device >= 0) cudaSetDevice(ctx->device);
+        cudaFree(ctx->d_err);
+        if (cur >= 0) cudaSetDevice(cur);
+    }
+    delete ctx;
+    return ok();
+}
+
+engram_status engram_layer_params(const engram_ctx* ctx, int layer, uint64_t* mult,
+                                  uint64_t* prime, uint64_t* offset, uint64_t* rows) {
+    engram_status st = check_layer(ctx, layer, false);
+    if (st) return st;
+    const LayerState& L = ctx->layers[layer];
+    if (mult) memcpy(mult, L.mult.data(), L.mult.size() * sizeof(uint64_t));
+    if (prime) memcpy(prime, L.prime.data(), L.prime.size() * sizeof(uint64_t));
+    if (offset) memcpy(offset, L.offset.data(), L.offset.size() * sizeof(uint64_t));
+    if (rows) *rows = L.rows;
+    return ok();
+}
+
+engram_status engram_layer_set_multipliers(engram_ctx* ctx, int layer, const uint64_t* mult) {
+    engram_status st = check_layer(ctx, layer, false);
+    if (st) return st;
+    if (!mult) return fail(ENGRAM_EINVAL, "null multiplier table");
+    std::copy(mult, mult + ctx->nb * 4, ctx->layers[layer].mult.begin());
+    return ok();
+}
+
+engram_status engram_layer_bind(engram_ctx* ctx, int layer, const engram_layer_weights* w) {
+    engram_status st = check_layer(ctx, layer, false);
+    if (st) return st;
+    if (!w || !w->table || !w->scales || !w->wkv || !w->wq || !w->wk)
+        return fail(ENGRAM_EINVAL, "null weight pointer");
+    LayerState& L = ctx->layers[layer];
+    if (w->rows != L.rows) return fail(ENGRAM_EINVAL, "table rows differ from the layer's row count");
+    if (!aligned16(w->table) || !aligned16(w->scales) || !aligned16(w->wkv) || !aligned16(w->wq) ||
+        !aligned16(w->wk))
+        return fail(ENGRAM_EINVAL, "weights must be 16-byte aligned");
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (ctx->device >= 0 && ctx->device != dev)
+        return fail(ENGRAM_ESTATE, "context already bound on another device");
+    // The table may live in pinned host memory read through UVA.
+    engram_layer_weights bw = *w;
+    for (const uint8_t** p : {&bw.table, &bw.scales}) {
+        cudaPointerAttributes attr{};
+        e = cudaPointerGetAttributes(&attr, *p);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return fail(ENGRAM_EINVAL, "table pointer is neither device nor registered host memory");
+        }
+        if (attr.type == cudaMemoryTypeHost) {
+            if (!attr.devicePointer)
+                return fail(ENGRAM_EUNSUPPORTED, "host table not mapped into the device address space");
+            *p = static_cast<const uint8_t*>(attr.devicePointer);
+        } else if (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged) {
+            return fail(ENGRAM_EINVAL, "table pointer must be device or pinned host memory");
+        }
+    }
+    if (!ctx->d_err) {
+        e = cudaMalloc(&ctx->d_err, sizeof(uint32_t));
+        if (e != cudaSuccess) return fail(ENGRAM_ENOMEM, "cudaMalloc of the error word");
+        e = cudaMemset(ctx->d_err, 0, sizeof(uint32_t));
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemset");
+        ctx->device = dev;
+    }
+    CUtensorMap tm;
+    e = make_tma_bf16(&tm, w->wkv, (uint64_t)ctx->N, (uint64_t)ctx->K, kBN);
+    if (e != cudaSuccess) return cuda_fail(e, "wkv tensor map");
+    L.w = bw;
+    L.tm_wkv = tm;
+    L.bound = true;
+    return ok();
+}
+
+engram_status engram_table_fill(const engram_ctx* ctx, uint64_t seed, uint8_t* data,
+                                uint8_t* scale, uint64_t row_begin, uint64_t row_end,
+                                void* stream) {
+    if (!ctx || !data || !scale) return fail(ENGRAM_EINVAL, "null argument");
+    if (row_end < row_begin) return fail(ENGRAM_EINVAL, "row_end < row_begin");
+    if (!aligned16(data)) return fail(ENGRAM_EINVAL, "data must be 16-byte aligned");
+    cudaError_t e = launch_table_fill(seed, data, scale, row_begin, row_end,
+                                      (int)ctx->desc.row_dim, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "table fill launch");
+    return ok();
+}
+
+// ---- sessions ---------------------------------------------------------------------------
+
+engram_status engram_session_create(engram_ctx* ctx, engram_session** out) {
+    if (!ctx || !out) return fail(ENGRAM_EINVAL, "null argument");
+    engram_session* s = new (std::nothrow) engram_session;
+    if (!s) return fail(ENGRAM_ENOMEM, "host allocation");
+    s->ctx = ctx;
+    s->hist[0] = s->hist[1] = s->hist[2] = ctx->desc.pad_cid;
+    s->count = 0;
+    s->magic = kSessionMagic;
+    *out = s;
+    return ok();
+}
+
+static engram_status check_session(const engram_session* s) {
+    if (!s) return fail(ENGRAM_EINVAL, "null session");
+    if (s->magic != kSessionMagic) return fail(ENGRAM_ESTATE, "destroyed or invalid session");
+    return ENGRAM_OK;
+}
+
+engram_status engram_session_fork(const engram_session* s, engram_session** out) {
+    engram_status st = check_session(s);
+    if (st) return st;
+    if (!out) return fail(ENGRAM_EINVAL, "null argument");
+    engram_session* c = new (std::nothrow) engram_session(*s);
+    if (!c) return fail(ENGRAM_ENOMEM, "host allocation");
+    *out = c;
+    return ok();
+}
+
+engram_status engram_session_reset(engram_session* s) {
+    engram_status st = check_session(s);
+    if (st) return st;
+    s->hist[0] = s->hist[1] = s->hist[2] = s->ctx->desc.pad_cid;
+    s->count = 0;
+    return ok();
+}
+
+engram_status engram_session_destroy(engram_session* s) {
+    engram_status st = check_session(s);
+    if (st) return st;
+    s->magic = 0;
+    delete s;
+    return ok();
+}
+
+static inline void push(engram_session* s, uint32_t c, uint32_t* w) {
+    w[0] = c;
+    w[1] = s->hist[0];
+    w[2] = s->hist[1];
+    w[3] = s->hist[2];
+    s->hist[2] = s->hist[1];
+    s->hist[1] = s->hist[0];
+    s->hist[0] = c;
+    ++s->count;
+}
+
+engram_status engram_session_append(engram_session* s, const int32_t* tokens,
+                                    const uint8_t* is_image, int64_t n, uint32_t* windows_out) {
+    engram_status st = check_session(s);
+    if (st) return st;
+    if (n < 0) return fail(ENGRAM_EINVAL, "n < 0");
+    if (n == 0) return ok();
+    if (!tokens || !windows_out) return fail(ENGRAM_EINVAL, "null argument");
+    const engram_ctx* ctx = s->ctx;
+    for (int64_t i = 0; i < n; ++i) {
+        if (is_image && is_image[i]) continue;
+        if (tokens[i] < 0 || (uint32_t)tokens[i] >= ctx->desc.vocab)
+            return fail(ENGRAM_EINVAL, "token id outside [0, vocab) at position " + std::to_string(i));
+    }
+    for (int64_t i = 0; i < n; ++i) {
+        const uint32_t c = (is_image && is_image[i]) ? ENGRAM_DEAD : ctx->map[(uint32_t)tokens[i]];
+        push(s, c, windows_out + 4 * i);
+    }
+    return ok();
+}
+
+engram_status engram_batch_append(engram_session* const* sessions, const int32_t* tokens,
+                                  const uint8_t* is_image, int64_t n, uint32_t* windows_out) {
+    if (n < 0) return fail(ENGRAM_EINVAL, "n < 0");
+    if (n == 0) return ok();
+    if (!sessions || !tokens || !windows_out) return fail(ENGRAM_EINVAL, "null argument");
+    for (int64_t i = 0; i < n; ++i) {
+        engram_status st = check_session(sessions[i]);
+        if (st) return st;
+        if (i > 0 && sessions[i]->ctx != sessions[0]->ctx)
+            return fail(ENGRAM_EINVAL, "sessions of different contexts");
+        if (is_image && is_image[i]) continue;
+        if (tokens[i] < 0 || (uint32_t)tokens[i] >= sessions[i]->ctx->desc.vocab)
+            return fail(ENGRAM_EINVAL, "token id outside [0, vocab) at position " + std::to_string(i));
+    }
+    for (int64_t i = 0; i < n; ++i) {
+        const engram_ctx* ctx = sessions[i]->ctx;
+        const uint32_t c = (is_image && is_image[i]) ? ENGRAM_DEAD : ctx->map[(uint32_t)tokens[i]];
+        push(sessions[i], c, windows_out + 4 * i);
+    }
+    return ok();
+}
+
+// ---- device steps ---------------------------------------------------------------------
+
+size_t engram_workspace_bytes(const engram_ctx* ctx, int64_t T) {
+    if (!ctx || T <= 0) return 0;
+    const size_t P = ctx->desc.d / kBN;
+    const size_t bytes = (size_t)T * ctx->desc.hc * P * 3 * sizeof(float);
+    return (bytes + 255) & ~(size_t)255;
+}
+
+engram_status engram_hash(const engram_ctx* ctx, int layer, const uint32_t* d_windows, int64_t T,
+                          uint32_t* d_rows, void* stream) {
+    engram_status st = check_layer(ctx, layer, false);
+    if (st || (st = check_T(T))) return st;
+    if (T == 0) return ok();
+    if (!d_windows || !d_rows || !aligned16(d_windows)) return fail(ENGRAM_EINVAL, "windows / rows");
+    cudaError_t e = launch_hash(hash_params(ctx, layer), reinterpret_cast<const uint4*>(d_windows), T,
+                                d_rows, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "hash launch");
+    return ok();
+}
+
+engram_status engram_gather_dequant(const engram_ctx* ctx, int layer, const uint32_t* d_rows,
+                                    int64_t T, uint16_t* d_emb, void* stream) {
+    engram_status st = check_layer(ctx, layer, true);
+    if (st || (st = check_T(T))) return st;
+    if (T == 0) return ok();
+    if (!d_rows || !d_emb || !aligned16(d_emb)) return fail(ENGRAM_EINVAL, "rows / emb");
+    const LayerState& L = ctx->layers[layer];
+    cudaError_t e = launch_gather(geometry(ctx), d_rows, T, L.w.table, L.w.scales, L.rows, d_emb,
+                                  ctx->d_err, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "gather launch");
+    return ok();
+}
+
+engram_status engram_project(const engram_ctx* ctx, int layer, const uint16_t* d_emb, int64_t T,
+                             float* d_kv, void* stream) {
+    engram_status st = check_layer(ctx, layer, true);
+    if (st || (st = check_T(T))) return st;
+    if (T == 0) return ok();
+    if (!d_emb || !d_kv || !aligned16(d_emb) || !aligned16(d_kv)) return fail(ENGRAM_EINVAL, "emb / kv");
+    CUtensorMap tmA;
+    cudaError_t e = make_tma_bf16(&tmA, d_emb, (uint64_t)T, (uint64_t)ctx->K, kBM);
+    if (e != cudaSuccess) return cuda_fail(e, "emb tensor map");
+    MmaArgs a = mma_args(ctx, layer, T);
+    a.n_tile_begin = 0;
+    a.n_tiles = ctx->N / kBN;
+    a.kv = d_kv;
+    a.ldkv = ctx->N;
+    e = launch_project(a, tmA, ctx->layers[layer].tm_wkv, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "project launch");
+    return ok();
+}
+
+engram_status engram_gate(const engram_ctx* ctx, int layer, const float* d_kv,
+                          const uint32_t* d_windows, int64_t T, uint16_t* d_hidden,
+                          float* d_gates, void* stream) {
+    engram_status st = check_layer(ctx, layer, true);
+    if (st || (st = check_T(T))) return st;
+    if (T == 0) return ok();
+    if (!d_kv || !d_windows || !d_hidden || !aligned16(d_windows))
+        return fail(ENGRAM_EINVAL, "kv / windows / hidden");
+    const LayerState& L = ctx->layers[layer];
+    cudaError_t e = launch_gate(geometry(ctx), d_kv, reinterpret_cast<const uint4*>(d_windows), T,
+                                d_hidden, L.w.wq, L.w.wk, d_gates, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "gate launch");
+    return ok();
+}
+
+engram_status engram_forward(const engram_ctx* ctx, int layer, const uint32_t* d_windows,
+                             int64_t T, uint16_t* d_hidden, void* d_workspace, float* d_gates,
+                             void* stream) {
+    engram_status st = check_layer(ctx, layer, true);
+    if (st || (st = check_T(T))) return st;
+    if (T == 0) return ok();
+    if (!d_windows || !d_hidden || !d_workspace || !aligned16(d_windows) || !aligned16(d_hidden) ||
+        !aligned16(d_workspace))
+        return fail(ENGRAM_EINVAL, "windows / hidden / workspace (16-byte aligned)");
+    const LayerState& L = ctx->layers[layer];
+    MmaArgs a = mma_args(ctx, layer, T);
+    a.windows = reinterpret_cast<const uint4*>(d_windows);
+    a.hidden = d_hidden;
+    a.partials = static_cast<float*>(d_workspace);
+    a.gates = d_gates;
+    const int key_tiles = (int)(ctx->desc.hc * ctx->desc.d / kBN);
+    const int value_tiles = (int)(ctx->desc.d / kBN);
+    // key tiles: per-(token, branch, tile) sums; stream order then makes every
+    // sum visible to the value tiles, which gate and update hidden.
+    a.n_tile_begin = 0;
+    a.n_tiles = key_tiles;
+    cudaError_t e = launch_forward_phase(a, kEpiKeyPartial, L.tm_wkv, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "forward key-phase launch");
+    a.n_tile_begin = key_tiles;
+    a.n_tiles = value_tiles;
+    e = launch_forward_phase(a, kEpiValueUpdate, L.tm_wkv, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "forward value-phase launch");
+    return ok();
+}
+
+engram_status engram_project_windows(const engram_ctx* ctx, int layer, const uint32_t* d_windows,
+                                     int64_t T, float* d_kv, void* stream) {
+    engram_status st = check_layer(ctx, layer, true);
+    if (st || (st = check_T(T))) return st;
+    if (T == 0) return ok();
+    if (!d_windows || !d_kv || !aligned16(d_windows) || !aligned16(d_kv))
+        return fail(ENGRAM_EINVAL, "windows / kv (16-byte aligned)");
+    MmaArgs a = mma_args(ctx, layer, T);
+    a.windows = reinterpret_cast<const uint4*>(d_windows);
+    a.kv = d_kv;
+    a.ldkv = ctx->N;
+    a.n_tile_begin = 0;
+    a.n_tiles = ctx->N / kBN;
+    cudaError_t e = launch_forward_phase(a, kEpiStoreKv, ctx->layers[layer].tm_wkv,
+                                         (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "fused projection launch");
+    return ok();
+}
+
+engram_status engram_sync(const engram_ctx* ctx, void* stream) {
+    if (!ctx) return fail(ENGRAM_EINVAL, "null context");
+    cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "asynchronous error");
+    if (ctx->d_err) {
+        uint32_t w = 0;
+        e = cudaMemcpy(&w, ctx->d_err, sizeof w, cudaMemcpyDeviceToHost);
+        if (e != cudaSuccess) return cuda_fail(e, "error word read");
+        if (w) {
+            cudaMemset(ctx->d_err, 0, sizeof(uint32_t));
+            if (w & kErrTimeout) return fail(ENGRAM_ETIMEOUT, "a kernel gave up a bounded wait");
+            return fail(ENGRAM_EBOUNDS, "a kernel met a row index outside the table");
+        }
+    }
+    return ok();
+}
+
+const char* engram_last_error(void) { return g_last_error.c_str(); }
+
+}  // extern "C"

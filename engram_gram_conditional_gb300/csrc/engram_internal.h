@@ -1,0 +1,99 @@
+// Internal declarations shared by the host API (engram_api.cpp) and the CUDA
+// kernels (kernels_misc.cu, kernels_mma.cu) of libengram.so.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace engram {
+
+constexpr uint32_t kDead = 0xFFFFFFFFu;
+constexpr uint32_t kMasked = 0xFFFFFFFFu;
+constexpr int kMaxBuckets = 32;  // (max_n - min_n + 1) <= 4 orders x heads <= 8
+
+// Device error word bits.
+constexpr uint32_t kErrBounds = 1u;   // a row index >= rows was met
+constexpr uint32_t kErrTimeout = 2u;  // a bounded wait gave up
+
+// Hash parameters of one layer, passed to kernels by value.
+struct HashParams {
+    uint64_t mult[kMaxBuckets][4];
+    uint64_t prime[kMaxBuckets];
+    uint64_t offset[kMaxBuckets];
+    int nb;
+    int heads;
+    int min_n;
+    int pad_;
+};
+
+// Layer geometry as the kernels see it.
+struct Geometry {
+    int nb, heads, min_n, row_dim;
+    int K, N, hc, d;
+    float eps;
+};
+
+// Tile shape of the tcgen05 kernels.
+constexpr int kBM = 128;  // tokens per tile (TMEM lanes)
+constexpr int kBN = 256;  // outputs per tile (TMEM columns per accumulator)
+constexpr int kBK = 64;   // reduction slice per pipeline stage (128-byte rows)
+
+enum EpilogueMode : int {
+    kEpiStoreKv = 0,   // write kv fp32
+    kEpiKeyPartial = 1,  // key tiles: per-(token, branch, tile) sums
+    kEpiValueUpdate = 2  // value tiles: gates from the sums, hidden += g v
+};
+
+struct MmaArgs {
+    int64_t T;
+    int K;
+    int n_tile_begin;  // first N tile (of kBN) of this launch
+    int n_tiles;       // N tiles of this launch
+    int m_blocks;      // ceil(T / kBM)
+    int group_m;       // tile rasterisation: M blocks per group
+    int hc, d;
+    float eps;
+    uint32_t* err;
+    long long wait_limit_ns;
+    // fused operand A
+    const uint4* windows;
+    const uint8_t* table;
+    const uint8_t* scales;
+    uint64_t rows;
+    int row_dim;
+    // epilogue
+    float* kv;             // kEpiStoreKv: [T][ldkv]
+    int64_t ldkv;
+    uint16_t* hidden;      // [T][hc][d]
+    const float* wq;       // [hc][d]
+    const float* wk;       // [hc][d]
+    float* partials;       // [T][hc][d / kBN][3]
+    float* gates;          // [T][hc] or null
+    HashParams hp;
+};
+
+// kernels_misc.cu
+cudaError_t launch_table_fill(uint64_t seed, uint8_t* data, uint8_t* scale, uint64_t row_begin,
+                              uint64_t row_end, int row_dim, cudaStream_t s);
+cudaError_t launch_hash(const HashParams& hp, const uint4* windows, int64_t T, uint32_t* rows,
+                        cudaStream_t s);
+cudaError_t launch_gather(const Geometry& g, const uint32_t* rows, int64_t T,
+                          const uint8_t* table, const uint8_t* scales, uint64_t nrows,
+                          uint16_t* emb, uint32_t* err, cudaStream_t s);
+cudaError_t launch_gate(const Geometry& g, const float* kv, const uint4* windows, int64_t T,
+                        uint16_t* hidden, const float* wq, const float* wk, float* gates,
+                        cudaStream_t s);
+
+// kernels_mma.cu
+// Host-side TMA descriptor for a row-major bf16 matrix [rows][cols] with a
+// (kBK x box_rows) box and 128-byte swizzle.
+cudaError_t make_tma_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                          uint32_t box_rows);
+cudaError_t launch_project(const MmaArgs& a, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                           cudaStream_t s);
+cudaError_t launch_forward_phase(const MmaArgs& a, int mode, const CUtensorMap& tmB,
+                                 cudaStream_t s);
+int device_sm_count();
+
+}  // namespace engram

@@ -1,0 +1,242 @@
+// Table fill, hash, gather-dequant and the standalone gate (sm_103a).
+//
+// All four are bound by memory or latency, not arithmetic: grids are sized in
+// multiples of the SM count with grid-stride loops, loads and stores are 8- or
+// 16-byte vectors, and consecutive threads touch consecutive bytes.
+#include <algorithm>
+
+#include "device_common.cuh"
+
+namespace engram {
+
+namespace {
+
+int g_sm_count = 0;
+
+int sm_count() {
+    if (g_sm_count == 0) {
+        int dev = 0, n = 0;
+        if (cudaGetDevice(&dev) == cudaSuccess &&
+            cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0)
+            g_sm_count = n;
+        else
+            g_sm_count = 148;
+    }
+    return g_sm_count;
+}
+
+int grid_for(int64_t items, int threads, int per_sm) {
+    int64_t want = (items + threads - 1) / threads;
+    int64_t cap = (int64_t)sm_count() * per_sm;
+    return (int)std::max<int64_t>(1, std::min(want, cap));
+}
+
+// Philox4x32-10 (Salmon et al., SC'11).
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        if (r) {
+            k0 += 0x9E3779B9u;
+            k1 += 0xBB67AE85u;
+        }
+        const uint32_t lo0 = 0xD2511F53u * c.x, hi0 = __umulhi(0xD2511F53u, c.x);
+        const uint32_t lo1 = 0xCD9E8D57u * c.z, hi1 = __umulhi(0xCD9E8D57u, c.z);
+        c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+    }
+    return c;
+}
+
+__device__ __forceinline__ uint32_t lane16(const uint4& o, int lane) {
+    const uint32_t w = (lane >> 1) == 0 ? o.x : (lane >> 1) == 1 ? o.y : (lane >> 1) == 2 ? o.z : o.w;
+    return (lane & 1) ? (w >> 16) : (w & 0xFFFFu);
+}
+
+// Table contents: code(row, col) from Philox counter (row, col / 8, 0) lane
+// col % 8, uniform over the 254 finite E4M3 codes; scale(row, g) from counter
+// (row, 0, 1) lane g, E8M0 exponent uniform over 119..127.
+// One thread per (row, 8-column chunk); chunk 0 also writes the row's scales.
+__global__ void k_table_fill(uint64_t seed, uint8_t* __restrict__ data,
+                             uint8_t* __restrict__ scale, uint64_t row_begin, uint64_t nrows,
+                             int row_dim) {
+    const uint32_t k0 = (uint32_t)seed, k1 = (uint32_t)(seed >> 32);
+    const int cpr = row_dim / 8;
+    const int groups = row_dim / 32;
+    const uint64_t items = nrows * (uint64_t)cpr;
+    for (uint64_t i = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; i < items;
+         i += (uint64_t)gridDim.x * blockDim.x) {
+        const uint64_t row = row_begin + i / cpr;
+        const uint32_t chunk = (uint32_t)(i % cpr);
+        const uint4 o = philox4x32_10(make_uint4((uint32_t)row, (uint32_t)(row >> 32), chunk, 0u),
+                                      k0, k1);
+        uint32_t w[2] = {0u, 0u};
+#pragma unroll
+        for (int l = 0; l < 8; ++l) {
+            const uint32_t idx = (lane16(o, l) * 254u) >> 16;
+            const uint32_t code = idx < 127u ? idx : idx + 1u;
+            w[l >> 2] |= code << (8 * (l & 3));
+        }
+        *reinterpret_cast<uint2*>(data + row * (uint64_t)row_dim + chunk * 8u) = make_uint2(w[0], w[1]);
+        if (chunk == 0) {
+            const uint4 s = philox4x32_10(make_uint4((uint32_t)row, (uint32_t)(row >> 32), 0u, 1u),
+                                          k0, k1);
+            uint8_t* dst = scale + row * (uint64_t)groups;
+            for (int g = 0; g < groups; ++g) dst[g] = (uint8_t)(119u + ((lane16(s, g) * 9u) >> 16));
+        }
+    }
+}
+
+// a2: one thread per (token, bucket).
+__global__ void k_hash(const __grid_constant__ HashParams hp, const uint4* __restrict__ windows,
+                       int64_t T, uint32_t* __restrict__ rows) {
+    const int64_t items = T * hp.nb;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < items;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t t = i / hp.nb;
+        const int b = (int)(i - t * hp.nb);
+        rows[i] = hash_bucket(hp, windows[t], b);
+    }
+}
+
+// a3: one thread per 16 columns of one (token, bucket) row: a 16-byte load of
+// codes, one scale byte, two 16-byte stores of BF16.
+__global__ void k_gather(const uint32_t* __restrict__ rows, int64_t T, int nb, int row_dim,
+                         const uint8_t* __restrict__ table, const uint8_t* __restrict__ scales,
+                         uint64_t nrows, uint16_t* __restrict__ emb, uint32_t* err) {
+    const int cpr = row_dim / 16;
+    const int groups = row_dim / 32;
+    const int64_t items = T * nb * (int64_t)cpr;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < items;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t tb = i / cpr;  // token * nb + bucket
+        const int chunk = (int)(i - tb * cpr);
+        uint32_t row = rows[tb];
+        uint4 out0 = make_uint4(0, 0, 0, 0), out1 = out0;
+        if (row != kMasked && row >= nrows) {
+            atomicOr(err, kErrBounds);
+            row = kMasked;
+        }
+        if (row != kMasked) {
+            const uint4 c = __ldg(reinterpret_cast<const uint4*>(table + (uint64_t)row * row_dim) + chunk);
+            const float sf = e8m0_to_f32(__ldg(scales + (uint64_t)row * groups + chunk / 2));
+            out0 = decode8(c.x, c.y, sf);
+            out1 = decode8(c.z, c.w, sf);
+        }
+        uint4* dst = reinterpret_cast<uint4*>(emb + tb * (int64_t)row_dim) + chunk * 2;
+        dst[0] = out0;
+        dst[1] = out1;
+    }
+}
+
+// a5 standalone: one CTA per token.  Pass 1 reduces, per branch, sum k^2,
+// sum h^2 and sum h w_q w_k k; pass 2 applies hidden += g v with one BF16
+// rounding.  Image rows (c_t == DEAD) are left untouched.
+constexpr int kGateThreads = 256;
+
+__global__ void __launch_bounds__(kGateThreads)
+k_gate(const float* __restrict__ kv, const uint4* __restrict__ windows, int64_t T, int hc, int d,
+       float eps, uint16_t* __restrict__ hidden, const float* __restrict__ wq,
+       const float* __restrict__ wk, float* __restrict__ gates) {
+    __shared__ float red[kGateThreads / 32][8][3];
+    __shared__ float gsh[8];
+    const int N = (hc + 1) * d;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    for (int64_t t = blockIdx.x; t < T; t += gridDim.x) {
+        const bool image = windows[t].x == kDead;
+        if (image) {
+            if (gates && threadIdx.x < hc) gates[t * hc + threadIdx.x] = 0.0f;
+            continue;
+        }
+        const float* kvt = kv + t * (int64_t)N;
+        uint16_t* ht = hidden + t * (int64_t)hc * d;
+        for (int b = 0; b < hc; ++b) {
+            float skk = 0.f, shh = 0.f, shk = 0.f;
+            for (int i = threadIdx.x; i < d; i += kGateThreads) {
+                const float k = kvt[(int64_t)b * d + i];
+                const float h = __uint_as_float((uint32_t)ht[(int64_t)b * d + i] << 16);
+                skk += k * k;
+                shh += h * h;
+                shk += h * wq[b * d + i] * wk[b * d + i] * k;
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                skk += __shfl_xor_sync(0xFFFFFFFFu, skk, o);
+                shh += __shfl_xor_sync(0xFFFFFFFFu, shh, o);
+                shk += __shfl_xor_sync(0xFFFFFFFFu, shk, o);
+            }
+            if (lane == 0) {
+                red[warp][b][0] = skk;
+                red[warp][b][1] = shh;
+                red[warp][b][2] = shk;
+            }
+        }
+        __syncthreads();
+        if (threadIdx.x < hc) {
+            const int b = threadIdx.x;
+            float skk = 0.f, shh = 0.f, shk = 0.f;
+            for (int w = 0; w < kGateThreads / 32; ++w) {
+                skk += red[w][b][0];
+                shh += red[w][b][1];
+                shk += red[w][b][2];
+            }
+            const float g = gate_from_sums(skk, shh, shk, d, eps);
+            gsh[b] = g;
+            if (gates) gates[t * hc + b] = g;
+        }
+        __syncthreads();
+        const float* v = kvt + (int64_t)hc * d;
+        for (int i = threadIdx.x; i < d; i += kGateThreads) {
+            const float vi = v[i];
+            for (int b = 0; b < hc; ++b) {
+                const float h = __uint_as_float((uint32_t)ht[(int64_t)b * d + i] << 16);
+                const float o = h + gsh[b] * vi;
+                ht[(int64_t)b * d + i] = __bfloat16_as_ushort(__float2bfloat16_rn(o));
+            }
+        }
+        __syncthreads();
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_table_fill(uint64_t seed, uint8_t* data, uint8_t* scale, uint64_t row_begin,
+                              uint64_t row_end, int row_dim, cudaStream_t s) {
+    const uint64_t nrows = row_end - row_begin;
+    if (nrows == 0) return cudaSuccess;
+    const int threads = 256;
+    const int grid = grid_for((int64_t)std::min<uint64_t>(nrows * (row_dim / 8), 1ull << 40),
+                              threads, 16);
+    k_table_fill<<<grid, threads, 0, s>>>(seed, data, scale, row_begin, nrows, row_dim);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_hash(const HashParams& hp, const uint4* windows, int64_t T, uint32_t* rows,
+                        cudaStream_t s) {
+    if (T == 0) return cudaSuccess;
+    const int threads = 256;
+    k_hash<<<grid_for(T * hp.nb, threads, 8), threads, 0, s>>>(hp, windows, T, rows);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gather(const Geometry& g, const uint32_t* rows, int64_t T,
+                          const uint8_t* table, const uint8_t* scales, uint64_t nrows,
+                          uint16_t* emb, uint32_t* err, cudaStream_t s) {
+    if (T == 0) return cudaSuccess;
+    const int threads = 256;
+    const int64_t items = T * g.nb * (int64_t)(g.row_dim / 16);
+    k_gather<<<grid_for(items, threads, 16), threads, 0, s>>>(rows, T, g.nb, g.row_dim, table,
+                                                              scales, nrows, emb, err);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gate(const Geometry& g, const float* kv, const uint4* windows, int64_t T,
+                        uint16_t* hidden, const float* wq, const float* wk, float* gates,
+                        cudaStream_t s) {
+    if (T == 0) return cudaSuccess;
+    const int grid = (int)std::min<int64_t>(T, (int64_t)sm_count() * 8);
+    k_gate<<<grid, kGateThreads, 0, s>>>(kv, windows, T, g.hc, g.d, g.eps, hidden, wq, wk, gates);
+    return cudaGetLastError();
+}
+
+int device_sm_count() { return sm_count(); }
+
+}  // namespace engram

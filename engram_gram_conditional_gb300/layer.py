@@ -1,0 +1,77 @@
+"""Device memory plumbing for a set of Engram layers.
+
+PyTorch allocates the buffers (device HBM, or pinned host memory for a table
+read through UVA); the library fills the tables on the device and binds the
+weights.  No forward arithmetic happens here.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from . import (engram_ctx_create, engram_ctx_destroy, engram_layer_bind, engram_layer_params,
+               engram_table_fill)
+
+
+def _round16(n: int) -> int:
+    return (n + 15) // 16 * 16
+
+
+def _as_device(x, dtype, device):
+    if isinstance(x, torch.Tensor):
+        return x.to(device=device, dtype=dtype).contiguous()
+    return torch.from_numpy(np.ascontiguousarray(x)).view(dtype).to(device)
+
+
+class EngramLayerSet:
+    """One context (geometry, token map, hash parameters) and its layers' weights."""
+
+    def __init__(self, vocab, vc, token_map, layer_seeds, bucket_bases, *, min_n=2, max_n=4,
+                 heads=8, row_dim=256, hc=4, d=5120, pad_cid=0, eps=1e-6, device="cuda"):
+        self.device = torch.device(device)
+        self.geom = dict(vocab=vocab, vc=vc, min_n=min_n, max_n=max_n, heads=heads,
+                         row_dim=row_dim, hc=hc, d=d, pad_cid=pad_cid, eps=eps)
+        self.nb = (max_n - min_n + 1) * heads
+        self.K = self.nb * row_dim
+        self.N = (hc + 1) * d
+        self.ctx = engram_ctx_create(vocab, vc, token_map, layer_seeds, bucket_bases, min_n=min_n,
+                                     max_n=max_n, heads=heads, row_dim=row_dim, hc=hc, d=d,
+                                     pad_cid=pad_cid, eps=eps)
+        self.n_layers = len(layer_seeds)
+        self.params = [engram_layer_params(self.ctx, l, self.nb) for l in range(self.n_layers)]
+        self.tensors = [dict() for _ in range(self.n_layers)]
+
+    @classmethod
+    def from_workload(cls, w, token_map, device="cuda"):
+        return cls(w.vocab, w.vc, token_map, w.hash_seeds, w.bucket_bases, min_n=w.min_n,
+                   max_n=w.max_n, heads=w.heads, row_dim=w.row_dim, hc=w.hc, d=w.d,
+                   pad_cid=w.pad_cid, eps=w.eps, device=device)
+
+    def rows(self, layer: int) -> int:
+        return self.params[layer][3]
+
+    def bind(self, layer: int, table_seed: int, wkv, wq, wk, host_table: bool = False,
+             stream=None):
+        """Allocate and fill the layer's MXFP8 table, upload wkv / w_q / w_k, bind."""
+        rows = self.rows(layer)
+        rd = self.geom["row_dim"]
+        if host_table:
+            table = torch.empty(_round16(rows * rd), dtype=torch.uint8, pin_memory=True)
+            scales = torch.empty(_round16(rows * rd // 32), dtype=torch.uint8, pin_memory=True)
+        else:
+            table = torch.empty(_round16(rows * rd), dtype=torch.uint8, device=self.device)
+            scales = torch.empty(_round16(rows * rd // 32), dtype=torch.uint8, device=self.device)
+        engram_table_fill(self.ctx, table_seed, table, scales, 0, rows, stream)
+        d_wkv = _as_device(wkv, torch.int16, self.device).view(self.N, self.K)
+        d_wq = _as_device(wq, torch.float32, self.device).view(-1)
+        d_wk = _as_device(wk, torch.float32, self.device).view(-1)
+        engram_layer_bind(self.ctx, layer, table, scales, rows, d_wkv, d_wq, d_wk)
+        self.tensors[layer] = dict(table=table, scales=scales, wkv=d_wkv, wq=d_wq, wk=d_wk,
+                                   table_seed=table_seed)
+        return self.tensors[layer]
+
+    def close(self):
+        if self.ctx is not None:
+            engram_ctx_destroy(self.ctx)
+            self.ctx = None
+        self.tensors = []

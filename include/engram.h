@@ -1,0 +1,212 @@
+/*
+ * engram.h - C ABI of the Engram per-layer forward step on one GB300 GPU.
+ *
+ * The Engram layer (conditional memory of DeepSeek V4.1 Flash) injects, at the
+ * entry of layers 1 and 14, a gated value read from a huge n-gram table:
+ *
+ *   tokens --append--> windows (c_t, c_{t-1}, c_{t-2}, c_{t-3})
+ *          --hash----> 24 row numbers (2/3/4-gram x 8 heads, each head its own
+ *                      prime-sized bucket range of the layer table)
+ *          --gather--> 24 MXFP8 rows of 256 values (E4M3 + one E8M0 per 32),
+ *                      dequantised to BF16 and concatenated: a 6,144-vector
+ *          --project-> kv = wkv e, wkv BF16 [25,600 x 6,144]: one 5,120-wide
+ *                      key per hyper-connection branch and one shared value
+ *          --gate----> per branch: hidden += sigmoid(copysign(sqrt(max(|dot|,
+ *                      1e-6)), dot)) * value, dot = <n(h) w_q, n(k) w_k>/sqrt(d)
+ *
+ * Sources (page title, section):
+ *   "DeepSeek V4.1 Flash 的 Engram" (zhuai.tech): "把知识变成可寻址的向量"
+ *     (geometry), "第一步" (token map, windows, 24 hashes), "第二步" (MXFP8
+ *     rows, wkv), "第三步" (gate), "第四步" (append once; fork/reset; DEAD).
+ *   "3.84 亿行 Embedding 的存法大揭秘" (lqnn.cn): row counts, group-32 UE8M0
+ *     scales, the value is the last 5,120 rows of wkv.
+ *   vLLM "Engram" feature wiki, "동작 방식 (How it works)": multiply-XOR hash
+ *     per (order, head) into its own prime bucket range; one key per branch
+ *     and a shared value; masked positions pass through.
+ *
+ * Conventions for every call:
+ *  - Every call returns an engram_status.  Arguments are validated before any
+ *    launch; on an error nothing is launched and no state changes.
+ *    engram_last_error() returns a thread-local message for the last error.
+ *  - The caller owns every device and pinned-host buffer and every stream and
+ *    the library never frees them.  The library owns engram_ctx, the sessions,
+ *    the per-layer hash parameters and one 4-byte device error word per
+ *    context (allocated at the first engram_layer_bind).
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *    Device calls are asynchronous on that stream.  Faults found by a kernel
+ *    (a row index outside the table, a wait that ran out) set the context's
+ *    device error word; engram_sync() synchronises the stream, reads and
+ *    clears that word and reports it.  The library never aborts, traps or
+ *    prints.
+ *  - BF16 values are passed as uint16_t bit patterns.
+ *  - Layout of the per-layer tensors (T tokens, nb = (max_n-min_n+1) * heads
+ *    buckets, K = nb * row_dim, N = (hc + 1) * d):
+ *      windows   uint32 [T][4]         (c_t, c_{t-1}, c_{t-2}, c_{t-3})
+ *      rows      uint32 [T][nb]        bucket b = (n - min_n) * heads + head
+ *      emb       bf16   [T][K]         bucket-major concatenation
+ *      kv        fp32   [T][N]         rows [b d, (b+1) d) key b; last d: value
+ *      hidden    bf16   [T][hc][d]     updated in place
+ *      gates     fp32   [T][hc]        0 for an image row
+ *      table     uint8  [rows][row_dim]       E4M3 codes
+ *      scales    uint8  [rows][row_dim / 32]  E8M0 exponents
+ *      wkv       bf16   [N][K]         row-major
+ *      wq, wk    fp32   [hc][d]        pre-multiplied norm weights
+ */
+#ifndef ENGRAM_H
+#define ENGRAM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define ENGRAM_DEAD   0xFFFFFFFFu /* compressed id of an image position (window slot) */
+#define ENGRAM_MASKED 0xFFFFFFFFu /* row index of an n-gram that touches DEAD          */
+
+typedef enum engram_status {
+    ENGRAM_OK = 0,
+    ENGRAM_EINVAL = 1,      /* bad argument: null pointer, size, layer, token, alignment   */
+    ENGRAM_ENOMEM = 2,      /* host or device allocation failed                            */
+    ENGRAM_ECUDA = 3,       /* a CUDA runtime call failed (launch or asynchronous error)   */
+    ENGRAM_ESTATE = 4,      /* object in the wrong state (layer not bound, bad session)    */
+    ENGRAM_ETIMEOUT = 5,    /* a kernel gave up a bounded wait and returned                */
+    ENGRAM_EUNSUPPORTED = 6,/* geometry or device the kernels do not support               */
+    ENGRAM_EBOUNDS = 7      /* a kernel met a row index outside the table (row zero-filled)*/
+} engram_status;
+
+typedef struct engram_ctx engram_ctx;
+typedef struct engram_session engram_session;
+
+/* Model geometry and per-layer hash configuration.
+ * Source: "把知识变成可寻址的向量" (2/3/4-gram, 8 heads, 256 values per row),
+ * "第一步" (129,280-entry token map; multipliers, primes, bucket offsets
+ * expanded per layer), FlagScale config fields engram_pad_id / engram_seed. */
+typedef struct engram_ctx_desc {
+    uint32_t vocab;                /* tokenizer vocabulary V (129,280)                 */
+    uint32_t vc;                   /* compressed vocabulary size (every map value < vc) */
+    uint32_t min_n;                /* smallest n-gram order (2), >= 1                  */
+    uint32_t max_n;                /* largest n-gram order (4), <= 4                   */
+    uint32_t heads;                /* hash heads per order (8), 1..8                   */
+    uint32_t row_dim;              /* values per row: 32, 64, 128 or 256               */
+    uint32_t hc;                   /* hyper-connection branches (4), 1..8              */
+    uint32_t d;                    /* hidden size per branch (5,120)                   */
+    uint32_t pad_cid;              /* compressed id before the start of history, < vc  */
+    uint32_t n_layers;             /* Engram layers of the model, 1..16                */
+    double eps;                    /* RMS-norm epsilon (1e-6)                          */
+    const uint64_t* layer_seeds;   /* [n_layers] hash seed of each layer               */
+    const uint64_t* bucket_bases;  /* [n_layers] primes of a layer are > its base      */
+} engram_ctx_desc;
+
+/* Weights of one layer.  table/scales: device memory, or pinned host memory
+ * mapped into the device address space (read through UVA, vLLM "CPU 오프로드").
+ * The scale array must be readable up to its size rounded up to 16 bytes.
+ * wkv must be 16-byte aligned. */
+typedef struct engram_layer_weights {
+    const uint8_t* table;   /* [rows][row_dim] E4M3 codes                     */
+    const uint8_t* scales;  /* [rows][row_dim / 32] E8M0 exponents            */
+    uint64_t rows;          /* must equal the layer's row count (engram_layer_params) */
+    const uint16_t* wkv;    /* bf16 [N][K], device                            */
+    const float* wq;        /* fp32 [hc][d], device                           */
+    const float* wk;        /* fp32 [hc][d], device                           */
+} engram_layer_weights;
+
+/* Create a context.  token_map: host uint32 [vocab] compressed id of each
+ * token (all < vc), copied.  No CUDA call is made. */
+engram_status engram_ctx_create(const engram_ctx_desc* desc, const uint32_t* token_map,
+                                engram_ctx** out);
+engram_status engram_ctx_destroy(engram_ctx* ctx);
+
+/* Hash parameters of a layer (host outputs, each may be NULL):
+ * mult [nb][4] uint64 (the multiplier of window slot j for bucket b),
+ * prime [nb], offset [nb] (prefix sums of the primes), rows = sum of primes.
+ * Primes: strictly increasing primes above the layer's bucket base, no prime
+ * reused by an earlier layer (vLLM wiki "동작 방식"; the row counts on the
+ * lqnn.cn page are sums of such primes).  Multipliers: odd, below
+ * floor((2^64-1)/vc), one per window slot shared by the layer's buckets,
+ * drawn from Philox4x32-10 keyed by the layer seed. */
+engram_status engram_layer_params(const engram_ctx* ctx, int layer, uint64_t* mult,
+                                  uint64_t* prime, uint64_t* offset, uint64_t* rows);
+
+/* Replace a layer's multiplier table with a general one (host [nb][4]),
+ * e.g. independent multipliers per head.  Applies to later calls. */
+engram_status engram_layer_set_multipliers(engram_ctx* ctx, int layer, const uint64_t* mult);
+
+/* Bind a layer's weights (pointers are kept, not copied).  Needs a GPU: it
+ * allocates the context's error word on the current device at first use and
+ * encodes the wkv TMA descriptor. */
+engram_status engram_layer_bind(engram_ctx* ctx, int layer, const engram_layer_weights* w);
+
+/* Fill rows [row_begin, row_end) of a table with its deterministic contents:
+ * code(row, col) and scale(row, group) are a Philox4x32-10 function of
+ * (seed, row, column) - uniform over the 254 finite E4M3 codes and over
+ * E8M0 exponents 119..127.  data/scale may be device or mapped pinned host. */
+engram_status engram_table_fill(const engram_ctx* ctx, uint64_t seed, uint8_t* data,
+                                uint8_t* scale, uint64_t row_begin, uint64_t row_end,
+                                void* stream);
+
+/* Sessions: a hash history (the last three compressed ids and a count).
+ * "第四步": every token enters the history exactly once; prefill appends a
+ * span, decode appends one token; fork copies the history; reset empties it.
+ * Layers never append: they consume the windows an append returned. */
+engram_status engram_session_create(engram_ctx* ctx, engram_session** out);
+engram_status engram_session_fork(const engram_session* s, engram_session** out);
+engram_status engram_session_reset(engram_session* s);
+engram_status engram_session_destroy(engram_session* s);
+/* Append n tokens (host int32 [n]; is_image host uint8 [n] or NULL) and write
+ * their windows (host uint32 [n][4]).  An image position appends DEAD (its
+ * token value is ignored).  A text token outside [0, vocab) is EINVAL and
+ * nothing is appended. */
+engram_status engram_session_append(engram_session* s, const int32_t* tokens,
+                                    const uint8_t* is_image, int64_t n, uint32_t* windows_out);
+/* Decode: append one token to each of n sessions (in array order). */
+engram_status engram_batch_append(engram_session* const* sessions, const int32_t* tokens,
+                                  const uint8_t* is_image, int64_t n, uint32_t* windows_out);
+
+/* Bytes of device workspace engram_forward needs for T tokens. */
+size_t engram_workspace_bytes(const engram_ctx* ctx, int64_t T);
+
+/* a2: windows (device [T][4]) -> row indices (device [T][nb]). */
+engram_status engram_hash(const engram_ctx* ctx, int layer, const uint32_t* d_windows, int64_t T,
+                          uint32_t* d_rows, void* stream);
+/* a3: row indices -> dequantised BF16 vectors (device [T][K]); a masked row
+ * gives zeros; an index >= rows gives zeros and sets the error word. */
+engram_status engram_gather_dequant(const engram_ctx* ctx, int layer, const uint32_t* d_rows,
+                                    int64_t T, uint16_t* d_emb, void* stream);
+/* a4: kv = emb wkv^T in fp32 (device [T][N]); d_emb 16-byte aligned. */
+engram_status engram_project(const engram_ctx* ctx, int layer, const uint16_t* d_emb, int64_t T,
+                             float* d_kv, void* stream);
+/* a5: gate and update hidden in place; image rows (window slot 0 == DEAD)
+ * pass through.  d_gates may be NULL. */
+engram_status engram_gate(const engram_ctx* ctx, int layer, const float* d_kv,
+                          const uint32_t* d_windows, int64_t T, uint16_t* d_hidden,
+                          float* d_gates, void* stream);
+/* a7: the whole step fused: hash, gather and dequantise into the GEMM's
+ * shared-memory operand tiles, the tcgen05 projection and the gate as the
+ * GEMM epilogue.  Neither the 6,144-vector nor the kv reaches HBM.
+ * d_workspace: engram_workspace_bytes(ctx, T) bytes of device memory. */
+engram_status engram_forward(const engram_ctx* ctx, int layer, const uint32_t* d_windows,
+                             int64_t T, uint16_t* d_hidden, void* d_workspace,
+                             float* d_gates, void* stream);
+
+/* a2 -> a4 fused, the part of the step that does not depend on hidden
+ * ("DeepSeek V4.1 Flash 的 Engram", section "提前投影": hashing, gather and
+ * projection depend only on the tokens and can run ahead of the layer):
+ * windows (device [T][4]) -> kv fp32 (device [T][N]); the 6,144-vector stays
+ * in shared memory.  engram_gate then finishes the step at the layer entry. */
+engram_status engram_project_windows(const engram_ctx* ctx, int layer, const uint32_t* d_windows,
+                                     int64_t T, float* d_kv, void* stream);
+
+/* Synchronise `stream`, then read and clear the context's device error word:
+ * ENGRAM_EBOUNDS / ENGRAM_ETIMEOUT if a kernel reported one, ENGRAM_ECUDA on
+ * an asynchronous CUDA error. */
+engram_status engram_sync(const engram_ctx* ctx, void* stream);
+
+/* Message of the calling thread's last error ("" if none). */
+const char* engram_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

@@ -1,0 +1,239 @@
+"""GPU parity of every step against the CPU oracle, through the C ABI.
+
+Integer and byte results (table contents, row indices, dequantised rows) must
+be bit-exact; floating-point results follow the tolerances in helpers.py.
+Sizes: the tiny workload in full (several tiles in N, ragged token counts in
+M), and the 2,048-token prefill at full geometry (all indices, sampled rows
+of the oracle's fp64 result).
+"""
+import numpy as np
+import pytest
+import torch
+
+import engram_gram_conditional_gb300 as eg
+import oracle as O
+import synth
+from helpers import (bf16_f64, check_hidden, check_kv, from_dev, geom, prefill_windows,
+                     setup_workload, to_dev)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from engram_gram_conditional_gb300 import build
+
+    build.build()
+    O.build()
+    assert torch.cuda.is_available()
+
+
+@pytest.fixture(scope="module")
+def tiny():
+    s = setup_workload("tiny")
+    yield s
+    s.close()
+
+
+@pytest.fixture(scope="module")
+def prefill():
+    s = setup_workload("prefill_2048")
+    yield s
+    s.close()
+
+
+def gpu_rows(s, win, layer=0):
+    T = win.shape[0]
+    d_win = to_dev(win)
+    d_rows = torch.empty((T, s.w.nb), dtype=torch.int32, device="cuda")
+    eg.engram_hash(s.model.ctx, layer, d_win, T, d_rows)
+    eg.engram_sync(s.model.ctx)
+    return from_dev(d_rows, np.uint32), d_rows
+
+
+def gpu_emb(s, d_rows, T, layer=0):
+    d_emb = torch.empty((T, s.w.K), dtype=torch.int16, device="cuda")
+    eg.engram_gather_dequant(s.model.ctx, layer, d_rows, T, d_emb)
+    eg.engram_sync(s.model.ctx)
+    return d_emb
+
+
+# ---- a0: table contents --------------------------------------------------------------
+
+def test_table_fill_tiny_whole_table(tiny):
+    t = tiny.model.tensors[0]
+    rows = tiny.model.rows(0)
+    data = t["table"].cpu().numpy()[: rows * 32].reshape(rows, 32)
+    scl = t["scales"].cpu().numpy()[:rows]
+    for r in range(rows):
+        c, s = O.table_row(t["table_seed"], r, 32)
+        assert np.array_equal(data[r], c) and scl[r] == s[0], r
+
+
+def test_table_fill_full_geometry_sampled(prefill):
+    t = prefill.model.tensors[0]
+    rows = prefill.model.rows(0)
+    rng = np.random.default_rng(0)
+    sample = np.concatenate([[0, 1, rows - 2, rows - 1], rng.integers(0, rows, 400)])
+    data = t["table"].view(-1)
+    scl = t["scales"].view(-1)
+    for r in sample.tolist():
+        c, s = O.table_row(t["table_seed"], r, 256)
+        assert np.array_equal(data[r * 256:(r + 1) * 256].cpu().numpy(), c), r
+        assert np.array_equal(scl[r * 8:(r + 1) * 8].cpu().numpy(), s), r
+
+
+# ---- a2 / a3: hash and gather, bit-exact ------------------------------------------------
+
+@pytest.mark.parametrize("sessions,per", [(1, 64), (3, 43), (1, 1)])
+def test_hash_and_gather_tiny_bit_exact(tiny, sessions, per):
+    win, _, _ = prefill_windows(tiny, sessions, per, spans=[(5, 3)] if per > 10 else [])
+    T = win.shape[0]
+    rows, d_rows = gpu_rows(tiny, win)
+    g = geom(tiny.w)
+    for t in range(T):
+        ref = O.hash_rows(g, tiny.oparams[0], win[t])
+        assert np.array_equal(rows[t], ref), t
+    emb = from_dev(gpu_emb(tiny, d_rows, T), np.uint16)
+    for t in range(T):
+        assert np.array_equal(emb[t], O.gather(g, tiny.w.table_seeds[0], rows[t])), t
+
+
+def test_hash_full_geometry_bit_exact(prefill):
+    win, _, _ = prefill_windows(prefill, 1, 2048)
+    rows, d_rows = gpu_rows(prefill, win)
+    g = geom(prefill.w)
+    for t in range(2048):
+        assert np.array_equal(rows[t], O.hash_rows(g, prefill.oparams[0], win[t])), t
+    # every index inside its bucket
+    p = prefill.oparams[0]
+    for b in range(24):
+        assert (rows[:, b] >= p.offset[b]).all() and (rows[:, b] < p.offset[b] + p.prime[b]).all()
+    emb = from_dev(gpu_emb(prefill, d_rows, 2048), np.uint16)
+    rng = np.random.default_rng(1)
+    for t in [0, 1, 2, 3, 2047] + rng.integers(0, 2048, 59).tolist():
+        assert np.array_equal(emb[t], O.gather(g, prefill.w.table_seeds[0], rows[t])), t
+
+
+# ---- a4: projection ---------------------------------------------------------------------
+
+@pytest.mark.parametrize("sessions,per", [(1, 64), (3, 43), (1, 1), (2, 100)])
+def test_project_tiny(tiny, sessions, per):
+    win, _, _ = prefill_windows(tiny, sessions, per)
+    T = win.shape[0]
+    rows, d_rows = gpu_rows(tiny, win)
+    d_emb = gpu_emb(tiny, d_rows, T)
+    d_kv = torch.empty((T, tiny.w.N), dtype=torch.float32, device="cuda")
+    eg.engram_project(tiny.model.ctx, 0, d_emb, T, d_kv)
+    eg.engram_sync(tiny.model.ctx)
+    kv = d_kv.cpu().numpy()
+    g = geom(tiny.w)
+    for t in range(T):
+        e = O.gather(g, tiny.w.table_seeds[0], O.hash_rows(g, tiny.oparams[0], win[t]))
+        ref = O.project(g, tiny.W[0], e)
+        check_kv(kv[t], ref, tiny.W[0], e, tiny.w.K, f"token {t}")
+    # the fused hash+gather+projection gives the same kv, bit for bit
+    d_kv2 = torch.full_like(d_kv, float("nan"))
+    eg.engram_project_windows(tiny.model.ctx, 0, to_dev(win), T, d_kv2)
+    eg.engram_sync(tiny.model.ctx)
+    assert torch.equal(d_kv, d_kv2)
+
+
+def test_project_full_geometry_sampled(prefill):
+    win, _, _ = prefill_windows(prefill, 1, 2048)
+    T = 2048
+    d_kv = torch.empty((T, prefill.w.N), dtype=torch.float32, device="cuda")
+    eg.engram_project_windows(prefill.model.ctx, 0, to_dev(win), T, d_kv)
+    eg.engram_sync(prefill.model.ctx)
+    g = geom(prefill.w)
+    sample = [0, 127, 128, 2047, 1000, 1500]
+    ref = O.forward(g, prefill.w.table_seeds[0], prefill.oparams[0], prefill.W[0], prefill.wq[0],
+                    prefill.wk[0], win, synth.hidden_bf16(prefill.w, T), np.array(sample),
+                    nthreads=8, want_e=True, want_kv=True, want_h64=False)
+    for i, t in enumerate(sample):
+        check_kv(d_kv[t].cpu().numpy(), ref["kv"][i], prefill.W[0], ref["e"][i], prefill.w.K,
+                 f"token {t}")
+
+
+# ---- a5: the gate alone, on the oracle's kv -------------------------------------------
+
+def test_gate_alone_on_oracle_kv(tiny):
+    win, _, _ = prefill_windows(tiny, 1, 64, spans=[(30, 4)])
+    T = 64
+    hidden = synth.hidden_bf16(tiny.w, T)
+    g = geom(tiny.w)
+    ref = O.forward(g, tiny.w.table_seeds[0], tiny.oparams[0], tiny.W[0], tiny.wq[0], tiny.wk[0],
+                    win, hidden, np.arange(T), want_kv=True, want_h64=False)
+    kv32 = ref["kv"].astype(np.float32)
+    exp_h = np.zeros_like(ref["h_bf16"])
+    exp_g = np.zeros_like(ref["gates"])
+    for t in range(T):
+        _, exp_h[t], exp_g[t] = O.gate(g, kv32[t].astype(np.float64), int(win[t][0]), hidden[t],
+                                       tiny.wq[0], tiny.wk[0])
+    d_h = to_dev(hidden)
+    d_g = torch.empty((T, tiny.w.hc), dtype=torch.float32, device="cuda")
+    eg.engram_gate(tiny.model.ctx, 0, torch.from_numpy(kv32).cuda(), to_dev(win), T, d_h, d_g)
+    eg.engram_sync(tiny.model.ctx)
+    check_hidden(from_dev(d_h, np.uint16), exp_h, "gate")
+    assert np.abs(d_g.cpu().numpy() - exp_g).max() <= 1e-3
+    assert np.array_equal(from_dev(d_h, np.uint16)[30:34], hidden[30:34])  # image rows
+
+
+# ---- a7: the fused forward --------------------------------------------------------------
+
+def run_forward(s, win, hidden, layer=0):
+    T = win.shape[0]
+    d_h = to_dev(hidden)
+    d_ws = torch.empty(max(16, eg.engram_workspace_bytes(s.model.ctx, T)), dtype=torch.uint8,
+                       device="cuda")
+    d_g = torch.full((T, s.w.hc), float("nan"), dtype=torch.float32, device="cuda")
+    eg.engram_forward(s.model.ctx, layer, to_dev(win), T, d_h, d_ws, d_g)
+    eg.engram_sync(s.model.ctx)
+    return from_dev(d_h, np.uint16), d_g.cpu().numpy()
+
+
+@pytest.mark.parametrize("sessions,per,spans", [(1, 64, [(20, 4)]), (3, 70, [(0, 2), (50, 9)]),
+                                                (1, 1, []), (2, 129, [(128, 1)])])
+def test_forward_tiny_all_tokens(tiny, sessions, per, spans):
+    win, _, _ = prefill_windows(tiny, sessions, per, spans)
+    T = win.shape[0]
+    hidden = synth.hidden_bf16(tiny.w, T)
+    h, gates = run_forward(tiny, win, hidden)
+    ref = O.forward(geom(tiny.w), tiny.w.table_seeds[0], tiny.oparams[0], tiny.W[0], tiny.wq[0],
+                    tiny.wk[0], win, hidden, np.arange(T), nthreads=4)
+    check_hidden(h, ref["h_bf16"], "forward")
+    assert np.abs(gates - ref["gates"]).max() <= 1e-3
+    image = win[:, 0] == eg.DEAD
+    assert np.array_equal(h[image], hidden[image])
+    assert (gates[image] == 0).all()
+    # rows whose every n-gram is masked keep their hidden bit for bit
+    allmasked = (win[:, 1] == eg.DEAD) & ~image
+    assert np.array_equal(h[allmasked], hidden[allmasked])
+
+
+def test_forward_full_geometry_sampled(prefill):
+    win, _, _ = prefill_windows(prefill, 1, 2048)
+    T = 2048
+    hidden = synth.hidden_bf16(prefill.w, T)
+    h, gates = run_forward(prefill, win, hidden)
+    sample = np.array([0, 1, 126, 127, 128, 129, 1023, 2046, 2047, 700])
+    ref = O.forward(geom(prefill.w), prefill.w.table_seeds[0], prefill.oparams[0], prefill.W[0],
+                    prefill.wq[0], prefill.wk[0], win, hidden, sample, nthreads=8)
+    check_hidden(h[sample], ref["h_bf16"], "forward 2048")
+    assert np.abs(gates[sample] - ref["gates"]).max() <= 1e-3
+    # and the unfused chain on the GPU agrees with the fused kernel
+    d_kv = torch.empty((T, prefill.w.N), dtype=torch.float32, device="cuda")
+    eg.engram_project_windows(prefill.model.ctx, 0, to_dev(win), T, d_kv)
+    d_h = to_dev(hidden)
+    eg.engram_gate(prefill.model.ctx, 0, d_kv, to_dev(win), T, d_h)
+    eg.engram_sync(prefill.model.ctx)
+    check_hidden(h, from_dev(d_h, np.uint16), "fused vs chain")
+
+
+def test_forward_edge_cases(tiny):
+    ctx = tiny.model.ctx
+    eg.engram_forward(ctx, 0, None, 0, None, None)  # T = 0
+    win, _, _ = prefill_windows(tiny, 1, 40, spans=[(0, 40)])  # all image rows
+    hidden = synth.hidden_bf16(tiny.w, 40)
+    h, gates = run_forward(tiny, win, hidden)
+    assert np.array_equal(h, hidden) and (gates == 0).all()
