@@ -1,0 +1,511 @@
+#!/usr/bin/env python
+"""Benchmark of the Engram per-layer forward step on GB300.
+
+One step = the whole hot path over one batch: the 2,048-token prefill at full
+geometry (24 MXFP8 rows of 256 from a 16.0M-row table, wkv 25,600 x 6,144, 4
+hyper-connection branches of 5,120).  `value` is device-timed (CUDA events,
+inputs resident in HBM) tokens/s per layer of engram_forward; `e2e` is the
+same metric through the C ABI with host buffers: append on the host, pinned
+H2D of windows and hidden, the forward, D2H of the updated hidden.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+N > 1 (torchrun): every rank runs its own replica on its own batches (weak
+scaling, no collective on the data path); the time is the max over ranks.
+`--impl reference` times the CPU oracle (the plain fp64 definition) on the
+host cores on the same workload: each step is a bounded sample of tokens.
+"""
+from __future__ import annotations
+
+import argparse
+import datetime as _dt
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = "prefill_2048"
+FLOP_PER_TOKEN = None  # set from the geometry: 2 N K
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="mine", choices=["mine", "reference"])
+    ap.add_argument("--no-extras", action="store_true", help="skip decode / gather / project lines")
+    ap.add_argument("--cpu-sample", type=int, default=256,
+                    help="oracle tokens for cpu_baseline (0: skip)")
+    ap.add_argument("--small", action="store_true",
+                    help="profiling case: same kernels and batch, a 4.8M-row table, 2 batches")
+    return ap.parse_args()
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return dict(hbm=float(d["hbm_gbs"]), bf16=float(d["bf16_tflops"]),
+                    bf16_sus=float(d["bf16_tflops_sustained"]), src="measured")
+    except Exception:
+        return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
+
+
+# ---- distributed plumbing (timing only: barrier and max over ranks) -------------------------
+
+class Dist:
+    def __init__(self):
+        import torch
+
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as dist
+
+            backend = "nccl" if torch.cuda.is_available() else "gloo"
+            if backend == "nccl":
+                torch.cuda.set_device(self.local)
+            dist.init_process_group(backend=backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, x: float) -> float:
+        if not self.pg:
+            return x
+        import torch
+
+        dev = "cuda" if torch.cuda.is_available() else "cpu"
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def sum(self, x: float) -> float:
+        if not self.pg:
+            return x
+        import torch
+
+        dev = "cuda" if torch.cuda.is_available() else "cpu"
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.SUM)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+def shard_sessions(n_sessions: int, rank: int, world: int):
+    """Sessions owned by a rank: contiguous, as even as possible (no data exchange)."""
+    lo = n_sessions * rank // world
+    hi = n_sessions * (rank + 1) // world
+    return list(range(lo, hi))
+
+
+# ---- clocks ------------------------------------------------------------------------------------
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a timed region."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu: int, interval_ms: int = 50):
+        self.gpu = gpu
+        self.interval = interval_ms
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", str(self.interval), "-i", str(self.gpu)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.5)
+        except Exception:
+            self.proc = None
+
+    def stop(self, t0: float, t1: float) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        rows = []
+        for ln in out.splitlines():
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 10:
+                continue
+            try:
+                ts = _dt.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(f[2]), float(f[3]), f[6:10]))
+            except ValueError:
+                continue
+        inside = [r for r in rows if t0 - 0.05 <= r[0] <= t1 + 0.05] or rows[-3:]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in inside for i, v in enumerate(r[3]) if v == "Active"})
+        sm = [r[1] for r in inside]
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": max(r[2] for r in inside) if inside else None,
+                "reasons": reasons, "samples": len(inside)}
+
+
+# ---- the reference arm: the CPU oracle ----------------------------------------------------
+
+def cpu_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def oracle_inputs(w, T):
+    import oracle as O
+    import synth
+
+    g = O.Geom(vocab=w.vocab, vc=w.vc, min_n=w.min_n, max_n=w.max_n, heads=w.heads,
+               row_dim=w.row_dim, hc=w.hc, d=w.d, pad_cid=w.pad_cid, eps=w.eps)
+    p = O.layer_params(g, w.hash_seeds, w.bucket_bases, 0)
+    tmap = synth.token_map(w.vocab, w.vc, w.seed)
+    win = O.windows(g, tmap, synth.session_tokens(w, 0, T))
+    return g, p, win
+
+
+def run_oracle_timed(w, W, wq, wk, hidden, win, g, p, tokens: np.ndarray, threads: int) -> float:
+    import oracle as O
+
+    t0 = time.perf_counter()
+    O.forward(g, w.table_seeds[0], p, W, wq, wk, win, hidden, tokens, nthreads=threads,
+              want_h64=False)
+    return time.perf_counter() - t0
+
+
+def reference_arm(args, dist: Dist):
+    if dist.rank != 0:
+        dist.close()
+        return
+    import oracle as O
+    import synth
+
+    O.build()
+    w = synth.WORKLOADS[WORKLOAD]
+    T = w.tokens_per_session
+    W = synth.wkv_bf16(w)
+    wq, wk = synth.wq_wk(w)
+    hidden = synth.hidden_bf16(w, T)
+    g, p, win = oracle_inputs(w, T)
+    cores = cpu_cores()
+    # size each step's sample so the whole run takes about 20-150 s of wall time
+    calib = run_oracle_timed(w, W, wq, wk, hidden, win, g, p, np.arange(cores) % T, cores)
+    rate = cores / calib  # tokens/s with all cores
+    steps, warm = args.steps, args.warmup
+    per_step = max(1, min(T, int(round(20.0 * rate / max(steps, 1)))))
+    rng = np.random.default_rng(0)
+    sample = rng.integers(0, T, (warm + steps) * per_step)
+    run_oracle_timed(w, W, wq, wk, hidden, win, g, p, sample[:warm * per_step], cores)
+    elapsed = run_oracle_timed(w, W, wq, wk, hidden, win, g, p, sample[warm * per_step:], cores)
+    toks = steps * per_step
+    value = toks / elapsed
+    line = {
+        "metric": "Engram tokens/s per layer (prefill, decode); gather HBM GB/s; wkv TC util %",
+        "impl": "reference", "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": steps, "warmup": warm, "ms_per_step": 1000.0 * elapsed / steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": workload_config(w),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{per_step} random tokens of the {T}-token prefill per step, "
+                                   f"all steps' tokens run by the oracle over {cores} threads"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    dist.close()
+
+
+def workload_config(w) -> dict:
+    return {"workload": f"{w.name}: {w.tokens_per_session} tokens, 1 Engram layer, "
+                        f"n=2..4 x {w.heads} heads x {w.row_dim}, wkv {w.N}x{w.K} bf16, "
+                        f"hc {w.hc} x {w.d}",
+            "tokens_per_step": w.sessions * w.tokens_per_session, "layers": 1,
+            "table_rows": None, "table_format": "MXFP8 (E4M3 + E8M0 per 32)",
+            "l2": "inputs larger than L2: wkv 314.6 MB per step plus a rotating pool of 8 "
+                  "hidden/window batches (671 MB)"}
+
+
+# ---- my arm ------------------------------------------------------------------------------------
+
+def main():
+    args = parse_args()
+    dist = Dist()
+    if args.impl == "reference":
+        reference_arm(args, dist)
+        return
+    import torch
+
+    import engram_gram_conditional_gb300 as eg
+    import oracle as O
+    import synth
+    from engram_gram_conditional_gb300 import build
+    from engram_gram_conditional_gb300.layer import EngramLayerSet
+
+    if dist.rank == 0:
+        build.build()
+    dist.barrier()
+    torch.cuda.set_device(dist.local)
+    dev = torch.device("cuda", dist.local)
+    stream = torch.cuda.current_stream()
+    peaks = load_peaks()
+
+    w = synth.WORKLOADS[WORKLOAD]
+    POOL = 8
+    if args.small:
+        import dataclasses
+
+        w = dataclasses.replace(w, bucket_bases=[200_000])
+        POOL = 2
+    T = w.tokens_per_session
+    flop_tok = 2.0 * w.N * w.K
+    tmap = synth.token_map(w.vocab, w.vc, w.seed)
+    W = synth.wkv_bf16(w)
+    wq, wk = synth.wq_wk(w)
+    model = EngramLayerSet.from_workload(w, tmap, device=dev)
+    model.bind(0, w.table_seeds[0], W, wq, wk)
+    rows = model.rows(0)
+    ctx = model.ctx
+
+    # a pool of distinct batches per rank (distinct sessions -> distinct rows)
+    base_session = dist.rank * POOL
+    win_h, hid_h = [], []
+    for i in range(POOL):
+        s = eg.engram_session_create(ctx)
+        win_h.append(eg.engram_session_append(s, synth.session_tokens(w, base_session + i, T)))
+        eg.engram_session_destroy(s)
+        hid_h.append(synth.normal_bf16((T, w.hc, w.d), 1.0, w.seed, 1000 + base_session + i))
+    d_win = [torch.from_numpy(x.view(np.int32)).to(dev) for x in win_h]
+    d_hid = [torch.from_numpy(x.view(np.int16)).to(dev) for x in hid_h]
+    d_ws = torch.empty(eg.engram_workspace_bytes(ctx, T), dtype=torch.uint8, device=dev)
+    sptr = stream.cuda_stream
+
+    def step(i):
+        j = i % POOL
+        eg.engram_forward(ctx, 0, d_win[j], T, d_hid[j], d_ws, None, sptr)
+
+    for i in range(args.warmup):
+        step(i)
+    eg.engram_sync(ctx, sptr)
+    clocks = ClockSampler(dist.local)
+    clocks.start()
+    dist.barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.time()
+    ev0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    dist.barrier()
+    clk = clocks.stop(t0, t1)
+    eg.engram_sync(ctx, sptr)
+    ms_local = ev0.elapsed_time(ev1)
+    ms = dist.max(ms_local)
+    total_tokens = dist.sum(float(T * args.steps))
+    value = total_tokens / (ms / 1000.0)
+    ms_step = ms / args.steps
+    flops_call = flop_tok * T
+    achieved = flops_call / (ms_local / args.steps / 1000.0) / 1e12
+
+    # ---- e2e through the C ABI with host buffers ----
+    h_win = torch.empty((T, 4), dtype=torch.int32, pin_memory=True)
+    h_hid_in = [torch.from_numpy(x.view(np.int16)).pin_memory() for x in hid_h[:2]]
+    h_hid_out = torch.empty((T, w.hc, w.d), dtype=torch.int16, pin_memory=True)
+    e_win = torch.empty((T, 4), dtype=torch.int32, device=dev)
+    e_hid = torch.empty((T, w.hc, w.d), dtype=torch.int16, device=dev)
+    tok_h = [synth.session_tokens(w, 100 + base_session + i, T) for i in range(2)]
+    h_win_np = h_win.numpy().view(np.uint32)
+
+    def e2e_step(i):
+        s = eg.engram_session_create(ctx)
+        eg.engram_session_append(s, tok_h[i % 2], None, h_win_np)
+        eg.engram_session_destroy(s)
+        e_win.copy_(h_win, non_blocking=True)
+        e_hid.copy_(h_hid_in[i % 2], non_blocking=True)
+        eg.engram_forward(ctx, 0, e_win, T, e_hid, d_ws, None, sptr)
+        h_hid_out.copy_(e_hid, non_blocking=True)
+        stream.synchronize()
+
+    e2e_steps = max(1, min(args.steps, 500))
+    for i in range(min(args.warmup, 5)):
+        e2e_step(i)
+    dist.barrier()
+    torch.cuda.synchronize()
+    t_e0 = time.perf_counter()
+    for i in range(e2e_steps):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    e2e_s = dist.max(time.perf_counter() - t_e0)
+    e2e_value = dist.sum(float(T * e2e_steps)) / e2e_s
+    eg.engram_sync(ctx, sptr)
+
+    line = {
+        "metric": "Engram tokens/s per layer (prefill, decode); gather HBM GB/s; wkv TC util %",
+        "value": value, "unit": "tokens/s", "n_gpus": dist.world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": dict(workload_config(w), table_rows=rows, parallelism=f"replicas x{dist.world}"),
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16"],
+                     "unit": "TFLOP/s", "frac": achieved / peaks["bf16"], "traffic": None,
+                     "kernel": "k_mma fused forward (key + value launches of one engram_forward)",
+                     "peak_kind": f"bf16 dense burst, {peaks['src']}",
+                     "frac_of_sustained": achieved / peaks["bf16_sus"],
+                     "flop_per_call": flops_call},
+        "e2e": {"value": e2e_value, "unit": "tokens/s",
+                "h2d_bytes_per_step": T * 16 + T * w.hc * w.d * 2,
+                "d2h_bytes_per_step": T * w.hc * w.d * 2, "steps": e2e_steps},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clk,
+    }
+
+    if args.small:
+        line["config"]["l2"] = "profiling case: 2 batches, 4.8M-row table"
+    if dist.rank == 0 and dist.world == 1 and not args.no_extras and not args.small:
+        try:
+            line.update(extras(args, w, W, wq, wk, tmap, win_h[0], d_win[0], model, peaks, dev,
+                               sptr, stream))
+        except Exception as exc:  # extras never hide the main line
+            line["extras_error"] = repr(exc)
+    if dist.rank == 0 and dist.world == 1 and args.cpu_sample > 0:
+        line["cpu_baseline"] = cpu_baseline(args, w, W, wq, wk, win_h[0], hid_h[0])
+    model.close()
+    if dist.rank == 0:
+        print(json.dumps(line), flush=True)
+    dist.close()
+
+
+def timed(fn, steps, stream):
+    import torch
+
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    for i in range(steps):
+        fn(i)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    return ev0.elapsed_time(ev1) / steps
+
+
+def extras(args, w, W, wq, wk, tmap, win0, d_win0, model, peaks, dev, sptr, stream):
+    """Side measurements: the unfused stages at the prefill, and the decode batch."""
+    import torch
+
+    import engram_gram_conditional_gb300 as eg
+    import synth
+    from engram_gram_conditional_gb300.layer import EngramLayerSet
+
+    out = {}
+    ctx, T = model.ctx, w.tokens_per_session
+    # unfused projection (TMA A operand) and the fused hash+gather+projection
+    d_rows = torch.empty((T, w.nb), dtype=torch.int32, device=dev)
+    d_emb = torch.empty((T, w.K), dtype=torch.int16, device=dev)
+    d_kv = torch.empty((T, w.N), dtype=torch.float32, device=dev)
+    eg.engram_hash(ctx, 0, d_win0, T, d_rows, sptr)
+    eg.engram_gather_dequant(ctx, 0, d_rows, T, d_emb, sptr)
+    for _ in range(3):
+        eg.engram_project(ctx, 0, d_emb, T, d_kv, sptr)
+    ms_p = timed(lambda i: eg.engram_project(ctx, 0, d_emb, T, d_kv, sptr), 50, stream)
+    ms_pw = timed(lambda i: eg.engram_project_windows(ctx, 0, d_win0, T, d_kv, sptr), 50, stream)
+    fl = 2.0 * w.N * w.K * T
+    out["project"] = {"ms": ms_p, "tflops": fl / ms_p / 1e9,
+                      "tc_frac": fl / ms_p / 1e9 / peaks["bf16"]}
+    out["project_windows"] = {"ms": ms_pw, "tflops": fl / ms_pw / 1e9,
+                              "tc_frac": fl / ms_pw / 1e9 / peaks["bf16"]}
+    del d_rows, d_emb, d_kv
+
+    # decode: 256 sessions x 1 token per step, 384M-row table resident in HBM
+    wd = synth.WORKLOADS["decode_256"]
+    dm = EngramLayerSet.from_workload(wd, tmap, device=dev)
+    dm.bind(0, wd.table_seeds[0], model.tensors[0]["wkv"], wq, wk)
+    S = wd.sessions
+    sess = [eg.engram_session_create(dm.ctx) for _ in range(S)]
+    streams = np.stack([synth.session_tokens(wd, i, wd.history + wd.steps) for i in range(S)])
+    for i, s in enumerate(sess):
+        eg.engram_session_append(s, streams[i, :wd.history])
+    wins = [eg.engram_batch_append(sess, streams[:, wd.history + step])
+            for step in range(wd.steps)]
+    d_wins = torch.from_numpy(np.stack(wins).view(np.int32)).to(dev)
+    d_h = torch.from_numpy(synth.normal_bf16((S, wd.hc, wd.d), 1.0, 0, 77).view(np.int16)).to(dev)
+    d_ws = torch.empty(eg.engram_workspace_bytes(dm.ctx, S), dtype=torch.uint8, device=dev)
+    for i in range(5):
+        eg.engram_forward(dm.ctx, 0, d_wins[i], S, d_h, d_ws, None, sptr)
+    ms_d = timed(lambda i: eg.engram_forward(dm.ctx, 0, d_wins[i % wd.steps], S, d_h, d_ws, None,
+                                             sptr), wd.steps, stream)
+    eg.engram_sync(dm.ctx, sptr)
+    bytes_step = w.N * w.K * 2 + S * (6336 + 81920 + 16)
+    gbs = bytes_step / ms_d / 1e6
+    out["decode"] = {"tokens_per_s": S / (ms_d / 1000.0), "ms_per_step": ms_d, "sessions": S,
+                     "steps": wd.steps, "table_rows": dm.rows(0),
+                     "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm"],
+                                  "unit": "GB/s", "frac": gbs / peaks["hbm"],
+                                  "bytes_per_step": bytes_step}}
+
+    # gather: unfused engram_gather_dequant over the 384M-row table, 50,032 tokens
+    Tg = 50_032
+    sg = eg.engram_session_create(dm.ctx)
+    wg = eg.engram_session_append(sg, synth.zipf_tokens(Tg, wd.vocab, seed=5))
+    d_wg = torch.from_numpy(wg.view(np.int32)).to(dev)
+    d_rg = torch.empty((Tg, w.nb), dtype=torch.int32, device=dev)
+    d_eg = torch.empty((Tg, w.K), dtype=torch.int16, device=dev)
+    eg.engram_hash(dm.ctx, 0, d_wg, Tg, d_rg, sptr)
+    for _ in range(3):
+        eg.engram_gather_dequant(dm.ctx, 0, d_rg, Tg, d_eg, sptr)
+    ms_g = timed(lambda i: eg.engram_gather_dequant(dm.ctx, 0, d_rg, Tg, d_eg, sptr), 20, stream)
+    eg.engram_sync(dm.ctx, sptr)
+    gb_alg = Tg * (w.nb * 4 + w.nb * 264 + w.K * 2)
+    out["gather"] = {"tokens": Tg, "table_rows": dm.rows(0), "ms": ms_g,
+                     "GB_per_s": gb_alg / ms_g / 1e6, "frac": gb_alg / ms_g / 1e6 / peaks["hbm"],
+                     "bytes_per_token": w.nb * 4 + w.nb * 264 + w.K * 2}
+    for s in sess + [sg]:
+        eg.engram_session_destroy(s)
+    dm.close()
+    return out
+
+
+def cpu_baseline(args, w, W, wq, wk, win, hidden):
+    import oracle as O
+
+    O.build()
+    g = O.Geom(vocab=w.vocab, vc=w.vc, min_n=w.min_n, max_n=w.max_n, heads=w.heads,
+               row_dim=w.row_dim, hc=w.hc, d=w.d, pad_cid=w.pad_cid, eps=w.eps)
+    p = O.layer_params(g, w.hash_seeds, w.bucket_bases, 0)
+    cores = cpu_cores()
+    n = max(cores, args.cpu_sample)
+    idx = np.random.default_rng(1).integers(0, w.tokens_per_session, n)
+    el = run_oracle_timed(w, W, wq, wk, hidden, win, g, p, idx, cores)
+    return {"value": n / el, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{n} random tokens of the {w.tokens_per_session}-token prefill, "
+                      f"threads over tokens", "seconds": el}
+
+
+if __name__ == "__main__":
+    main()
