@@ -32,7 +32,8 @@ EXPORTS = (
     "engram_session_create", "engram_session_fork", "engram_session_reset",
     "engram_session_destroy", "engram_session_append", "engram_batch_append",
     "engram_workspace_bytes", "engram_hash", "engram_gather_dequant", "engram_project",
-    "engram_gate", "engram_forward", "engram_project_windows", "engram_sync",
+    "engram_gate", "engram_forward", "engram_forward_noalloc", "engram_project_windows",
+    "engram_sync",
     "engram_last_error",
 )
 
@@ -91,6 +92,7 @@ def lib() -> C.CDLL:
             "engram_gate": [vp, C.c_int, vp, vp, i64, vp, vp, vp],
             "engram_forward": [vp, C.c_int, vp, i64, vp, vp, vp, vp],
             "engram_project_windows": [vp, C.c_int, vp, i64, vp, vp],
+            "engram_forward_noalloc": [vp, C.c_int, vp, i64, vp, vp, vp],
             "engram_sync": [vp, vp],
         }
         for name, args in sig.items():
@@ -256,6 +258,13 @@ def engram_gate(ctx, layer, d_kv, d_windows, T, d_hidden, d_gates=None, stream=N
 def engram_forward(ctx, layer, d_windows, T, d_hidden, d_workspace, d_gates=None, stream=None):
     _check(lib().engram_forward(ctx, layer, _ptr(d_windows), T, _ptr(d_hidden), _ptr(d_workspace),
                                 _ptr(d_gates), _stream(stream)))
+
+
+def engram_forward_noalloc(ctx, layer, d_windows, T, d_hidden, d_gates=None, stream=None):
+    """engram_forward without a workspace argument, for callers that cannot allocate:
+    the scratch is the library's built-in 8 MiB device buffer (see include/engram.h)."""
+    _check(lib().engram_forward_noalloc(ctx, layer, _ptr(d_windows), T, _ptr(d_hidden),
+                                        _ptr(d_gates), _stream(stream)))
 
 
 def engram_project_windows(ctx, layer, d_windows, T, d_kv, stream=None):

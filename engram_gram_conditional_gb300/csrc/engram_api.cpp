@@ -35,6 +35,15 @@ engram_status cuda_fail(cudaError_t e, const char* what) {
 
 constexpr uint32_t kSessionMagic = 0x53474E45u;  // "ENGS"
 
+}  // namespace
+
+namespace engram {
+// Message for engram_last_error() from the library's other translation units.
+void set_last_error(const std::string& msg) { g_last_error = msg; }
+}  // namespace engram
+
+namespace {
+
 // ---- hash parameters (setup) -------------------------------------------------------
 // Deterministic Miller-Rabin for 64-bit n (bases 2..37).
 uint64_t mulmod(uint64_t a, uint64_t b, uint64_t m) {

@@ -190,6 +190,22 @@ engram_status engram_forward(const engram_ctx* ctx, int layer, const uint32_t* d
                              int64_t T, uint16_t* d_hidden, void* d_workspace,
                              float* d_gates, void* stream);
 
+/* engram_forward for callers that cannot allocate device memory.  The pages
+ * have no counterpart: this is a deployment variant.  A serving engine that
+ * reserves the GPU's memory for its own pools, or a plugin host that forbids
+ * its plugins to allocate, can pass only the buffers it already owns; this
+ * call needs no workspace argument because its scratch (the gate sums) lives
+ * in an 8 MiB buffer inside the library's device image, held on every GPU
+ * that loads the library until the process exits.  It makes no cudaMalloc or
+ * cudaFree call.  T is limited to what 8 MiB holds (8,738 tokens at hc 4,
+ * d 5,120); a larger T returns ENGRAM_EINVAL with the limit in the message.
+ * The first call on a device looks up the buffer's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture.  All calls share the buffer: calls whose kernels may overlap on the
+ * GPU (other streams, other threads) race on it - keep them on one stream. */
+engram_status engram_forward_noalloc(const engram_ctx* ctx, int layer, const uint32_t* d_windows,
+                                     int64_t T, uint16_t* d_hidden, float* d_gates, void* stream);
+
 /* a2 -> a4 fused, the part of the step that does not depend on hidden
  * ("DeepSeek V4.1 Flash 的 Engram", section "提前投影": hashing, gather and
  * projection depend only on the tokens and can run ahead of the layer):
