@@ -28,11 +28,13 @@ OK, EINVAL, ENOMEM, ECUDA, ESTATE, ETIMEOUT, EUNSUPPORTED, EBOUNDS = range(8)
 # Names exported by the library (the declarations of include/engram.h).
 EXPORTS = (
     "engram_ctx_create", "engram_ctx_destroy", "engram_layer_params",
-    "engram_layer_set_multipliers", "engram_layer_bind", "engram_table_fill",
+    "engram_layer_set_multipliers", "engram_layer_bind", "engram_layer_info",
+    "engram_table_fill",
     "engram_session_create", "engram_session_fork", "engram_session_reset",
     "engram_session_destroy", "engram_session_append", "engram_batch_append",
     "engram_workspace_bytes", "engram_hash", "engram_gather_dequant", "engram_project",
-    "engram_gate", "engram_forward", "engram_forward_noalloc", "engram_project_windows",
+    "engram_gate", "engram_forward", "engram_forward_noalloc", "engram_forward_staged",
+    "engram_forward_staged_workspace_bytes", "engram_project_windows",
     "engram_sync",
     "engram_last_error",
 )
@@ -54,10 +56,21 @@ class CtxDesc(C.Structure):
     ]
 
 
+BIND_BF16_OPERANDS = 1
+
+
 class LayerWeights(C.Structure):
     _fields_ = [
         ("table", C.c_void_p), ("scales", C.c_void_p), ("rows", C.c_uint64),
-        ("wkv", C.c_void_p), ("wq", C.c_void_p), ("wk", C.c_void_p),
+        ("wkv", C.c_void_p), ("wq", C.c_void_p), ("wk", C.c_void_p), ("flags", C.c_uint32),
+    ]
+
+
+class LayerInfo(C.Structure):
+    _fields_ = [
+        ("rows", C.c_uint64), ("bound", C.c_int32), ("fp16_operands", C.c_int32),
+        ("scale_min", C.c_uint32), ("scale_max", C.c_uint32), ("wkv_exp", C.c_int32),
+        ("a_exp_shift", C.c_int32), ("bucket_gather", C.c_int32),
     ]
 
 
@@ -79,6 +92,7 @@ def lib() -> C.CDLL:
             "engram_layer_params": [vp, C.c_int, vp, vp, vp, vp],
             "engram_layer_set_multipliers": [vp, C.c_int, vp],
             "engram_layer_bind": [vp, C.c_int, C.POINTER(LayerWeights)],
+            "engram_layer_info": [vp, C.c_int, C.POINTER(LayerInfo)],
             "engram_table_fill": [vp, C.c_uint64, vp, vp, C.c_uint64, C.c_uint64, vp],
             "engram_session_create": [vp, C.POINTER(vp)],
             "engram_session_fork": [vp, C.POINTER(vp)],
@@ -93,14 +107,16 @@ def lib() -> C.CDLL:
             "engram_forward": [vp, C.c_int, vp, i64, vp, vp, vp, vp],
             "engram_project_windows": [vp, C.c_int, vp, i64, vp, vp],
             "engram_forward_noalloc": [vp, C.c_int, vp, i64, vp, vp, vp],
+            "engram_forward_staged": [vp, C.c_int, vp, i64, vp, vp, vp, vp],
             "engram_sync": [vp, vp],
         }
         for name, args in sig.items():
             fn = getattr(L, name)
             fn.argtypes = args
             fn.restype = st
-        L.engram_workspace_bytes.argtypes = [vp, i64]
-        L.engram_workspace_bytes.restype = C.c_size_t
+        for name in ("engram_workspace_bytes", "engram_forward_staged_workspace_bytes"):
+            getattr(L, name).argtypes = [vp, i64]
+            getattr(L, name).restype = C.c_size_t
         L.engram_last_error.argtypes = []
         L.engram_last_error.restype = C.c_char_p
         _lib = L
@@ -176,9 +192,15 @@ def engram_layer_set_multipliers(ctx, layer: int, mult):
     _check(lib().engram_layer_set_multipliers(ctx, layer, m.ctypes.data))
 
 
-def engram_layer_bind(ctx, layer: int, table, scales, rows: int, wkv, wq, wk):
-    w = LayerWeights(_ptr(table), _ptr(scales), rows, _ptr(wkv), _ptr(wq), _ptr(wk))
+def engram_layer_bind(ctx, layer: int, table, scales, rows: int, wkv, wq, wk, flags: int = 0):
+    w = LayerWeights(_ptr(table), _ptr(scales), rows, _ptr(wkv), _ptr(wq), _ptr(wk), flags)
     _check(lib().engram_layer_bind(ctx, layer, C.byref(w)))
+
+
+def engram_layer_info(ctx, layer: int) -> dict:
+    info = LayerInfo()
+    _check(lib().engram_layer_info(ctx, layer, C.byref(info)))
+    return {name: getattr(info, name) for name, _ in LayerInfo._fields_}
 
 
 def engram_table_fill(ctx, seed: int, data, scale, row_begin: int, row_end: int, stream=None):
@@ -258,6 +280,16 @@ def engram_gate(ctx, layer, d_kv, d_windows, T, d_hidden, d_gates=None, stream=N
 def engram_forward(ctx, layer, d_windows, T, d_hidden, d_workspace, d_gates=None, stream=None):
     _check(lib().engram_forward(ctx, layer, _ptr(d_windows), T, _ptr(d_hidden), _ptr(d_workspace),
                                 _ptr(d_gates), _stream(stream)))
+
+
+def engram_forward_staged_workspace_bytes(ctx, T: int) -> int:
+    return int(lib().engram_forward_staged_workspace_bytes(ctx, T))
+
+
+def engram_forward_staged(ctx, layer, d_windows, T, d_hidden, d_workspace, d_gates=None,
+                          stream=None):
+    _check(lib().engram_forward_staged(ctx, layer, _ptr(d_windows), T, _ptr(d_hidden),
+                                       _ptr(d_workspace), _ptr(d_gates), _stream(stream)))
 
 
 def engram_forward_noalloc(ctx, layer, d_windows, T, d_hidden, d_gates=None, stream=None):

@@ -7,6 +7,8 @@
 #include <cuda_runtime.h>
 #include <string.h>
 
+#include <math.h>
+
 #include <algorithm>
 #include <new>
 #include <string>
@@ -123,7 +125,15 @@ struct LayerState {
     uint64_t rows = 0;
     bool bound = false;
     engram_layer_weights w{};
-    CUtensorMap tm_wkv{};
+    CUtensorMap tm_wkv{};          // the caller's BF16 wkv
+    // FP16 operand path of the fused kernels (see engram_layer_info)
+    bool f16 = false;
+    uint16_t* wkv_f16 = nullptr;   // library-owned copy, wkv x 2^wkv_exp
+    CUtensorMap tm_wkv_f16{};
+    int wkv_exp = 0;
+    int a_exp_shift = 0;
+    uint32_t scale_min = 0, scale_max = 0;
+    bool bucket_gather = false;    // whole 256-wide rows gathered once per tile and bucket
 };
 
 struct engram_ctx {
@@ -132,7 +142,7 @@ struct engram_ctx {
     std::vector<uint32_t> map;
     int nb = 0, K = 0, N = 0;
     std::vector<LayerState> layers;
-    uint32_t* d_err = nullptr;
+    uint32_t* d_err = nullptr;  // [0] error word, [1..3] bind-time scan results
     int device = -1;
     long long wait_limit_ns = 4000000000LL;
 };
@@ -205,6 +215,9 @@ MmaArgs mma_args(const engram_ctx* ctx, int layer, int64_t T) {
     a.scales = L.w.scales;
     a.rows = L.rows;
     a.row_dim = (int)ctx->desc.row_dim;
+    a.row_dim_log2 = 31 - __builtin_clz(ctx->desc.row_dim);
+    a.a_exp_shift = 0;
+    a.out_scale = 1.0f;
     a.wq = L.w.wq;
     a.wk = L.w.wk;
     a.hp = hash_params(ctx, layer);
@@ -291,6 +304,8 @@ engram_status engram_ctx_destroy(engram_ctx* ctx) {
         int cur = -1;
         cudaGetDevice(&cur);
         if (ctx->device >= 0) cudaSetDevice(ctx->device);
+        for (LayerState& L : ctx->layers)
+            if (L.wkv_f16) cudaFree(L.wkv_f16);
         cudaFree(ctx->d_err);
         if (cur >= 0) cudaSetDevice(cur);
     }
@@ -335,6 +350,7 @@ engram_status engram_layer_bind(engram_ctx* ctx, int layer, const engram_layer_w
         return fail(ENGRAM_ESTATE, "context already bound on another device");
     // The table may live in pinned host memory read through UVA.
     engram_layer_weights bw = *w;
+    bool host_table = false;
     for (const uint8_t** p : {&bw.table, &bw.scales}) {
         cudaPointerAttributes attr{};
         e = cudaPointerGetAttributes(&attr, *p);
@@ -346,23 +362,104 @@ engram_status engram_layer_bind(engram_ctx* ctx, int layer, const engram_layer_w
             if (!attr.devicePointer)
                 return fail(ENGRAM_EUNSUPPORTED, "host table not mapped into the device address space");
             *p = static_cast<const uint8_t*>(attr.devicePointer);
+            host_table = true;
         } else if (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged) {
             return fail(ENGRAM_EINVAL, "table pointer must be device or pinned host memory");
         }
     }
     if (!ctx->d_err) {
-        e = cudaMalloc(&ctx->d_err, sizeof(uint32_t));
+        e = cudaMalloc(&ctx->d_err, 4 * sizeof(uint32_t));
         if (e != cudaSuccess) return fail(ENGRAM_ENOMEM, "cudaMalloc of the error word");
-        e = cudaMemset(ctx->d_err, 0, sizeof(uint32_t));
+        e = cudaMemset(ctx->d_err, 0, 4 * sizeof(uint32_t));
         if (e != cudaSuccess) return cuda_fail(e, "cudaMemset");
         ctx->device = dev;
     }
     CUtensorMap tm;
-    e = make_tma_bf16(&tm, w->wkv, (uint64_t)ctx->N, (uint64_t)ctx->K, kBN);
+    e = make_tma_16bit(&tm, w->wkv, (uint64_t)ctx->N, (uint64_t)ctx->K, kBN, false);
     if (e != cudaSuccess) return cuda_fail(e, "wkv tensor map");
+
+    // Operand path of the fused kernels.  FP16 operands hold the same values
+    // exactly when (a) every E8M0 exponent of the table lies in a window of 23
+    // values, so code x 2^(s - 127 + shift) is exact in FP16 for one shift,
+    // and (b) wkv, scaled by 2^wkv_exp so that max |w| <= 2^15, is exact in
+    // FP16 for every weight above max|w| 2^-28 (smaller ones round to a
+    // multiple of 2^-(24 + wkv_exp)).  Otherwise the fused kernels decode to
+    // BF16 through fp32.
+    const uint32_t init[3] = {255u, 0u, 0u};
+    e = cudaMemcpy(ctx->d_err + 1, init, sizeof init, cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return cuda_fail(e, "bind scan init");
+    const uint64_t nscale = L.rows * (ctx->desc.row_dim / 32);
+    e = launch_scale_range(bw.scales, nscale, ctx->d_err + 1, 0);
+    if (e == cudaSuccess)
+        e = launch_absmax_bf16(w->wkv, (uint64_t)ctx->N * ctx->K, ctx->d_err + 3, 0);
+    uint32_t res[3] = {0, 0, 0};
+    if (e == cudaSuccess) e = cudaMemcpy(res, ctx->d_err + 1, sizeof res, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "bind scans");
+    const uint32_t smin = res[0], smax = res[1], wabs = res[2];
+    const bool want_f16 = !(w->flags & ENGRAM_BIND_BF16_OPERANDS);
+    const bool scales_fit = smax != 255u && smax >= smin && smax - smin <= 22u;
+    const bool w_finite = wabs < 0x7F80u;
+    if (L.wkv_f16) {
+        cudaFree(L.wkv_f16);
+        L.wkv_f16 = nullptr;
+    }
+    L.f16 = false;
+    if (want_f16 && scales_fit && w_finite) {
+        // exponent shift: all decoded values FP16-normal when the span allows
+        const int shift = (smax - smin <= 12u) ? 122 - (int)smin : 112 - (int)smin;
+        int wexp = 0;
+        if (wabs) {
+            uint32_t fb = wabs << 16;
+            float maxabs;
+            memcpy(&maxabs, &fb, sizeof maxabs);
+            int ex;
+            frexpf(maxabs, &ex);  // maxabs < 2^ex
+            wexp = 15 - ex;
+        }
+        const size_t bytes = (size_t)ctx->N * ctx->K * sizeof(uint16_t);
+        e = cudaMalloc(&L.wkv_f16, bytes);
+        if (e != cudaSuccess) {
+            L.wkv_f16 = nullptr;
+            return fail(ENGRAM_ENOMEM, "cudaMalloc of the FP16 wkv copy");
+        }
+        e = launch_bf16_to_f16(w->wkv, L.wkv_f16, (uint64_t)ctx->N * ctx->K, ldexpf(1.0f, wexp), 0);
+        if (e == cudaSuccess) e = cudaDeviceSynchronize();
+        if (e == cudaSuccess)
+            e = make_tma_16bit(&L.tm_wkv_f16, L.wkv_f16, (uint64_t)ctx->N, (uint64_t)ctx->K, kBN, true);
+        if (e != cudaSuccess) {
+            cudaFree(L.wkv_f16);
+            L.wkv_f16 = nullptr;
+            return cuda_fail(e, "FP16 wkv copy");
+        }
+        L.f16 = true;
+        L.wkv_exp = wexp;
+        L.a_exp_shift = shift;
+    }
+    // 256-wide rows are gathered whole, once per tile and bucket; other widths
+    // per 64-column k-block.
+    L.bucket_gather = L.f16 && ctx->desc.row_dim == 256;
+    (void)host_table;
+    L.scale_min = smin;
+    L.scale_max = smax;
     L.w = bw;
     L.tm_wkv = tm;
     L.bound = true;
+    return ok();
+}
+
+engram_status engram_layer_info(const engram_ctx* ctx, int layer, engram_layer_info_t* out) {
+    engram_status st = check_layer(ctx, layer, false);
+    if (st) return st;
+    if (!out) return fail(ENGRAM_EINVAL, "null argument");
+    const LayerState& L = ctx->layers[layer];
+    out->rows = L.rows;
+    out->bound = L.bound ? 1 : 0;
+    out->fp16_operands = L.f16 ? 1 : 0;
+    out->scale_min = L.scale_min;
+    out->scale_max = L.scale_max;
+    out->wkv_exp = L.wkv_exp;
+    out->a_exp_shift = L.a_exp_shift;
+    out->bucket_gather = L.bucket_gather ? 1 : 0;
     return ok();
 }
 
@@ -482,8 +579,9 @@ engram_status engram_batch_append(engram_session* const* sessions, const int32_t
 size_t engram_workspace_bytes(const engram_ctx* ctx, int64_t T) {
     if (!ctx || T <= 0) return 0;
     const size_t P = ctx->desc.d / kBN;
-    const size_t bytes = (size_t)T * ctx->desc.hc * P * 3 * sizeof(float);
-    return (bytes + 255) & ~(size_t)255;
+    const size_t part = ((size_t)T * ctx->desc.hc * P * 3 * sizeof(float) + 255) & ~(size_t)255;
+    const size_t counters = (((size_t)T + kBM - 1) / kBM * sizeof(uint32_t) + 255) & ~(size_t)255;
+    return part + counters;
 }
 
 engram_status engram_hash(const engram_ctx* ctx, int layer, const uint32_t* d_windows, int64_t T,
@@ -518,7 +616,7 @@ engram_status engram_project(const engram_ctx* ctx, int layer, const uint16_t* d
     if (T == 0) return ok();
     if (!d_emb || !d_kv || !aligned16(d_emb) || !aligned16(d_kv)) return fail(ENGRAM_EINVAL, "emb / kv");
     CUtensorMap tmA;
-    cudaError_t e = make_tma_bf16(&tmA, d_emb, (uint64_t)T, (uint64_t)ctx->K, kBM);
+    cudaError_t e = make_tma_16bit(&tmA, d_emb, (uint64_t)T, (uint64_t)ctx->K, kBM, false);
     if (e != cudaSuccess) return cuda_fail(e, "emb tensor map");
     MmaArgs a = mma_args(ctx, layer, T);
     a.n_tile_begin = 0;
@@ -560,18 +658,71 @@ engram_status engram_forward(const engram_ctx* ctx, int layer, const uint32_t* d
     a.hidden = d_hidden;
     a.partials = static_cast<float*>(d_workspace);
     a.gates = d_gates;
-    const int key_tiles = (int)(ctx->desc.hc * ctx->desc.d / kBN);
-    const int value_tiles = (int)(ctx->desc.d / kBN);
-    // key tiles: per-(token, branch, tile) sums; stream order then makes every
-    // sum visible to the value tiles, which gate and update hidden.
+    // one launch: key tiles publish their sums and count in per M block; a
+    // value tile's epilogue waits for its block's count before gating
+    const size_t part_bytes = (size_t)T * ctx->desc.hc * (ctx->desc.d / kBN) * 3 * sizeof(float);
+    a.counters = reinterpret_cast<uint32_t*>(static_cast<char*>(d_workspace) +
+                                             ((part_bytes + 255) & ~(size_t)255));
+    if (L.f16) {
+        a.a_exp_shift = L.a_exp_shift;
+        a.out_scale = ldexpf(1.0f, -(L.a_exp_shift + L.wkv_exp));
+    }
+    const CUtensorMap& tmB = L.f16 ? L.tm_wkv_f16 : L.tm_wkv;
     a.n_tile_begin = 0;
-    a.n_tiles = key_tiles;
-    cudaError_t e = launch_forward_phase(a, kEpiKeyPartial, L.tm_wkv, (cudaStream_t)stream);
-    if (e != cudaSuccess) return cuda_fail(e, "forward key-phase launch");
-    a.n_tile_begin = key_tiles;
-    a.n_tiles = value_tiles;
-    e = launch_forward_phase(a, kEpiValueUpdate, L.tm_wkv, (cudaStream_t)stream);
-    if (e != cudaSuccess) return cuda_fail(e, "forward value-phase launch");
+    a.n_tiles = ctx->N / kBN;
+    cudaError_t e = cudaMemsetAsync(a.counters, 0, sizeof(uint32_t) * a.m_blocks, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "forward counters");
+    e = launch_forward_phase(a, kEpiForward, L.f16, L.bucket_gather, tmB, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "forward launch");
+    return ok();
+}
+
+size_t engram_forward_staged_workspace_bytes(const engram_ctx* ctx, int64_t T) {
+    if (!ctx || T <= 0) return 0;
+    const size_t e = ((size_t)T * ctx->K * sizeof(uint16_t) + 255) & ~(size_t)255;
+    return e + engram_workspace_bytes(ctx, T);
+}
+
+engram_status engram_forward_staged(const engram_ctx* ctx, int layer, const uint32_t* d_windows,
+                                    int64_t T, uint16_t* d_hidden, void* d_workspace,
+                                    float* d_gates, void* stream) {
+    engram_status st = check_layer(ctx, layer, true);
+    if (st || (st = check_T(T))) return st;
+    if (T == 0) return ok();
+    if (!d_windows || !d_hidden || !d_workspace || !aligned16(d_windows) || !aligned16(d_hidden) ||
+        !aligned16(d_workspace))
+        return fail(ENGRAM_EINVAL, "windows / hidden / workspace (16-byte aligned)");
+    const LayerState& L = ctx->layers[layer];
+    uint16_t* e_scratch = static_cast<uint16_t*>(d_workspace);
+    char* rest = static_cast<char*>(d_workspace) +
+                 (((size_t)T * ctx->K * sizeof(uint16_t) + 255) & ~(size_t)255);
+    MmaArgs a = mma_args(ctx, layer, T);
+    a.windows = reinterpret_cast<const uint4*>(d_windows);
+    a.hidden = d_hidden;
+    a.partials = reinterpret_cast<float*>(rest);
+    a.gates = d_gates;
+    const size_t part_bytes = (size_t)T * ctx->desc.hc * (ctx->desc.d / kBN) * 3 * sizeof(float);
+    a.counters = reinterpret_cast<uint32_t*>(rest + ((part_bytes + 255) & ~(size_t)255));
+    if (L.f16) {
+        a.a_exp_shift = L.a_exp_shift;
+        a.out_scale = ldexpf(1.0f, -(L.a_exp_shift + L.wkv_exp));
+    }
+    a.n_tile_begin = 0;
+    a.n_tiles = ctx->N / kBN;
+    cudaStream_t s = (cudaStream_t)stream;
+    // 1: gather and dequantise every (token, bucket) row once into e
+    cudaError_t e = launch_gather_stage(hash_params(ctx, layer), a.windows, T,
+                                        (int)ctx->desc.row_dim, L.w.table, L.w.scales, L.rows,
+                                        L.f16, L.a_exp_shift, e_scratch, ctx->d_err, s);
+    if (e != cudaSuccess) return cuda_fail(e, "staged gather launch");
+    // 2: the forward GEMM reading e through TMA
+    CUtensorMap tmA;
+    e = make_tma_16bit(&tmA, e_scratch, (uint64_t)T, (uint64_t)ctx->K, kBM, L.f16);
+    if (e != cudaSuccess) return cuda_fail(e, "e tensor map");
+    e = cudaMemsetAsync(a.counters, 0, sizeof(uint32_t) * a.m_blocks, s);
+    if (e != cudaSuccess) return cuda_fail(e, "forward counters");
+    e = launch_forward_tma(a, L.f16, tmA, L.f16 ? L.tm_wkv_f16 : L.tm_wkv, s);
+    if (e != cudaSuccess) return cuda_fail(e, "staged forward launch");
     return ok();
 }
 
@@ -582,14 +733,19 @@ engram_status engram_project_windows(const engram_ctx* ctx, int layer, const uin
     if (T == 0) return ok();
     if (!d_windows || !d_kv || !aligned16(d_windows) || !aligned16(d_kv))
         return fail(ENGRAM_EINVAL, "windows / kv (16-byte aligned)");
+    const LayerState& L = ctx->layers[layer];
     MmaArgs a = mma_args(ctx, layer, T);
     a.windows = reinterpret_cast<const uint4*>(d_windows);
     a.kv = d_kv;
     a.ldkv = ctx->N;
     a.n_tile_begin = 0;
     a.n_tiles = ctx->N / kBN;
-    cudaError_t e = launch_forward_phase(a, kEpiStoreKv, ctx->layers[layer].tm_wkv,
-                                         (cudaStream_t)stream);
+    if (L.f16) {
+        a.a_exp_shift = L.a_exp_shift;
+        a.out_scale = ldexpf(1.0f, -(L.a_exp_shift + L.wkv_exp));
+    }
+    cudaError_t e = launch_forward_phase(a, kEpiStoreKv, L.f16, L.bucket_gather,
+                                         L.f16 ? L.tm_wkv_f16 : L.tm_wkv, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "fused projection launch");
     return ok();
 }

@@ -42,7 +42,9 @@ constexpr int kBK = 64;   // reduction slice per pipeline stage (128-byte rows)
 enum EpilogueMode : int {
     kEpiStoreKv = 0,   // write kv fp32
     kEpiKeyPartial = 1,  // key tiles: per-(token, branch, tile) sums
-    kEpiValueUpdate = 2  // value tiles: gates from the sums, hidden += g v
+    kEpiValueUpdate = 2, // value tiles: gates from the sums, hidden += g v
+    kEpiForward = 3      // both in one launch: a value tile's epilogue first waits
+                         // until every key tile of its M block has counted in
 };
 
 struct MmaArgs {
@@ -62,6 +64,9 @@ struct MmaArgs {
     const uint8_t* scales;
     uint64_t rows;
     int row_dim;
+    int row_dim_log2;
+    int a_exp_shift;       // FP16 operands: decoded value x 2^(scale - 127 + a_exp_shift)
+    float out_scale;       // accumulator x out_scale = kv (undoes the operand scaling)
     // epilogue
     float* kv;             // kEpiStoreKv: [T][ldkv]
     int64_t ldkv;
@@ -69,6 +74,7 @@ struct MmaArgs {
     const float* wq;       // [hc][d]
     const float* wk;       // [hc][d]
     float* partials;       // [T][hc][d / kBN][3]
+    uint32_t* counters;    // kEpiForward: finished key tiles per M block (zeroed per call)
     float* gates;          // [T][hc] or null
     HashParams hp;
 };
@@ -84,16 +90,32 @@ cudaError_t launch_gather(const Geometry& g, const uint32_t* rows, int64_t T,
 cudaError_t launch_gate(const Geometry& g, const float* kv, const uint4* windows, int64_t T,
                         uint16_t* hidden, const float* wq, const float* wk, float* gates,
                         cudaStream_t s);
+// Bind-time scans: out[0] = min, out[1] = max of n E8M0 bytes (out preset by
+// the caller to 255 / 0); out[2] = largest |x| of n BF16 values as its bit
+// pattern without the sign (out[2] preset to 0).
+cudaError_t launch_scale_range(const uint8_t* scales, uint64_t n, uint32_t* out, cudaStream_t s);
+cudaError_t launch_absmax_bf16(const uint16_t* x, uint64_t n, uint32_t* out, cudaStream_t s);
+// Staged forward, step 1: windows -> operand rows e [T][K] (FP16 or BF16).
+cudaError_t launch_gather_stage(const HashParams& hp, const uint4* windows, int64_t T, int row_dim,
+                                const uint8_t* table, const uint8_t* scales, uint64_t nrows,
+                                bool f16, int exp_shift, uint16_t* e, uint32_t* err,
+                                cudaStream_t s);
+// dst[i] = fp16(bf16 src[i] * scale), round to nearest even.
+cudaError_t launch_bf16_to_f16(const uint16_t* src, uint16_t* dst, uint64_t n, float scale,
+                               cudaStream_t s);
 
 // kernels_mma.cu
-// Host-side TMA descriptor for a row-major bf16 matrix [rows][cols] with a
-// (kBK x box_rows) box and 128-byte swizzle.
-cudaError_t make_tma_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
-                          uint32_t box_rows);
+// Host-side TMA descriptor for a row-major 16-bit (BF16 or FP16) matrix
+// [rows][cols] with a (kBK x box_rows) box and 128-byte swizzle.
+cudaError_t make_tma_16bit(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                           uint32_t box_rows, bool f16);
 cudaError_t launch_project(const MmaArgs& a, const CUtensorMap& tmA, const CUtensorMap& tmB,
                            cudaStream_t s);
-cudaError_t launch_forward_phase(const MmaArgs& a, int mode, const CUtensorMap& tmB,
-                                 cudaStream_t s);
+cudaError_t launch_forward_phase(const MmaArgs& a, int mode, bool f16, bool bucket,
+                                 const CUtensorMap& tmB, cudaStream_t s);
+// Staged forward, step 2: the whole forward GEMM with a TMA-fed A operand.
+cudaError_t launch_forward_tma(const MmaArgs& a, bool f16, const CUtensorMap& tmA,
+                               const CUtensorMap& tmB, cudaStream_t s);
 int device_sm_count();
 
 }  // namespace engram

@@ -127,6 +127,70 @@ __global__ void k_gather(const uint32_t* __restrict__ rows, int64_t T, int nb, i
     }
 }
 
+// Staged forward, step 1: windows -> dequantised operand rows in a scratch
+// matrix e [T][K] (FP16 scaled by 2^(s - 127 + exp_shift), or BF16).  Each table
+// row is read whole: row_dim / 16 lanes per row, 16 codes and their scale per
+// lane; the first lane of a row hashes its (token, bucket) pair.
+template <bool kF16>
+__global__ void k_gather_stage(const __grid_constant__ HashParams hp, const uint4* __restrict__ windows,
+                               int64_t T, int row_dim, const uint8_t* __restrict__ table,
+                               const uint8_t* __restrict__ scales, uint64_t nrows, int exp_shift,
+                               uint16_t* __restrict__ e, uint32_t* err) {
+    const int lpr = row_dim / 16;              // lanes per row
+    const int rpw = 32 / lpr;                  // rows per warp pass
+    const int lane = threadIdx.x & 31;
+    const int sub = lane / lpr, chunk = lane % lpr;
+    const int K = hp.nb * row_dim;
+    const int64_t items = T * hp.nb;
+    const int64_t warp0 = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t base = warp0 * rpw; base < items; base += nwarps * rpw) {
+        const int64_t item = base + sub;
+        const bool live_item = item < items;
+        const int64_t t = live_item ? item / hp.nb : 0;
+        const int b = live_item ? (int)(item - t * hp.nb) : 0;
+        uint32_t row = kMasked;
+        if (live_item && chunk == 0) {
+            row = hash_bucket(hp, windows[t], b);
+            if (row != kMasked && (uint64_t)row >= nrows) {
+                atomicOr(err, kErrBounds);
+                row = kMasked;
+            }
+        }
+        row = __shfl_sync(0xFFFFFFFFu, row, sub * lpr);
+        if (!live_item) continue;
+        uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
+        if (row != kMasked) {
+            const uint4 c = __ldg(reinterpret_cast<const uint4*>(table + (uint64_t)row * row_dim) + chunk);
+            const uint32_t se = __ldg(scales + (uint64_t)row * (row_dim / 32) + chunk / 2);
+            if (kF16) {
+                const int ex = (int)se - 127 + exp_shift;  // in [-24, 15] (checked at bind)
+                const uint32_t h = ex >= -14 ? (uint32_t)(ex + 15) << 10 : 1u << (ex + 24);
+                const uint32_t sc2 = h | (h << 16);
+                const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+                uint32_t o[8];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    asm("{\n\t.reg .b16 l, h;\n\t.reg .b32 a, b;\n\tmov.b32 {l, h}, %2;\n\t"
+                        "cvt.rn.f16x2.e4m3x2 a, l;\n\tcvt.rn.f16x2.e4m3x2 b, h;\n\t"
+                        "mul.rn.f16x2 %0, a, %3;\n\tmul.rn.f16x2 %1, b, %3;\n\t}"
+                        : "=r"(o[2 * q]), "=r"(o[2 * q + 1])
+                        : "r"(w[q]), "r"(sc2));
+                }
+                lo = make_uint4(o[0], o[1], o[2], o[3]);
+                hi = make_uint4(o[4], o[5], o[6], o[7]);
+            } else {
+                const float sf = e8m0_to_f32(se);
+                lo = decode8(c.x, c.y, sf);
+                hi = decode8(c.z, c.w, sf);
+            }
+        }
+        uint4* dst = reinterpret_cast<uint4*>(e + t * (int64_t)K + (int64_t)b * row_dim + 16 * chunk);
+        dst[0] = lo;
+        dst[1] = hi;
+    }
+}
+
 // a5 standalone: one CTA per token.  Pass 1 reduces, per branch, sum k^2,
 // sum h^2 and sum h w_q w_k k; pass 2 applies hidden += g v with one BF16
 // rounding.  Image rows (c_t == DEAD) are left untouched.
@@ -196,6 +260,56 @@ k_gate(const float* __restrict__ kv, const uint4* __restrict__ windows, int64_t 
     }
 }
 
+// Bind-time scans and the FP16 copy of wkv.
+__global__ void k_scale_range(const uint8_t* __restrict__ s, uint64_t n, uint32_t* out) {
+    uint32_t lo = 255u, hi = 0u;
+    const uint64_t nv = n / 16;
+    for (uint64_t i = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; i < nv;
+         i += (uint64_t)gridDim.x * blockDim.x) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(s) + i);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            const uint32_t b = (w[k >> 2] >> (8 * (k & 3))) & 0xFFu;
+            lo = min(lo, b);
+            hi = max(hi, b);
+        }
+    }
+    for (uint64_t i = nv * 16 + blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; i < n;
+         i += (uint64_t)gridDim.x * blockDim.x) {
+        lo = min(lo, (uint32_t)s[i]);
+        hi = max(hi, (uint32_t)s[i]);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        lo = min(lo, __shfl_xor_sync(0xFFFFFFFFu, lo, o));
+        hi = max(hi, __shfl_xor_sync(0xFFFFFFFFu, hi, o));
+    }
+    if ((threadIdx.x & 31) == 0) {
+        atomicMin(out, lo);
+        atomicMax(out + 1, hi);
+    }
+}
+
+__global__ void k_absmax_bf16(const uint16_t* __restrict__ x, uint64_t n, uint32_t* out) {
+    uint32_t m = 0;
+    for (uint64_t i = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; i < n;
+         i += (uint64_t)gridDim.x * blockDim.x)
+        m = max(m, (uint32_t)(x[i] & 0x7FFFu));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    if ((threadIdx.x & 31) == 0) atomicMax(out, m);
+}
+
+__global__ void k_bf16_to_f16(const uint16_t* __restrict__ src, uint16_t* __restrict__ dst,
+                              uint64_t n, float scale) {
+    for (uint64_t i = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; i < n;
+         i += (uint64_t)gridDim.x * blockDim.x) {
+        const float v = __uint_as_float((uint32_t)src[i] << 16) * scale;
+        dst[i] = __half_as_ushort(__float2half_rn(v));
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_table_fill(uint64_t seed, uint8_t* data, uint8_t* scale, uint64_t row_begin,
@@ -234,6 +348,44 @@ cudaError_t launch_gate(const Geometry& g, const float* kv, const uint4* windows
     if (T == 0) return cudaSuccess;
     const int grid = (int)std::min<int64_t>(T, (int64_t)sm_count() * 8);
     k_gate<<<grid, kGateThreads, 0, s>>>(kv, windows, T, g.hc, g.d, g.eps, hidden, wq, wk, gates);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_scale_range(const uint8_t* scales, uint64_t n, uint32_t* out, cudaStream_t s) {
+    if (n == 0) return cudaSuccess;
+    k_scale_range<<<grid_for((int64_t)std::min<uint64_t>(n / 16 + 1, 1ull << 40), 256, 8), 256, 0,
+                    s>>>(scales, n, out);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_absmax_bf16(const uint16_t* x, uint64_t n, uint32_t* out, cudaStream_t s) {
+    if (n == 0) return cudaSuccess;
+    k_absmax_bf16<<<grid_for((int64_t)n, 256, 8), 256, 0, s>>>(x, n, out);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bf16_to_f16(const uint16_t* src, uint16_t* dst, uint64_t n, float scale,
+                               cudaStream_t s) {
+    if (n == 0) return cudaSuccess;
+    k_bf16_to_f16<<<grid_for((int64_t)n, 256, 8), 256, 0, s>>>(src, dst, n, scale);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gather_stage(const HashParams& hp, const uint4* windows, int64_t T, int row_dim,
+                                const uint8_t* table, const uint8_t* scales, uint64_t nrows,
+                                bool f16, int exp_shift, uint16_t* e, uint32_t* err,
+                                cudaStream_t s) {
+    if (T == 0) return cudaSuccess;
+    const int threads = 256;
+    const int64_t rows_per_warp = 32 / (row_dim / 16);
+    const int64_t warps = (T * hp.nb + rows_per_warp - 1) / rows_per_warp;
+    const int grid = grid_for(warps * 32, threads, 8);
+    if (f16)
+        k_gather_stage<true><<<grid, threads, 0, s>>>(hp, windows, T, row_dim, table, scales, nrows,
+                                                      exp_shift, e, err);
+    else
+        k_gather_stage<false><<<grid, threads, 0, s>>>(hp, windows, T, row_dim, table, scales, nrows,
+                                                       exp_shift, e, err);
     return cudaGetLastError();
 }
 

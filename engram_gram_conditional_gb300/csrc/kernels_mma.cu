@@ -1,23 +1,38 @@
 // The wkv projection on the 5th-generation tensor cores (tcgen05 + TMEM), and
 // the fused Engram forward built on it (sm_103a).
 //
-// One persistent CTA per SM (320 threads, ~223 KB of shared memory) walks a
-// list of 128 x 256 output tiles.  Warp roles:
-//   warp 0      TMA producer: wkv tiles (and, unfused, the emb tiles) into a
-//               4-stage ring of 128-byte-swizzled K-major shared-memory tiles
-//   warp 1      MMA issuer: one thread issues tcgen05.mma kind::f16 (BF16 x
-//               BF16 -> F32) into one of two TMEM accumulators of 256 columns;
-//               the warp owns the TMEM allocation
-//   warps 2..5  (fused only) A-operand producers, one thread per token row:
-//               hash the token's window in registers, copy the selected MXFP8
-//               row slice and its E8M0 scales into a private cp.async ring,
-//               decode E4M3 x 2^E8M0 -> BF16 and write it straight into the
-//               swizzled A tile - the 6,144-vector never reaches HBM
-//   warps 6..9  epilogue: tcgen05.ld of the accumulator, then
-//               store kv (unfused projection), or per-(token, branch, tile)
-//               sums of k^2, h^2 and h w_q w_k k (key tiles), or gates from
-//               those sums and hidden += g v (value tiles) - kv never reaches
-//               HBM in the fused forward.
+// One persistent CTA per SM (512 threads) walks a list of 128 x 256 output
+// tiles; every tile reduces over K = 6,144 in 64-wide k-blocks.  Operands sit
+// in 128-byte-swizzled K-major shared-memory tiles: an A ring (128 tokens x 64)
+// and a B ring (256 wkv rows x 64).  Warp roles, by warpgroup (each group
+// sets its own register budget with setmaxnreg):
+//   warp 12     TMA producer: wkv tiles into the B ring (and, for the unfused
+//               projection, the emb tiles into the A ring)
+//   warp 13     MMA issuer: one thread issues tcgen05.mma kind::f16 into one
+//               of two TMEM accumulators of 256 columns; the warp owns TMEM
+//               (warps 12..15: 56 registers each, warps 14 and 15 idle)
+//   warps 0..7  fused A producers, 144 registers (16 token rows each): hash each token's
+//               window in registers, load the selected MXFP8 rows, decode
+//               E4M3 x 2^E8M0 and write the operand straight into the swizzled
+//               A tiles - the 6,144-vector never reaches HBM.  Two gathers:
+//                 bucket gather (256-wide rows): each table row is loaded whole
+//                 (16 lanes x 16 bytes, two rows per instruction) once per
+//                 tile and bucket, one bucket ahead in registers, and decoded
+//                 into the four A stages of its bucket at once (8-stage A
+//                 ring, 3-stage B ring).  Fetching whole rows matters: random
+//                 row fetches, not bytes, limit a gather on this GPU (about
+//                 0.12 rows per clock per SM whatever their size).
+//                 k-block gather (other row widths): per k-block, four lanes
+//                 load a row's 64-byte slice (4-stage rings).
+//               Operands are FP16 when they hold the values exactly (one
+//               e4m3x2->f16x2 conversion and one f16x2 multiply per pair;
+//               wkv as an exact FP16 copy scaled by a power of two), else BF16
+//               (decode through fp32)
+//   warps 8..11 epilogue, 168 registers: tcgen05.ld of the accumulator, then store kv
+//               (projection), or per-(token, branch, tile) sums of k^2, h^2
+//               and h w_q w_k k (key tiles), or gates from those sums and
+//               hidden += g v (value tiles) - kv never reaches HBM in the
+//               fused forward.
 // Every mbarrier wait is bounded: on time-out the kernel raises an abort flag,
 // sets the error word and all roles leave their loops and free TMEM.
 #include <cudaTypedefs.h>
@@ -31,31 +46,60 @@ namespace engram {
 
 namespace {
 
-constexpr int kThreads = 320;
-constexpr int kWarpTma = 0, kWarpMma = 1, kWarpProd = 2, kWarpEpi = 6;
-constexpr int kStages = 4;
+constexpr int kThreads = 512;  // four warpgroups
+constexpr int kProdWarps = 8;  // A producers: warps 0..7, 16 token rows each
+constexpr int kRowsPerProd = kBM / kProdWarps;
+constexpr int kWarpProd = 0, kWarpEpi = 8, kWarpTma = 12, kWarpMma = 13;
+// Register split (setmaxnreg): launch budget 512 x 128 = 65,536 registers;
+// 128 x (2 x 144 + 168 + 56) = 65,536 - the four shares add up to it exactly
+// (and each scheduler holds one warp of each group: 32 x 512 = 16,384).
+constexpr int kLaunchRegs = 128;
+constexpr int kRegsProd = 144, kRegsEpi = 168, kRegsCtl = 56;
+static_assert(kThreads * kLaunchRegs == 128 * (2 * kRegsProd + kRegsEpi + kRegsCtl),
+              "setmaxnreg shares must add up to the launch allocation");
 constexpr int kAStage = kBM * kBK * 2;  // 16 KB
 constexpr int kBStage = kBN * kBK * 2;  // 32 KB
-constexpr int kRawDepth = 3;            // k-blocks of raw MXFP8 in flight per producer
-constexpr int kRawRow = 80;             // 64 code bytes + 2 scale words + shifts
-constexpr int kOffA = 0;
-constexpr int kOffB = kOffA + kStages * kAStage;
-constexpr int kOffRaw = kOffB + kStages * kBStage;
-constexpr int kOffBar = kOffRaw + kRawDepth * kBM * kRawRow;
-constexpr int kNumBars = 2 * kStages + 4;
-constexpr int kOffTmem = kOffBar + kNumBars * 8;
-constexpr int kOffFlag = kOffTmem + 4;
-constexpr int kSmemUsed = kOffFlag + 4;
-constexpr int kSmemBytes = kSmemUsed + 1024;  // slack to align the base to 1024 B
+constexpr int kRowStride = kMaxBuckets + 1;  // row-index table stride (odd: no bank conflicts)
+#ifndef ENGRAM_PREFETCH
+#define ENGRAM_PREFETCH 3
+#endif
+constexpr int kPrefetch = ENGRAM_PREFETCH;   // k-blocks of row slices in flight per lane
 constexpr int kTmemCols = 2 * kBN;
-static_assert(kSmemBytes <= 232448, "shared memory above the sm_100 per-block limit");
-static_assert(kOffB % 1024 == 0 && kAStage % 1024 == 0 && kBStage % 1024 == 0,
-              "swizzled tiles need 1024-byte alignment");
+
+// Source of the A operand.
+enum ASource : int {
+    kASrcTma = 0,           // TMA tiles of a BF16 emb matrix (unfused projection)
+    kASrcGatherKb = 1,      // fused: k-block gather of 64-byte row slices
+    kASrcGatherBucket = 2,  // fused: bucket gather of whole 256-byte rows
+};
+
+// Shared-memory layout of each variant.
+template <int kASrc>
+struct Layout {
+    static constexpr int kA = kASrc == kASrcGatherBucket ? 8 : 4;  // A ring stages
+    static constexpr int kB = kASrc == kASrcGatherBucket ? 3 : 4;  // B ring stages
+    static constexpr int kOffA = 0;
+    static constexpr int kOffB = kOffA + kA * kAStage;
+    static constexpr int kOffRows = kOffB + kB * kBStage;
+    static constexpr int kRowsBytes = kASrc == kASrcGatherKb ? kBM * kRowStride * 4 : 0;
+    static constexpr int kOffBar = kOffRows + kRowsBytes;
+    // a_full[kA], a_empty[kA], b_full[kB], b_empty[kB], tfull[2], tempty[2]
+    static constexpr int kNumBars = 2 * kA + 2 * kB + 4;
+    static constexpr int kOffTmem = kOffBar + kNumBars * 8;
+    static constexpr int kOffFlag = kOffTmem + 4;
+    static constexpr int kBytes = kOffFlag + 4 + 1024;  // + slack to align the base to 1 KB
+    static_assert(kBytes <= 232448, "shared memory above the per-block limit");
+    static_assert(kOffB % 1024 == 0 && kOffRows % 1024 == 0, "swizzled tiles need 1 KB alignment");
+};
 
 // Instruction descriptor, kind::f16: F32 accumulate (bits 4-5 = 1), A and B
-// BF16 (bits 7-9 = 1, 10-12 = 1), both K-major, N >> 3 at bit 17, M >> 4 at 24.
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
-                            ((uint32_t)(kBN >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
+// both BF16 (bits 7-9 = 1, 10-12 = 1) or both FP16 (0, 0), both K-major,
+// N >> 3 at bit 17, M >> 4 at bit 24.
+template <bool kF16>
+__host__ __device__ constexpr uint32_t idesc() {
+    return (1u << 4) | (kF16 ? 0u : (1u << 7) | (1u << 10)) | ((uint32_t)(kBN >> 3) << 17) |
+           ((uint32_t)(kBM >> 4) << 24);
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return (uint32_t)__cvta_generic_to_shared(p);
@@ -110,17 +154,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
         "l"((uint64_t)map), "r"(bar), "r"(x), "r"(y)
         : "memory");
 }
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
 __device__ __forceinline__ void fence_proxy_async() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -129,29 +162,30 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
                  "r"(v.z), "r"(v.w)
                  : "memory");
 }
-__device__ __forceinline__ void st_shared_u32(uint32_t addr, uint32_t v) {
-    asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
-}
-__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
-    uint4 v;
-    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "r"(addr)
-                 : "memory");
-    return v;
-}
-__device__ __forceinline__ uint32_t ld_shared_u32(uint32_t addr) {
-    uint32_t v;
-    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
-    return v;
-}
 
 // ---- tcgen05 -------------------------------------------------------------------
+// Named barrier of the four epilogue warps (id 1; id 0 is __syncthreads).
+__device__ __forceinline__ void epilogue_bar() {
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
 __device__ __forceinline__ void tc_fence_before() {
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
 __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+template <int kRegs>
+__device__ __forceinline__ void setmaxnreg_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+template <int kRegs>
+__device__ __forceinline__ void setmaxnreg_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegs));
 }
 __device__ __forceinline__ void tmem_alloc(uint32_t slot, uint32_t ncols) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot),
@@ -169,12 +203,12 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
     return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) |
            ((uint64_t)(1024 >> 4) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
-__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                          uint32_t accumulate) {
+__device__ __forceinline__ void umma_f16kind(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                             uint32_t idesc_bits, uint32_t accumulate) {
     asm volatile(
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
+        "l"(adesc), "l"(bdesc), "r"(idesc_bits), "r"(accumulate)
         : "memory");
 }
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
@@ -214,108 +248,190 @@ __device__ __forceinline__ void tile_coords(const MmaArgs& a, int tile, int& mb,
 }
 
 // ---- fused A producer ------------------------------------------------------------
-struct RowCache {
-    int b;
-    uint32_t row;
+// Lane l of a producer warp owns the 16-column chunk c = l % 4 of each 64-column
+// k-block for the rows rsub + 8 j (j = 0..1, rsub = l / 4) of its 16-row slice:
+// the four lanes of a row load its 64 contiguous code bytes, one instruction
+// covers eight rows.
+struct RawKb {
+    uint4 code[kRowsPerProd / 8];      // 16 E4M3 codes per row slot
+    uint32_t scale[kRowsPerProd / 8];  // E8M0 exponent of those 16 columns
 };
 
-__device__ __forceinline__ uint32_t row_of(const MmaArgs& a, uint4 w, int b, RowCache& rc) {
-    if (b != rc.b) {
-        rc.b = b;
-        uint32_t r = hash_bucket(a.hp, w, b);
-        if (r != kMasked && (uint64_t)r >= a.rows) {
-            atomicOr(a.err, kErrBounds);
-            r = kMasked;
-        }
-        rc.row = r;
-    }
-    return rc.row;
-}
-
-// Copy k-block kb (64 columns) of one token's concatenated rows into its raw
-// slot: 64 code bytes at +0, the aligned 4-byte scale words at +64/+68, the
-// byte offsets of the scales inside those words at +72.  A masked row gets
-// zero codes and scale exponent 127, which decode to +0.
-__device__ __forceinline__ void issue_kblock(const MmaArgs& a, uint4 w, int kb, uint32_t slot,
-                                             RowCache& rc) {
-    const int sub = a.row_dim < 64 ? a.row_dim : 64;
-    const int nsub = 64 / sub;
-    uint32_t shifts = 0;
-    for (int j = 0; j < nsub; ++j) {
-        const int col = kb * 64 + j * sub;
-        const int b = col / a.row_dim;
-        const int c0 = col - b * a.row_dim;
-        const uint32_t row = row_of(a, w, b, rc);
-        const uint32_t dst = slot + (uint32_t)(j * sub);
-        if (row == kMasked) {
-            for (int q = 0; q < sub / 16; ++q) st_shared_v4(dst + q * 16, make_uint4(0, 0, 0, 0));
-            st_shared_u32(slot + 64 + 4 * j, 0x7F7F7F7Fu);
+__device__ __forceinline__ void load_kb(const MmaArgs& a, const uint32_t* rows_s, int m0, int c,
+                                        int kb, RawKb& o) {
+    const int col = kb * kBK + 16 * c;
+    const int b = col >> a.row_dim_log2;
+    const int c0 = col & (a.row_dim - 1);
+    const int groups_log2 = a.row_dim_log2 - 5;
+#pragma unroll
+    for (int j = 0; j < kRowsPerProd / 8; ++j) {
+        const uint32_t row = rows_s[(m0 + 8 * j) * kRowStride + b];
+        if (row != kMasked) {
+            o.code[j] = __ldg(reinterpret_cast<const uint4*>(a.table + ((uint64_t)row << a.row_dim_log2) + c0));
+            o.scale[j] = __ldg(a.scales + ((uint64_t)row << groups_log2) + (c0 >> 5));
         } else {
-            const uint8_t* src = a.table + (uint64_t)row * a.row_dim + c0;
-            for (int q = 0; q < sub / 16; ++q) cp_async16(dst + q * 16, src + q * 16);
-            const uint64_t sidx = (uint64_t)row * (a.row_dim / 32) + c0 / 32;
-            cp_async4(slot + 64 + 4 * j, a.scales + (sidx & ~3ull));
-            shifts |= (uint32_t)(sidx & 3ull) << (8 * j);
+            o.code[j] = make_uint4(0, 0, 0, 0);
+            o.scale[j] = 127u;
         }
     }
-    st_shared_u32(slot + 72, shifts);
 }
 
-// Decode a raw slot into row m of a swizzled A stage (128-byte rows; 16-byte
-// chunk q of row m lives at chunk q ^ (m % 8)).
-__device__ __forceinline__ void decode_kblock(uint32_t slot, uint32_t a_stage, int m, int row_dim) {
-    uint4 c[4];
+// 2^e in both halves of an f16x2, e in [-24, 15].
+__device__ __forceinline__ uint32_t f16x2_pow2(int e) {
+    const uint32_t h = e >= -14 ? (uint32_t)(e + 15) << 10 : 1u << (e + 24);
+    return h | (h << 16);
+}
+
+// Four E4M3 codes -> four FP16 values times 2^e (two f16x2, low code first).
+__device__ __forceinline__ void e4m3x4_f16_scaled(uint32_t w, uint32_t sc2, uint32_t& lo,
+                                                  uint32_t& hi) {
+    asm("{\n\t.reg .b16 l, h;\n\t.reg .b32 a, b;\n\tmov.b32 {l, h}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 a, l;\n\tcvt.rn.f16x2.e4m3x2 b, h;\n\t"
+        "mul.rn.f16x2 %0, a, %3;\n\tmul.rn.f16x2 %1, b, %3;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(w), "r"(sc2));
+}
+
+// Decode one k-block's raw codes into the A stage (row m of a 128-byte
+// swizzled K-major tile: 16-byte chunk q lives at chunk q ^ (m % 8)).
+template <bool kF16>
+__device__ __forceinline__ void store_kb(const RawKb& r, uint32_t a_stage, int m0, int c,
+                                         int exp_shift) {
 #pragma unroll
-    for (int q = 0; q < 4; ++q) c[q] = ld_shared_v4(slot + 16 * q);
-    const uint32_t sw0 = ld_shared_u32(slot + 64);
-    const uint32_t sw1 = ld_shared_u32(slot + 68);
-    const uint32_t sh = ld_shared_u32(slot + 72);
-    float sf0, sf1;
-    if (row_dim >= 64) {
-        const uint32_t s0 = (sh & 0xFFu) * 8u;
-        sf0 = e8m0_to_f32((sw0 >> s0) & 0xFFu);
-        sf1 = e8m0_to_f32((sw0 >> (s0 + 8u)) & 0xFFu);
-    } else {
-        sf0 = e8m0_to_f32((sw0 >> ((sh & 0xFFu) * 8u)) & 0xFFu);
-        sf1 = e8m0_to_f32((sw1 >> (((sh >> 8) & 0xFFu) * 8u)) & 0xFFu);
+    for (int j = 0; j < kRowsPerProd / 8; ++j) {
+        const int m = m0 + 8 * j;
+        uint32_t o[8];
+        if (kF16) {
+            const uint32_t sc2 = f16x2_pow2((int)r.scale[j] - 127 + exp_shift);
+            e4m3x4_f16_scaled(r.code[j].x, sc2, o[0], o[1]);
+            e4m3x4_f16_scaled(r.code[j].y, sc2, o[2], o[3]);
+            e4m3x4_f16_scaled(r.code[j].z, sc2, o[4], o[5]);
+            e4m3x4_f16_scaled(r.code[j].w, sc2, o[6], o[7]);
+        } else {
+            const float sf = e8m0_to_f32(r.scale[j]);
+            const uint4 lo = decode8(r.code[j].x, r.code[j].y, sf);
+            const uint4 hi = decode8(r.code[j].z, r.code[j].w, sf);
+            o[0] = lo.x; o[1] = lo.y; o[2] = lo.z; o[3] = lo.w;
+            o[4] = hi.x; o[5] = hi.y; o[6] = hi.z; o[7] = hi.w;
+        }
+        const uint32_t rowbase = a_stage + (uint32_t)m * 128u;
+        const uint32_t sw = (uint32_t)(m & 7);
+        st_shared_v4(rowbase + (((uint32_t)(2 * c) ^ sw) << 4), make_uint4(o[0], o[1], o[2], o[3]));
+        st_shared_v4(rowbase + (((uint32_t)(2 * c + 1) ^ sw) << 4), make_uint4(o[4], o[5], o[6], o[7]));
     }
-    const uint32_t rowbase = a_stage + (uint32_t)m * 128u;
-    const uint32_t sw = (uint32_t)(m & 7);
+}
+
+
+// ---- bucket gather ---------------------------------------------------------------
+// Lane l of a producer warp loads 16-byte chunk (l % 16) of rows 2 i + l / 16
+// (i = 0..7) of the warp's 16 rows: chunk c holds columns 16 c .. 16 c + 15 of
+// the 256-wide row, i.e. k-block c / 4 of the bucket, columns 16 (c % 4) ...
+// The row index of each token comes from the lane that hashed it (shuffle).
+struct BucketRows {
+    uint4 r[kRowsPerProd / 2];
+};
+
+__device__ __forceinline__ void load_bucket(const MmaArgs& a, uint32_t own_row, int lane,
+                                            BucketRows& o) {
+    const int half = lane >> 4, chunk = lane & 15;
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-        const uint4& cc = c[q >> 1];
-        const uint32_t w0 = (q & 1) ? cc.z : cc.x;
-        const uint32_t w1 = (q & 1) ? cc.w : cc.y;
-        const uint4 o = decode8(w0, w1, q < 4 ? sf0 : sf1);
-        st_shared_v4(rowbase + (((uint32_t)q ^ sw) << 4), o);
+    for (int i = 0; i < kRowsPerProd / 2; ++i) {
+        const uint32_t row = __shfl_sync(0xFFFFFFFFu, own_row, 2 * i + half);
+        if (row != kMasked)
+            o.r[i] = __ldg(reinterpret_cast<const uint4*>(a.table + ((uint64_t)row << 8)) + chunk);
+        else
+            o.r[i] = make_uint4(0, 0, 0, 0);
+    }
+}
+
+// Row of bucket b for this lane's token (bounds-checked) and its 8 scale bytes.
+__device__ __forceinline__ uint32_t own_bucket_row(const MmaArgs& a, uint4 w, int b) {
+    uint32_t r = hash_bucket(a.hp, w, b);
+    if (r != kMasked && (uint64_t)r >= a.rows) {
+        atomicOr(a.err, kErrBounds);
+        r = kMasked;
+    }
+    return r;
+}
+__device__ __forceinline__ uint2 own_scale_word(const MmaArgs& a, uint32_t row) {
+    if (row == kMasked) return make_uint2(0x7F7F7F7Fu, 0x7F7F7F7Fu);  // 2^0: zeros stay zeros
+    return __ldg(reinterpret_cast<const uint2*>(a.scales + ((uint64_t)row << 3)));
+}
+
+// Decode a loaded bucket into its four A stages (base stage index `it`).
+// The two 16-byte stores of a lane go to chunks 2 (c % 4) and 2 (c % 4) + 1 of
+// its row; odd k-blocks store the odd chunk first, so the eight lanes of a
+// shared-memory wavefront always hit eight different bank groups.
+template <bool kF16>
+__device__ __forceinline__ void decode_bucket(const MmaArgs& a, const BucketRows& br, uint2 sw,
+                                              uint32_t a_base, int kA, int it, int pw, int lane) {
+    const int half = lane >> 4, chunk = lane & 15;
+    const int kbl = chunk >> 2, cp = chunk & 3;
+    const int g = chunk >> 1;  // 32-column scale group of the chunk
+    const uint32_t stage = a_base + (uint32_t)(((it + kbl) % kA) * kAStage);
+    const uint32_t first = (uint32_t)(2 * cp + (kbl & 1));
+    const uint32_t second = first ^ 1u;
+#pragma unroll
+    for (int i = 0; i < kRowsPerProd / 2; ++i) {
+        const int tl = 2 * i + half;  // token lane of this slot
+        const int m = pw * kRowsPerProd + tl;
+        const uint32_t swx = __shfl_sync(0xFFFFFFFFu, sw.x, tl);
+        const uint32_t swy = __shfl_sync(0xFFFFFFFFu, sw.y, tl);
+        const uint32_t se = ((g < 4 ? swx : swy) >> (8 * (g & 3))) & 0xFFu;
+        uint4 lo, hi;  // columns 16 cp .. +7 and +8 .. +15
+        if (kF16) {
+            const uint32_t sc2 = f16x2_pow2((int)se - 127 + a.a_exp_shift);
+            e4m3x4_f16_scaled(br.r[i].x, sc2, lo.x, lo.y);
+            e4m3x4_f16_scaled(br.r[i].y, sc2, lo.z, lo.w);
+            e4m3x4_f16_scaled(br.r[i].z, sc2, hi.x, hi.y);
+            e4m3x4_f16_scaled(br.r[i].w, sc2, hi.z, hi.w);
+        } else {
+            const float sf = e8m0_to_f32(se);
+            lo = decode8(br.r[i].x, br.r[i].y, sf);
+            hi = decode8(br.r[i].z, br.r[i].w, sf);
+        }
+        const uint32_t rowbase = stage + (uint32_t)m * 128u;
+        const uint32_t swz = (uint32_t)(m & 7);
+        st_shared_v4(rowbase + ((first ^ swz) << 4), (kbl & 1) ? hi : lo);
+        st_shared_v4(rowbase + ((second ^ swz) << 4), (kbl & 1) ? lo : hi);
     }
 }
 
 // ---- the kernel ---------------------------------------------------------------------
-template <bool kFusedA, int kMode>
+template <int kASrc, bool kF16, int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
 k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
       const __grid_constant__ MmaArgs a) {
+    using L = Layout<kASrc>;
+    constexpr int kA = L::kA, kB = L::kB;
+    constexpr bool kFusedA = kASrc != kASrcTma;
     extern __shared__ uint8_t smem_dyn[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~(uintptr_t)1023);
     const uint32_t sbase = smem_u32(smem);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    const uint32_t bar0 = sbase + kOffBar;
-    auto full = [&](int s) { return bar0 + 8u * (uint32_t)s; };
-    auto empty = [&](int s) { return bar0 + 8u * (uint32_t)(kStages + s); };
-    auto tfull = [&](int acc) { return bar0 + 8u * (uint32_t)(2 * kStages + acc); };
-    auto tempty = [&](int acc) { return bar0 + 8u * (uint32_t)(2 * kStages + 2 + acc); };
-    auto a_stage = [&](int s) { return sbase + kOffA + (uint32_t)(s * kAStage); };
-    auto b_stage = [&](int s) { return sbase + kOffB + (uint32_t)(s * kBStage); };
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffFlag);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffTmem);
+    const uint32_t bar0 = sbase + L::kOffBar;
+    auto a_full = [&](int s) { return bar0 + 8u * (uint32_t)s; };
+    auto a_empty = [&](int s) { return bar0 + 8u * (uint32_t)(kA + s); };
+    auto b_full = [&](int s) { return bar0 + 8u * (uint32_t)(2 * kA + s); };
+    auto b_empty = [&](int s) { return bar0 + 8u * (uint32_t)(2 * kA + kB + s); };
+    auto tfull = [&](int acc) { return bar0 + 8u * (uint32_t)(2 * kA + 2 * kB + acc); };
+    auto tempty = [&](int acc) { return bar0 + 8u * (uint32_t)(2 * kA + 2 * kB + 2 + acc); };
+    const uint32_t a_base = sbase + L::kOffA;
+    auto a_stage = [&](int s) { return a_base + (uint32_t)(s * kAStage); };
+    auto b_stage = [&](int s) { return sbase + L::kOffB + (uint32_t)(s * kBStage); };
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffFlag);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffTmem);
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(full(s), kFusedA ? 1u + kBM : 1u);
-            mbar_init(empty(s), 1u);
+        for (int s = 0; s < kA; ++s) {
+            mbar_init(a_full(s), kFusedA ? (uint32_t)kProdWarps : 1u);  // producer warps or TMA
+            mbar_init(a_empty(s), 1u);
+        }
+        for (int s = 0; s < kB; ++s) {
+            mbar_init(b_full(s), 1u);
+            mbar_init(b_empty(s), 1u);
         }
         for (int acc = 0; acc < 2; ++acc) {
             mbar_init(tfull(acc), 1u);
@@ -343,6 +459,9 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
         atomicOr(a.err, kErrTimeout);
     };
 
+    if (warp >= kWarpTma) {
+        setmaxnreg_dec<kRegsCtl>();
+    }
     if (warp == kWarpTma) {
         if (lane == 0) {
             int it = 0;
@@ -352,16 +471,24 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
                 tile_coords(a, tile, mb, nt);
                 const int n0 = (a.n_tile_begin + nt) * kBN;
                 for (int kb = 0; kb < KB; ++kb, ++it) {
-                    const int s = it % kStages;
-                    const uint32_t ph = (uint32_t)(it / kStages) & 1u;
-                    if (!mbar_wait(empty(s), ph ^ 1u, abort_flag, lim)) {
+                    const int sb = it % kB;
+                    if (!mbar_wait(b_empty(sb), ((uint32_t)(it / kB) & 1u) ^ 1u, abort_flag, lim)) {
                         fail();
                         ok = false;
                         break;
                     }
-                    mbar_expect_tx(full(s), kFusedA ? kBStage : kAStage + kBStage);
-                    if (!kFusedA) tma_load_2d(a_stage(s), &tmA, full(s), kb * kBK, mb * kBM);
-                    tma_load_2d(b_stage(s), &tmB, full(s), kb * kBK, n0);
+                    mbar_expect_tx(b_full(sb), kBStage);
+                    tma_load_2d(b_stage(sb), &tmB, b_full(sb), kb * kBK, n0);
+                    if (!kFusedA) {
+                        const int sa = it % kA;
+                        if (!mbar_wait(a_empty(sa), ((uint32_t)(it / kA) & 1u) ^ 1u, abort_flag, lim)) {
+                            fail();
+                            ok = false;
+                            break;
+                        }
+                        mbar_expect_tx(a_full(sa), kAStage);
+                        tma_load_2d(a_stage(sa), &tmA, a_full(sa), kb * kBK, mb * kBM);
+                    }
                 }
             }
         }
@@ -379,62 +506,149 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * kBN);
                 for (int kb = 0; kb < KB; ++kb, ++it) {
-                    const int s = it % kStages;
-                    const uint32_t ph = (uint32_t)(it / kStages) & 1u;
-                    if (!mbar_wait(full(s), ph, abort_flag, lim)) {
+                    const int sa = it % kA, sb = it % kB;
+                    if (!mbar_wait(a_full(sa), (uint32_t)(it / kA) & 1u, abort_flag, lim) ||
+                        !mbar_wait(b_full(sb), (uint32_t)(it / kB) & 1u, abort_flag, lim)) {
                         fail();
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t ad = sdesc_sw128(a_stage(s));
-                    const uint64_t bd = sdesc_sw128(b_stage(s));
+                    const uint64_t ad = sdesc_sw128(a_stage(sa));
+                    const uint64_t bd = sdesc_sw128(b_stage(sb));
 #pragma unroll
-                    for (int k = 0; k < kBK / 16; ++k)  // 16 BF16 = 32 bytes per MMA
-                        umma_bf16(d_tmem, ad + 2ull * k, bd + 2ull * k, (kb | k) != 0);
-                    umma_commit(empty(s));
+                    for (int k = 0; k < kBK / 16; ++k)  // 16 elements = 32 bytes per MMA
+                        umma_f16kind(d_tmem, ad + 2ull * k, bd + 2ull * k, idesc<kF16>(),
+                                     (kb | k) != 0);
+                    umma_commit(a_empty(sa));
+                    umma_commit(b_empty(sb));
                 }
                 if (ok) umma_commit(tfull(acc));
             }
         }
+    } else if (warp >= kWarpTma) {
+        // warps 14, 15: idle
     } else if (warp < kWarpEpi) {
-        if (kFusedA) {
-            const int p = threadIdx.x - kWarpProd * 32;  // token row of the tile
-            const uint32_t raw = sbase + kOffRaw;
-            auto slot = [&](int j) { return raw + (uint32_t)((j * kBM + p) * kRawRow); };
+        setmaxnreg_inc<kRegsProd>();
+        if (kASrc == kASrcGatherBucket) {
+            // whole-row gather; rows of this warp: [16 pw, 16 pw + 16); lanes
+            // l and l + 16 both hash token 16 pw + (l % 16)
+            const int pw = warp - kWarpProd;
+            const int nbk = a.hp.nb;
+            int it = 0;
+            bool ok = true;
+            BucketRows R0, R1;
+            for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+                int mb, nt;
+                tile_coords(a, tile, mb, nt);
+                const int64_t t = (int64_t)mb * kBM + pw * kRowsPerProd + (lane & (kRowsPerProd - 1));
+                const uint4 w = t < a.T ? a.windows[t] : make_uint4(kDead, kDead, kDead, kDead);
+                uint32_t row0 = own_bucket_row(a, w, 0);
+                uint2 sw0 = own_scale_word(a, row0);
+                load_bucket(a, row0, lane, R0);
+                uint2 sw1 = make_uint2(0x7F7F7F7Fu, 0x7F7F7F7Fu);
+                // buckets in pairs so the two register sets keep static names
+                auto run = [&](int b, const BucketRows& cur, uint2 cur_sw, BucketRows& nxt,
+                               uint2& nxt_sw) -> bool {
+                    if (b + 1 < nbk) {  // the next bucket's loads go out first
+                        const uint32_t r = own_bucket_row(a, w, b + 1);
+                        nxt_sw = own_scale_word(a, r);
+                        load_bucket(a, r, lane, nxt);
+                    }
+                    int freed = 1;
+                    if (lane == 0) {
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            if (freed)
+                                freed = mbar_wait(a_empty((it + j) % kA),
+                                                  ((uint32_t)((it + j) / kA) & 1u) ^ 1u, abort_flag,
+                                                  lim);
+                    }
+                    freed = __shfl_sync(0xFFFFFFFFu, freed, 0);
+                    if (!freed) {
+                        if (lane == 0) fail();
+                        return false;
+                    }
+                    decode_bucket<kF16>(a, cur, cur_sw, a_base, kA, it, pw, lane);
+                    fence_proxy_async();
+                    __syncwarp();
+                    if (lane == 0) {
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) mbar_arrive(a_full((it + j) % kA));
+                    }
+                    it += 4;
+                    return true;
+                };
+                for (int b = 0; b < nbk && ok; b += 2) {
+                    ok = run(b, R0, sw0, R1, sw1);
+                    if (ok && b + 1 < nbk) ok = run(b + 1, R1, sw1, R0, sw0);
+                }
+            }
+        } else if (kASrc == kASrcGatherKb) {
+            const int pw = warp - kWarpProd;        // rows [16 pw, 16 pw + 16) of the tile
+            const int c = lane & 3;                 // 16-column chunk of each k-block
+            const int m0 = pw * kRowsPerProd + (lane >> 2);  // this lane's rows: m0 + 8 j
+            uint32_t* rows_s = reinterpret_cast<uint32_t*>(smem + L::kOffRows);
             int it = 0;
             bool ok = true;
             for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
                 int mb, nt;
                 tile_coords(a, tile, mb, nt);
-                const int64_t t = (int64_t)mb * kBM + p;
-                const uint4 w = t < a.T ? a.windows[t] : make_uint4(kDead, kDead, kDead, kDead);
-                RowCache rc{-1, kMasked};
-#pragma unroll
-                for (int j = 0; j < kRawDepth; ++j) {
-                    if (j < KB) issue_kblock(a, w, j, slot(j), rc);
-                    cp_async_commit();
-                }
-                for (int kb = 0; kb < KB; ++kb, ++it) {
-                    cp_async_wait<kRawDepth - 1>();
-                    const int s = it % kStages;
-                    const uint32_t ph = (uint32_t)(it / kStages) & 1u;
-                    if (!mbar_wait(empty(s), ph ^ 1u, abort_flag, lim)) {
-                        fail();
-                        ok = false;
-                        break;
+                {   // hash: lanes l, l + 16 <-> token, every bucket, into the row-index table
+                    const int m = pw * kRowsPerProd + (lane & (kRowsPerProd - 1));
+                    const int64_t t = (int64_t)mb * kBM + m;
+                    const uint4 w = t < a.T ? a.windows[t] : make_uint4(kDead, kDead, kDead, kDead);
+                    for (int b = 0; b < a.hp.nb; ++b) {
+                        uint32_t r = hash_bucket(a.hp, w, b);
+                        if (r != kMasked && (uint64_t)r >= a.rows) {
+                            atomicOr(a.err, kErrBounds);
+                            r = kMasked;
+                        }
+                        rows_s[m * kRowStride + b] = r;
                     }
-                    decode_kblock(slot(kb % kRawDepth), a_stage(s), p, a.row_dim);
-                    fence_proxy_async();
-                    mbar_arrive(full(s));
-                    if (kb + kRawDepth < KB) issue_kblock(a, w, kb + kRawDepth, slot(kb % kRawDepth), rc);
-                    cp_async_commit();
                 }
+                __syncwarp();
+                // Ring of kPrefetch k-blocks of loads in flight.  The loop body
+                // is unrolled kPrefetch times so every slot index is static:
+                // a register that still awaits its load is never copied (a copy
+                // would stall the warp until the load lands).
+                RawKb q[kPrefetch];
+#pragma unroll
+                for (int i = 0; i < kPrefetch; ++i)
+                    if (i < KB) load_kb(a, rows_s, m0, c, i, q[i]);
+                for (int kb0 = 0; kb0 < KB && ok; kb0 += kPrefetch) {
+#pragma unroll
+                    for (int u = 0; u < kPrefetch; ++u) {
+                        const int kb = kb0 + u;
+                        if (kb < KB && ok) {
+                            const int s = it % kA;
+                            const uint32_t ph = (uint32_t)(it / kA) & 1u;
+                            ++it;
+                            // one lane waits for the stage to be free, the warp follows
+                            int freed = 1;
+                            if (lane == 0) freed = mbar_wait(a_empty(s), ph ^ 1u, abort_flag, lim);
+                            freed = __shfl_sync(0xFFFFFFFFu, freed, 0);
+                            if (!freed) {
+                                if (lane == 0) fail();
+                                ok = false;
+                            } else {
+                                store_kb<kF16>(q[u], a_stage(s), m0, c, a.a_exp_shift);
+                                // every lane makes its writes visible to the tensor
+                                // core's (async) proxy, then one arrival per warp
+                                fence_proxy_async();
+                                __syncwarp();
+                                if (lane == 0) mbar_arrive(a_full(s));
+                                if (kb + kPrefetch < KB) load_kb(a, rows_s, m0, c, kb + kPrefetch, q[u]);
+                            }
+                        }
+                    }
+                }
+                __syncwarp();  // the row-index table is rewritten by the next tile
             }
-            cp_async_wait<0>();
         }
     } else {
         // ---- epilogue ----
+        setmaxnreg_inc<kRegsEpi>();
         const int q = warp & 3;  // TMEM lane quadrant this warp may read
         const int m = q * 32 + lane;
         int tc = 0;
@@ -443,8 +657,11 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
             tile_coords(a, tile, mb, nt);
             const int acc = tc & 1;
             const uint32_t aph = (uint32_t)(tc >> 1) & 1u;
-            if (!mbar_wait(tfull(acc), aph, abort_flag, lim)) {
-                fail();
+            int full_ok = 1;
+            if (lane == 0) full_ok = mbar_wait(tfull(acc), aph, abort_flag, lim);
+            full_ok = __shfl_sync(0xFFFFFFFFu, full_ok, 0);
+            if (!full_ok) {
+                if (lane == 0) fail();
                 break;
             }
             tc_fence_after();
@@ -461,11 +678,13 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
                         float4* dst = reinterpret_cast<float4*>(a.kv + t * a.ldkv + n0 + c * 32);
 #pragma unroll
                         for (int i = 0; i < 8; ++i)
-                            dst[i] = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
-                                                 __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
+                            dst[i] = make_float4(__uint_as_float(r[4 * i]) * a.out_scale,
+                                                 __uint_as_float(r[4 * i + 1]) * a.out_scale,
+                                                 __uint_as_float(r[4 * i + 2]) * a.out_scale,
+                                                 __uint_as_float(r[4 * i + 3]) * a.out_scale);
                     }
                 }
-            } else if (kMode == kEpiKeyPartial) {
+            } else if (kMode == kEpiKeyPartial || (kMode == kEpiForward && n0 < a.hc * a.d)) {
                 const int branch = n0 / a.d;
                 const int col0 = n0 - branch * a.d;
                 const bool text = t < a.T && a.windows[t].x != kDead;
@@ -497,7 +716,7 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
 #pragma unroll
                             for (int e = 0; e < 8; ++e) {
                                 const float h = (e & 1) ? bf16_hi(hw[e >> 1]) : bf16_lo(hw[e >> 1]);
-                                const float k = __uint_as_float(r[8 * i + e]);
+                                const float k = __uint_as_float(r[8 * i + e]) * a.out_scale;
                                 skk = fmaf(k, k, skk);
                                 shh = fmaf(h, h, shh);
                                 shk = fmaf(h * wqk[e], k, shk);
@@ -512,7 +731,30 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
                     pp[1] = shh;
                     pp[2] = shk;
                 }
-            } else {  // kEpiValueUpdate
+                if (kMode == kEpiForward) {
+                    // publish: every thread's sums, then one count for the M block
+                    __threadfence();
+                    epilogue_bar();
+                    if (warp == kWarpEpi && lane == 0) atomicAdd(a.counters + mb, 1u);
+                }
+            } else {  // value tile
+                if (kMode == kEpiForward) {
+                    // wait (bounded) until every key tile of this M block has counted in
+                    if (warp == kWarpEpi && lane == 0) {
+                        const uint32_t target = (uint32_t)(a.hc * a.d / kBN);
+                        const uint64_t t0 = globaltimer();
+                        uint32_t n = 0;
+                        while (ld_acquire_u32(a.counters + mb) < target) {
+                            if ((++n & 63u) == 0u &&
+                                ((long long)(globaltimer() - t0) > lim || *abort_flag)) {
+                                fail();
+                                break;
+                            }
+                        }
+                    }
+                    epilogue_bar();
+                    __threadfence();
+                }
                 const int cv = n0 - a.hc * a.d;
                 const bool text = t < a.T && a.windows[t].x != kDead;
                 const int P = a.d / kBN;
@@ -523,15 +765,15 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
                     if (b < a.hc && text) {
                         const float* pp = a.partials + (t * a.hc + b) * (int64_t)P * 3;
                         float skk = 0.f, shh = 0.f, shk = 0.f;
-                        for (int p = 0; p < P; ++p) {
-                            skk += pp[3 * p];
-                            shh += pp[3 * p + 1];
-                            shk += pp[3 * p + 2];
+                        for (int p = 0; p < P; ++p) {  // L2 reads: written by other CTAs
+                            skk += __ldcg(pp + 3 * p);
+                            shh += __ldcg(pp + 3 * p + 1);
+                            shk += __ldcg(pp + 3 * p + 2);
                         }
                         g[b] = gate_from_sums(skk, shh, shk, a.d, a.eps);
                     }
                 }
-                if (a.gates && nt == 0 && t < a.T) {
+                if (a.gates && n0 == a.hc * a.d && t < a.T) {
                     for (int b = 0; b < a.hc; ++b) a.gates[t * a.hc + b] = text ? g[b] : 0.f;
                 }
 #pragma unroll 1
@@ -552,8 +794,8 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
                                     uint32_t o[4];
 #pragma unroll
                                     for (int e2 = 0; e2 < 4; ++e2) {
-                                        const float v0 = __uint_as_float(r[8 * i + 2 * e2]);
-                                        const float v1 = __uint_as_float(r[8 * i + 2 * e2 + 1]);
+                                        const float v0 = __uint_as_float(r[8 * i + 2 * e2]) * a.out_scale;
+                                        const float v1 = __uint_as_float(r[8 * i + 2 * e2 + 1]) * a.out_scale;
                                         o[e2] = bf16x2_pack_rn(fmaf(g[b], v0, bf16_lo(hw[e2])),
                                                                fmaf(g[b], v1, bf16_hi(hw[e2])));
                                     }
@@ -588,27 +830,33 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
 
-template <bool kFusedA, int kMode>
+template <int kASrc, bool kF16, int kMode>
 cudaError_t launch(const MmaArgs& a, const CUtensorMap& tmA, const CUtensorMap& tmB,
                    cudaStream_t s) {
     static bool attr_set = false;
-    auto kern = k_mma<kFusedA, kMode>;
+    auto kern = k_mma<kASrc, kF16, kMode>;
+    constexpr int kSmem = Layout<kASrc>::kBytes;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
     const int total = a.m_blocks * a.n_tiles;
     if (total == 0) return cudaSuccess;
     const int grid = std::min(total, device_sm_count());
-    kern<<<grid, kThreads, kSmemBytes, s>>>(tmA, tmB, a);
+    kern<<<grid, kThreads, kSmem, s>>>(tmA, tmB, a);
     return cudaGetLastError();
 }
 
-}  // namespace
+template <int kASrc, bool kF16>
+cudaError_t launch_mode(const MmaArgs& a, int mode, const CUtensorMap& tmB, cudaStream_t s) {
+    if (mode == kEpiForward) return launch<kASrc, kF16, kEpiForward>(a, tmB, tmB, s);
+    return launch<kASrc, kF16, kEpiStoreKv>(a, tmB, tmB, s);
+}
 
-cudaError_t make_tma_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
-                          uint32_t box_rows) {
+}  // namespace
+cudaError_t make_tma_16bit(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                           uint32_t box_rows, bool f16) {
     std::call_once(g_encode_once, [] {
         void* fn = nullptr;
         cudaDriverEntryPointQueryResult q;
@@ -622,7 +870,7 @@ cudaError_t make_tma_bf16(CUtensorMap* map, const void* base, uint64_t rows, uin
     const cuuint64_t strides[1] = {cols * 2};
     const cuuint32_t box[2] = {(cuuint32_t)kBK, box_rows};
     const cuuint32_t estr[2] = {1, 1};
-    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+    CUresult r = g_encode(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -631,14 +879,22 @@ cudaError_t make_tma_bf16(CUtensorMap* map, const void* base, uint64_t rows, uin
 
 cudaError_t launch_project(const MmaArgs& a, const CUtensorMap& tmA, const CUtensorMap& tmB,
                            cudaStream_t s) {
-    return launch<false, kEpiStoreKv>(a, tmA, tmB, s);
+    return launch<kASrcTma, false, kEpiStoreKv>(a, tmA, tmB, s);
 }
 
-cudaError_t launch_forward_phase(const MmaArgs& a, int mode, const CUtensorMap& tmB,
-                                 cudaStream_t s) {
-    if (mode == kEpiKeyPartial) return launch<true, kEpiKeyPartial>(a, tmB, tmB, s);
-    if (mode == kEpiValueUpdate) return launch<true, kEpiValueUpdate>(a, tmB, tmB, s);
-    return launch<true, kEpiStoreKv>(a, tmB, tmB, s);
+cudaError_t launch_forward_tma(const MmaArgs& a, bool f16, const CUtensorMap& tmA,
+                               const CUtensorMap& tmB, cudaStream_t s) {
+    if (f16) return launch<kASrcTma, true, kEpiForward>(a, tmA, tmB, s);
+    return launch<kASrcTma, false, kEpiForward>(a, tmA, tmB, s);
+}
+
+// Operand paths of the fused kernels: bucket gather (256-wide rows) or k-block
+// gather, with FP16 operands; k-block gather with BF16 operands.
+cudaError_t launch_forward_phase(const MmaArgs& a, int mode, bool f16, bool bucket,
+                                 const CUtensorMap& tmB, cudaStream_t s) {
+    if (f16 && bucket) return launch_mode<kASrcGatherBucket, true>(a, mode, tmB, s);
+    if (f16) return launch_mode<kASrcGatherKb, true>(a, mode, tmB, s);
+    return launch_mode<kASrcGatherKb, false>(a, mode, tmB, s);
 }
 
 }  // namespace engram

@@ -51,7 +51,7 @@ class EngramLayerSet:
         return self.params[layer][3]
 
     def bind(self, layer: int, table_seed: int, wkv, wq, wk, host_table: bool = False,
-             stream=None):
+             stream=None, flags: int = 0):
         """Allocate and fill the layer's MXFP8 table, upload wkv / w_q / w_k, bind."""
         rows = self.rows(layer)
         rd = self.geom["row_dim"]
@@ -65,7 +65,7 @@ class EngramLayerSet:
         d_wkv = _as_device(wkv, torch.int16, self.device).view(self.N, self.K)
         d_wq = _as_device(wq, torch.float32, self.device).view(-1)
         d_wk = _as_device(wk, torch.float32, self.device).view(-1)
-        engram_layer_bind(self.ctx, layer, table, scales, rows, d_wkv, d_wq, d_wk)
+        engram_layer_bind(self.ctx, layer, table, scales, rows, d_wkv, d_wq, d_wk, flags)
         self.tensors[layer] = dict(table=table, scales=scales, wkv=d_wkv, wq=d_wq, wk=d_wk,
                                    table_seed=table_seed)
         return self.tensors[layer]

@@ -30,8 +30,11 @@
  *    engram_last_error() returns a thread-local message for the last error.
  *  - The caller owns every device and pinned-host buffer and every stream and
  *    the library never frees them.  The library owns engram_ctx, the sessions,
- *    the per-layer hash parameters and one 4-byte device error word per
- *    context (allocated at the first engram_layer_bind).
+ *    the per-layer hash parameters, a 16-byte device word per context (error
+ *    word and bind-time scan results, allocated at the first
+ *    engram_layer_bind) and, per bound layer on the FP16 operand path, an
+ *    FP16 copy of wkv (N x K x 2 bytes, allocated by engram_layer_bind and
+ *    freed by a rebind or engram_ctx_destroy).
  *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
  *    Device calls are asynchronous on that stream.  Faults found by a kernel
  *    (a row index outside the table, a wait that ran out) set the context's
@@ -102,7 +105,10 @@ typedef struct engram_ctx_desc {
 /* Weights of one layer.  table/scales: device memory, or pinned host memory
  * mapped into the device address space (read through UVA, vLLM "CPU 오프로드").
  * The scale array must be readable up to its size rounded up to 16 bytes.
- * wkv must be 16-byte aligned. */
+ * wkv must be 16-byte aligned.  The table's contents are scanned at bind
+ * (the E8M0 exponent range, see engram_layer_info): bind again after
+ * rewriting a table. */
+#define ENGRAM_BIND_BF16_OPERANDS 1u /* flags: fused kernels decode to BF16 only */
 typedef struct engram_layer_weights {
     const uint8_t* table;   /* [rows][row_dim] E4M3 codes                     */
     const uint8_t* scales;  /* [rows][row_dim / 32] E8M0 exponents            */
@@ -110,7 +116,29 @@ typedef struct engram_layer_weights {
     const uint16_t* wkv;    /* bf16 [N][K], device                            */
     const float* wq;        /* fp32 [hc][d], device                           */
     const float* wk;        /* fp32 [hc][d], device                           */
+    uint32_t flags;         /* 0 or ENGRAM_BIND_BF16_OPERANDS                  */
 } engram_layer_weights;
+
+/* How a bound layer runs.  The fused kernels feed the tensor cores FP16
+ * operands that hold the BF16 values exactly (fp16_operands = 1) when the
+ * table's E8M0 exponents span at most 23 values: each decoded value is the
+ * exact product code x 2^(e - 127 + a_exp_shift), and wkv is held as an FP16
+ * copy scaled by 2^wkv_exp (exact for every weight above 2^-28 of the largest;
+ * smaller ones round to a multiple of 2^-(24 + wkv_exp)); the accumulator is
+ * scaled back by 2^-(a_exp_shift + wkv_exp).  Otherwise (fp16_operands = 0)
+ * they decode to BF16 through fp32 and multiply the caller's BF16 wkv. */
+typedef struct engram_layer_info_t {
+    uint64_t rows;
+    int32_t bound;
+    int32_t fp16_operands;
+    uint32_t scale_min, scale_max;  /* E8M0 exponent range of the table       */
+    int32_t wkv_exp;
+    int32_t a_exp_shift;
+    int32_t bucket_gather;          /* 1: each 256-wide table row is loaded whole,
+                                       once per output tile (FP16 path, row_dim
+                                       256); 0: 64-column slices per k-block     */
+} engram_layer_info_t;
+engram_status engram_layer_info(const engram_ctx* ctx, int layer, engram_layer_info_t* out);
 
 /* Create a context.  token_map: host uint32 [vocab] compressed id of each
  * token (all < vc), copied.  No CUDA call is made. */
@@ -134,8 +162,10 @@ engram_status engram_layer_params(const engram_ctx* ctx, int layer, uint64_t* mu
 engram_status engram_layer_set_multipliers(engram_ctx* ctx, int layer, const uint64_t* mult);
 
 /* Bind a layer's weights (pointers are kept, not copied).  Needs a GPU: it
- * allocates the context's error word on the current device at first use and
- * encodes the wkv TMA descriptor. */
+ * allocates the context's device word at first use, scans the table's scale
+ * exponents and wkv's magnitude, builds the FP16 copy of wkv when the FP16
+ * operand path applies (engram_layer_info) and encodes the TMA descriptors.
+ * It synchronises the device. */
 engram_status engram_layer_bind(engram_ctx* ctx, int layer, const engram_layer_weights* w);
 
 /* Fill rows [row_begin, row_end) of a table with its deterministic contents:
@@ -190,6 +220,19 @@ engram_status engram_forward(const engram_ctx* ctx, int layer, const uint32_t* d
                              int64_t T, uint16_t* d_hidden, void* d_workspace,
                              float* d_gates, void* stream);
 
+/* a7, staged: the same result as engram_forward in two kernels.  Step 1
+ * gathers and dequantises every (token, bucket) row once into a scratch
+ * matrix e [T][K] in d_workspace; step 2 is the forward GEMM with its A
+ * operand read from e by TMA and the same gate epilogue (kv stays on chip).
+ * Unlike engram_forward, the 6,144-vectors pass through device memory (an
+ * L2-resident scratch of 12 KB per token for moderate T); in exchange each
+ * table row is read once per call instead of once per output tile.
+ * d_workspace: engram_forward_staged_workspace_bytes(ctx, T) bytes. */
+size_t engram_forward_staged_workspace_bytes(const engram_ctx* ctx, int64_t T);
+engram_status engram_forward_staged(const engram_ctx* ctx, int layer, const uint32_t* d_windows,
+                                    int64_t T, uint16_t* d_hidden, void* d_workspace,
+                                    float* d_gates, void* stream);
+
 /* engram_forward for callers that cannot allocate device memory.  The pages
  * have no counterpart: this is a deployment variant.  A serving engine that
  * reserves the GPU's memory for its own pools, or a plugin host that forbids
@@ -197,7 +240,7 @@ engram_status engram_forward(const engram_ctx* ctx, int layer, const uint32_t* d
  * call needs no workspace argument because its scratch (the gate sums) lives
  * in an 8 MiB buffer inside the library's device image, held on every GPU
  * that loads the library until the process exits.  It makes no cudaMalloc or
- * cudaFree call.  T is limited to what 8 MiB holds (8,738 tokens at hc 4,
+ * cudaFree call.  T is limited to what 8 MiB holds (8,737 tokens at hc 4,
  * d 5,120); a larger T returns ENGRAM_EINVAL with the limit in the message.
  * The first call on a device looks up the buffer's device address (once per
  * device, with that device current); make that first call before any stream

@@ -72,7 +72,7 @@ class Setup:
         torch.cuda.empty_cache()
 
 
-def setup_workload(name: str, layers=None, host_table=False, **overrides) -> Setup:
+def setup_workload(name: str, layers=None, host_table=False, flags=0, **overrides) -> Setup:
     import dataclasses
 
     w = dataclasses.replace(synth.WORKLOADS[name], **overrides) if overrides else \
@@ -85,7 +85,7 @@ def setup_workload(name: str, layers=None, host_table=False, **overrides) -> Set
         if l in layers:
             Wl = synth.wkv_bf16(w, l)
             q, k = synth.wq_wk(w, l)
-            model.bind(l, w.table_seeds[l], Wl, q, k, host_table=host_table)
+            model.bind(l, w.table_seeds[l], Wl, q, k, host_table=host_table, flags=flags)
         else:
             Wl = q = k = None
         W.append(Wl)

@@ -42,6 +42,24 @@ def prefill():
     s.close()
 
 
+@pytest.fixture(scope="module")
+def tiny_bf16():
+    s = setup_workload("tiny", flags=eg.BIND_BF16_OPERANDS)
+    yield s
+    s.close()
+
+
+def test_layer_info_selects_the_operand_path(tiny, tiny_bf16, prefill):
+    for s in (tiny, prefill):
+        info = eg.engram_layer_info(s.model.ctx, 0)
+        assert info["bound"] == 1 and info["rows"] == s.model.rows(0)
+        assert (info["scale_min"], info["scale_max"]) == (119, 127)  # table exponents
+        assert info["fp16_operands"] == 1 and info["a_exp_shift"] == 3
+        wmax = np.abs(bf16_f64(s.W[0])).max()
+        assert 2.0**14 <= wmax * 2.0 ** info["wkv_exp"] <= 2.0**15
+    assert eg.engram_layer_info(tiny_bf16.model.ctx, 0)["fp16_operands"] == 0
+
+
 def gpu_rows(s, win, layer=0):
     T = win.shape[0]
     d_win = to_dev(win)
@@ -132,11 +150,15 @@ def test_project_tiny(tiny, sessions, per):
         e = O.gather(g, tiny.w.table_seeds[0], O.hash_rows(g, tiny.oparams[0], win[t]))
         ref = O.project(g, tiny.W[0], e)
         check_kv(kv[t], ref, tiny.W[0], e, tiny.w.K, f"token {t}")
-    # the fused hash+gather+projection gives the same kv, bit for bit
+    # the fused hash+gather+projection: FP16 operands hold the same values and
+    # the scalings are powers of two, so kv matches the unfused BF16 GEMM
     d_kv2 = torch.full_like(d_kv, float("nan"))
     eg.engram_project_windows(tiny.model.ctx, 0, to_dev(win), T, d_kv2)
     eg.engram_sync(tiny.model.ctx)
-    assert torch.equal(d_kv, d_kv2)
+    kv2 = d_kv2.cpu().numpy()
+    for t in range(T):
+        e = O.gather(g, tiny.w.table_seeds[0], O.hash_rows(g, tiny.oparams[0], win[t]))
+        check_kv(kv2[t], O.project(g, tiny.W[0], e), tiny.W[0], e, tiny.w.K, f"fused token {t}")
 
 
 def test_project_full_geometry_sampled(prefill):
@@ -181,24 +203,28 @@ def test_gate_alone_on_oracle_kv(tiny):
 
 # ---- a7: the fused forward --------------------------------------------------------------
 
-def run_forward(s, win, hidden, layer=0):
+def run_forward(s, win, hidden, layer=0, staged=False):
     T = win.shape[0]
     d_h = to_dev(hidden)
-    d_ws = torch.empty(max(16, eg.engram_workspace_bytes(s.model.ctx, T)), dtype=torch.uint8,
-                       device="cuda")
+    ws = (eg.engram_forward_staged_workspace_bytes if staged else eg.engram_workspace_bytes)
+    d_ws = torch.empty(max(16, ws(s.model.ctx, T)), dtype=torch.uint8, device="cuda")
     d_g = torch.full((T, s.w.hc), float("nan"), dtype=torch.float32, device="cuda")
-    eg.engram_forward(s.model.ctx, layer, to_dev(win), T, d_h, d_ws, d_g)
+    fwd = eg.engram_forward_staged if staged else eg.engram_forward
+    fwd(s.model.ctx, layer, to_dev(win), T, d_h, d_ws, d_g)
     eg.engram_sync(s.model.ctx)
     return from_dev(d_h, np.uint16), d_g.cpu().numpy()
 
 
+@pytest.mark.parametrize("entry", ["fused", "staged"])
+@pytest.mark.parametrize("path", ["fp16", "bf16"])
 @pytest.mark.parametrize("sessions,per,spans", [(1, 64, [(20, 4)]), (3, 70, [(0, 2), (50, 9)]),
                                                 (1, 1, []), (2, 129, [(128, 1)])])
-def test_forward_tiny_all_tokens(tiny, sessions, per, spans):
+def test_forward_tiny_all_tokens(tiny, tiny_bf16, path, entry, sessions, per, spans):
+    tiny = tiny if path == "fp16" else tiny_bf16
     win, _, _ = prefill_windows(tiny, sessions, per, spans)
     T = win.shape[0]
     hidden = synth.hidden_bf16(tiny.w, T)
-    h, gates = run_forward(tiny, win, hidden)
+    h, gates = run_forward(tiny, win, hidden, staged=entry == "staged")
     ref = O.forward(geom(tiny.w), tiny.w.table_seeds[0], tiny.oparams[0], tiny.W[0], tiny.wq[0],
                     tiny.wk[0], win, hidden, np.arange(T), nthreads=4)
     check_hidden(h, ref["h_bf16"], "forward")
@@ -211,11 +237,12 @@ def test_forward_tiny_all_tokens(tiny, sessions, per, spans):
     assert np.array_equal(h[allmasked], hidden[allmasked])
 
 
-def test_forward_full_geometry_sampled(prefill):
+@pytest.mark.parametrize("entry", ["fused", "staged"])
+def test_forward_full_geometry_sampled(prefill, entry):
     win, _, _ = prefill_windows(prefill, 1, 2048)
     T = 2048
     hidden = synth.hidden_bf16(prefill.w, T)
-    h, gates = run_forward(prefill, win, hidden)
+    h, gates = run_forward(prefill, win, hidden, staged=entry == "staged")
     sample = np.array([0, 1, 126, 127, 128, 129, 1023, 2046, 2047, 700])
     ref = O.forward(geom(prefill.w), prefill.w.table_seeds[0], prefill.oparams[0], prefill.W[0],
                     prefill.wq[0], prefill.wk[0], win, hidden, sample, nthreads=8)
@@ -237,3 +264,19 @@ def test_forward_edge_cases(tiny):
     hidden = synth.hidden_bf16(tiny.w, 40)
     h, gates = run_forward(tiny, win, hidden)
     assert np.array_equal(h, hidden) and (gates == 0).all()
+
+
+def test_forward_full_geometry_bf16_operands_sampled():
+    s = setup_workload("prefill_2048", flags=eg.BIND_BF16_OPERANDS)
+    try:
+        assert eg.engram_layer_info(s.model.ctx, 0)["fp16_operands"] == 0
+        win, _, _ = prefill_windows(s, 1, 2048, spans=[(1000, 100)])
+        hidden = synth.hidden_bf16(s.w, 2048)
+        h, gates = run_forward(s, win, hidden)
+        sample = np.array([0, 127, 128, 999, 1000, 1100, 1101, 1102, 2047])
+        ref = O.forward(geom(s.w), s.w.table_seeds[0], s.oparams[0], s.W[0], s.wq[0], s.wk[0],
+                        win, hidden, sample, nthreads=8)
+        check_hidden(h[sample], ref["h_bf16"], "forward 2048 bf16 operands")
+        assert np.abs(gates[sample] - ref["gates"]).max() <= 1e-3
+    finally:
+        s.close()

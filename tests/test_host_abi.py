@@ -226,7 +226,8 @@ def test_device_calls_validate_before_launch():
         eg.engram_hash(ctx, 0, 8, 1, 16)  # misaligned windows
     assert e.value.status == eg.EINVAL
     eg.engram_hash(ctx, 0, None, 0, None)  # T = 0 is a no-op
-    assert eg.engram_workspace_bytes(ctx, 64) == 64 * 2 * 1 * 3 * 4
+    # gate sums [T][hc][d/256][3] fp32 and one counter per 128-token block, 256-byte aligned
+    assert eg.engram_workspace_bytes(ctx, 64) == 64 * 2 * 1 * 3 * 4 + 256
     assert eg.engram_workspace_bytes(ctx, 0) == 0
     eg.engram_ctx_destroy(ctx)
 
