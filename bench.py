@@ -4,7 +4,9 @@
 One step = the whole hot path over one batch: the 2,048-token prefill at full
 geometry (24 MXFP8 rows of 256 from a 16.0M-row table, wkv 25,600 x 6,144, 4
 hyper-connection branches of 5,120).  `value` is device-timed (CUDA events,
-inputs resident in HBM) tokens/s per layer of engram_forward; `e2e` is the
+inputs resident in HBM) tokens/s per layer of the forward step through the
+faster of the two forward entries (engram_forward_staged; the single fused
+kernel engram_forward is reported beside it under "fused"); `e2e` is the
 same metric through the C ABI with host buffers: append on the host, pinned
 H2D of windows and hidden, the forward, D2H of the updated hidden.
 
@@ -302,10 +304,15 @@ def main():
         hid_h.append(synth.normal_bf16((T, w.hc, w.d), 1.0, w.seed, 1000 + base_session + i))
     d_win = [torch.from_numpy(x.view(np.int32)).to(dev) for x in win_h]
     d_hid = [torch.from_numpy(x.view(np.int16)).to(dev) for x in hid_h]
-    d_ws = torch.empty(eg.engram_workspace_bytes(ctx, T), dtype=torch.uint8, device=dev)
+    d_ws = torch.empty(eg.engram_forward_staged_workspace_bytes(ctx, T), dtype=torch.uint8,
+                       device=dev)
     sptr = stream.cuda_stream
 
     def step(i):
+        j = i % POOL
+        eg.engram_forward_staged(ctx, 0, d_win[j], T, d_hid[j], d_ws, None, sptr)
+
+    def step_fused(i):
         j = i % POOL
         eg.engram_forward(ctx, 0, d_win[j], T, d_hid[j], d_ws, None, sptr)
 
@@ -335,6 +342,14 @@ def main():
     flops_call = flop_tok * T
     achieved = flops_call / (ms_local / args.steps / 1000.0) / 1e12
 
+    # the single fused kernel (engram_forward) on the same batches
+    fused_steps = max(1, min(args.steps, 500))
+    for i in range(min(args.warmup, 5)):
+        step_fused(i)
+    ms_fused = timed(step_fused, fused_steps, stream)
+    eg.engram_sync(ctx, sptr)
+    fused_tf = flops_call / (ms_fused / 1000.0) / 1e12
+
     # ---- e2e through the C ABI with host buffers ----
     h_win = torch.empty((T, 4), dtype=torch.int32, pin_memory=True)
     h_hid_in = [torch.from_numpy(x.view(np.int16)).pin_memory() for x in hid_h[:2]]
@@ -350,7 +365,7 @@ def main():
         eg.engram_session_destroy(s)
         e_win.copy_(h_win, non_blocking=True)
         e_hid.copy_(h_hid_in[i % 2], non_blocking=True)
-        eg.engram_forward(ctx, 0, e_win, T, e_hid, d_ws, None, sptr)
+        eg.engram_forward_staged(ctx, 0, e_win, T, e_hid, d_ws, None, sptr)
         h_hid_out.copy_(e_hid, non_blocking=True)
         stream.synchronize()
 
@@ -372,17 +387,24 @@ def main():
         "value": value, "unit": "tokens/s", "n_gpus": dist.world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": dict(workload_config(w), table_rows=rows, parallelism=f"replicas x{dist.world}"),
+        "config": dict(workload_config(w), table_rows=rows, parallelism=f"replicas x{dist.world}",
+                       entry="engram_forward_staged"),
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16"],
                      "unit": "TFLOP/s", "frac": achieved / peaks["bf16"], "traffic": None,
-                     "kernel": "k_mma fused forward (key + value launches of one engram_forward)",
+                     "kernel": "engram_forward_staged: k_gather_stage + k_mma (TMA-fed A, gate "
+                               "epilogue); time per call covers both launches",
                      "peak_kind": f"bf16 dense burst, {peaks['src']}",
                      "frac_of_sustained": achieved / peaks["bf16_sus"],
                      "flop_per_call": flops_call},
+        "fused": {"entry": "engram_forward (one kernel: hash, gather and decode into the "
+                           "shared-memory operand tiles, GEMM, gate epilogue)",
+                  "ms_per_step": ms_fused, "tokens_per_s": T / (ms_fused / 1000.0),
+                  "achieved_tflops": fused_tf, "frac": fused_tf / peaks["bf16"],
+                  "steps": fused_steps},
         "e2e": {"value": e2e_value, "unit": "tokens/s",
                 "h2d_bytes_per_step": T * 16 + T * w.hc * w.d * 2,
                 "d2h_bytes_per_step": T * w.hc * w.d * 2, "steps": e2e_steps},
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": 2 * args.steps,  # k_gather_stage + k_mma per step
         "clocks": clk,
     }
 
