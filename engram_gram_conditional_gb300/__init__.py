@@ -35,7 +35,7 @@ EXPORTS = (
     "engram_workspace_bytes", "engram_hash", "engram_gather_dequant", "engram_project",
     "engram_gate", "engram_forward", "engram_forward_noalloc", "engram_forward_staged",
     "engram_forward_staged_workspace_bytes", "engram_project_windows",
-    "engram_sync",
+    "engram_sync", "engram_ctx_set_wait_limit", "engram_debug_starve_operand",
     "engram_last_error",
 )
 
@@ -109,6 +109,8 @@ def lib() -> C.CDLL:
             "engram_forward_noalloc": [vp, C.c_int, vp, i64, vp, vp, vp],
             "engram_forward_staged": [vp, C.c_int, vp, i64, vp, vp, vp, vp],
             "engram_sync": [vp, vp],
+            "engram_ctx_set_wait_limit": [vp, i64],
+            "engram_debug_starve_operand": [vp, C.c_int],
         }
         for name, args in sig.items():
             fn = getattr(L, name)
@@ -302,6 +304,14 @@ def engram_forward_noalloc(ctx, layer, d_windows, T, d_hidden, d_gates=None, str
 def engram_project_windows(ctx, layer, d_windows, T, d_kv, stream=None):
     _check(lib().engram_project_windows(ctx, layer, _ptr(d_windows), T, _ptr(d_kv),
                                         _stream(stream)))
+
+
+def engram_ctx_set_wait_limit(ctx, ns: int):
+    _check(lib().engram_ctx_set_wait_limit(ctx, ns))
+
+
+def engram_debug_starve_operand(ctx, on: bool):
+    _check(lib().engram_debug_starve_operand(ctx, 1 if on else 0))
 
 
 def engram_sync(ctx, stream=None):

@@ -145,6 +145,7 @@ struct engram_ctx {
     uint32_t* d_err = nullptr;  // [0] error word, [1..3] bind-time scan results
     int device = -1;
     long long wait_limit_ns = 4000000000LL;
+    int starve_b = 0;
 };
 
 struct engram_session {
@@ -211,6 +212,7 @@ MmaArgs mma_args(const engram_ctx* ctx, int layer, int64_t T) {
     a.eps = (float)ctx->desc.eps;
     a.err = ctx->d_err;
     a.wait_limit_ns = ctx->wait_limit_ns;
+    a.starve_b = ctx->starve_b;
     a.table = L.w.table;
     a.scales = L.w.scales;
     a.rows = L.rows;
@@ -766,6 +768,18 @@ engram_status engram_sync(const engram_ctx* ctx, void* stream) {
             return fail(ENGRAM_EBOUNDS, "a kernel met a row index outside the table");
         }
     }
+    return ok();
+}
+
+engram_status engram_ctx_set_wait_limit(engram_ctx* ctx, int64_t ns) {
+    if (!ctx || ns < 1000) return fail(ENGRAM_EINVAL, "wait limit must be >= 1 us");
+    ctx->wait_limit_ns = ns;
+    return ok();
+}
+
+engram_status engram_debug_starve_operand(engram_ctx* ctx, int on) {
+    if (!ctx) return fail(ENGRAM_EINVAL, "null context");
+    ctx->starve_b = on ? 1 : 0;
     return ok();
 }
 

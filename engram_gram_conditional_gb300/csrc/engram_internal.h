@@ -58,6 +58,7 @@ struct MmaArgs {
     float eps;
     uint32_t* err;
     long long wait_limit_ns;
+    int starve_b;          // test hook: the TMA producer issues no wkv loads
     // fused operand A
     const uint4* windows;
     const uint8_t* table;

@@ -470,7 +470,7 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
                 int mb, nt;
                 tile_coords(a, tile, mb, nt);
                 const int n0 = (a.n_tile_begin + nt) * kBN;
-                for (int kb = 0; kb < KB; ++kb, ++it) {
+                for (int kb = 0; kb < KB && !a.starve_b; ++kb, ++it) {
                     const int sb = it % kB;
                     if (!mbar_wait(b_empty(sb), ((uint32_t)(it / kB) & 1u) ^ 1u, abort_flag, lim)) {
                         fail();

@@ -262,6 +262,16 @@ engram_status engram_project_windows(const engram_ctx* ctx, int layer, const uin
  * an asynchronous CUDA error. */
 engram_status engram_sync(const engram_ctx* ctx, void* stream);
 
+/* Upper bound, in nanoseconds, of every wait inside a kernel launched from
+ * this context (default 4 s).  A wait that runs out makes the kernel raise
+ * an abort flag, leave its loops, free its tensor memory and return; the next
+ * engram_sync reports ENGRAM_ETIMEOUT and the context stays usable. */
+engram_status engram_ctx_set_wait_limit(engram_ctx* ctx, int64_t ns);
+/* Test hook for the bounded waits: while on, the GEMM kernels issue no wkv
+ * loads, so the tensor-core issuer's wait for them runs out (after the wait
+ * limit) and the call ends with ENGRAM_ETIMEOUT.  Nothing faults or hangs. */
+engram_status engram_debug_starve_operand(engram_ctx* ctx, int on);
+
 /* Message of the calling thread's last error ("" if none). */
 const char* engram_last_error(void);
 

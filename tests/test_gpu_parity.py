@@ -280,3 +280,29 @@ def test_forward_full_geometry_bf16_operands_sampled():
         assert np.abs(gates[sample] - ref["gates"]).max() <= 1e-3
     finally:
         s.close()
+
+
+def test_bounded_wait_times_out_and_the_context_stays_usable(tiny):
+    # the GEMM's operand loads are withheld, so the tensor-core issuer's wait
+    # for them runs out after the wait limit; the call reports ETIMEOUT
+    ctx = tiny.model.ctx
+    win, _, _ = prefill_windows(tiny, 1, 64)
+    hidden = synth.hidden_bf16(tiny.w, 64)
+    eg.engram_ctx_set_wait_limit(ctx, 50_000_000)  # 50 ms
+    eg.engram_debug_starve_operand(ctx, True)
+    d_h = to_dev(hidden)
+    ws = torch.empty(max(16, eg.engram_workspace_bytes(ctx, 64)), dtype=torch.uint8, device="cuda")
+    import time
+
+    t0 = time.time()
+    eg.engram_forward(ctx, 0, to_dev(win), 64, d_h, ws)
+    with pytest.raises(eg.EngramError) as e:
+        eg.engram_sync(ctx)
+    assert e.value.status == eg.ETIMEOUT
+    assert time.time() - t0 < 5.0
+    eg.engram_debug_starve_operand(ctx, False)
+    eg.engram_ctx_set_wait_limit(ctx, 4_000_000_000)
+    h, gates = run_forward(tiny, win, hidden)
+    ref = O.forward(geom(tiny.w), tiny.w.table_seeds[0], tiny.oparams[0], tiny.W[0], tiny.wq[0],
+                    tiny.wk[0], win, hidden, np.arange(64))
+    check_hidden(h, ref["h_bf16"], "after a time-out")
