@@ -477,19 +477,23 @@ def extras(args, w, W, wq, wk, tmap, win0, d_win0, model, peaks, dev, sptr, stre
             for step in range(wd.steps)]
     d_wins = torch.from_numpy(np.stack(wins).view(np.int32)).to(dev)
     d_h = torch.from_numpy(synth.normal_bf16((S, wd.hc, wd.d), 1.0, 0, 77).view(np.int16)).to(dev)
-    d_ws = torch.empty(eg.engram_workspace_bytes(dm.ctx, S), dtype=torch.uint8, device=dev)
-    for i in range(5):
-        eg.engram_forward(dm.ctx, 0, d_wins[i], S, d_h, d_ws, None, sptr)
-    ms_d = timed(lambda i: eg.engram_forward(dm.ctx, 0, d_wins[i % wd.steps], S, d_h, d_ws, None,
-                                             sptr), wd.steps, stream)
-    eg.engram_sync(dm.ctx, sptr)
+    ws_bytes = max(eg.engram_workspace_bytes(dm.ctx, S),
+                   eg.engram_forward_staged_workspace_bytes(dm.ctx, S))
+    d_ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     bytes_step = w.N * w.K * 2 + S * (6336 + 81920 + 16)
-    gbs = bytes_step / ms_d / 1e6
-    out["decode"] = {"tokens_per_s": S / (ms_d / 1000.0), "ms_per_step": ms_d, "sessions": S,
-                     "steps": wd.steps, "table_rows": dm.rows(0),
-                     "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm"],
-                                  "unit": "GB/s", "frac": gbs / peaks["hbm"],
-                                  "bytes_per_step": bytes_step}}
+    entries = {"staged": eg.engram_forward_staged, "fused": eg.engram_forward}
+    for name, fwd in entries.items():
+        for i in range(5):
+            fwd(dm.ctx, 0, d_wins[i], S, d_h, d_ws, None, sptr)
+        ms_d = timed(lambda i: fwd(dm.ctx, 0, d_wins[i % wd.steps], S, d_h, d_ws, None, sptr),
+                     wd.steps, stream)
+        eg.engram_sync(dm.ctx, sptr)
+        gbs = bytes_step / ms_d / 1e6
+        out["decode" if name == "staged" else "decode_fused"] = {
+            "entry": fwd.__name__, "tokens_per_s": S / (ms_d / 1000.0), "ms_per_step": ms_d,
+            "sessions": S, "steps": wd.steps, "table_rows": dm.rows(0),
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm"], "unit": "GB/s",
+                         "frac": gbs / peaks["hbm"], "bytes_per_step": bytes_step}}
 
     # gather: unfused engram_gather_dequant over the 384M-row table, 50,032 tokens
     Tg = 50_032

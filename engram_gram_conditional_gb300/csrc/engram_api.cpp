@@ -207,6 +207,7 @@ MmaArgs mma_args(const engram_ctx* ctx, int layer, int64_t T) {
     a.K = ctx->K;
     a.m_blocks = (int)((T + kBM - 1) / kBM);
     a.group_m = 16;
+    a.k_splits = 1;
     a.hc = (int)ctx->desc.hc;
     a.d = (int)ctx->desc.d;
     a.eps = (float)ctx->desc.eps;
@@ -227,6 +228,112 @@ MmaArgs mma_args(const engram_ctx* ctx, int layer, int64_t T) {
 }
 
 }  // namespace
+
+namespace engram {
+
+// Split-K factor of the forward for T tokens on this device: 1 while the
+// output tiles fill the GPU twice over.  A smaller batch (decode) would leave
+// SMs idle while wkv streams, so K is split until there are about four waves
+// of (tile, split) work items: the largest s <= that (at most 8, at least 8
+// k-blocks per split) that divides the k-blocks - and, for 256-wide rows, the
+// buckets, since the fused gather splits on bucket boundaries.
+int forward_k_splits(const engram_ctx* ctx, int64_t T, int max_splits) {
+    const int64_t tiles = (T + kBM - 1) / kBM * (ctx->N / kBN);
+    const int sms = device_sm_count();
+    if (max_splits <= 1 || tiles >= 2 * (int64_t)sms) return 1;
+    int want = (int)((4 * (int64_t)sms + tiles / 2) / tiles);
+    want = std::max(2, std::min({want, 8, max_splits}));
+    const int KB = ctx->K / kBK;
+    const int nb = ctx->K / (int)ctx->desc.row_dim;
+    for (int s = want; s > 1; --s) {
+        if (KB % s != 0 || KB / s < 8) continue;
+        if (ctx->desc.row_dim == 256 && nb % s != 0) continue;
+        return s;
+    }
+    return 1;
+}
+
+// Workspace of the forward epilogue, in order: the gate sums [T][hc][d/kBN][3];
+// the counters (finished key-tile quadrants per M block, then with split K two
+// per (M block, N tile, quadrant)), zeroed by each call; with split K the
+// parked partial accumulators, one 128 x 256 fp32 slot per (M block, N tile,
+// split).  Each part starts on a 256-byte boundary.
+struct ForwardWs {
+    int splits;
+    size_t part, counters, counter_words, slots;
+    size_t total() const { return part + counters + slots; }
+};
+
+ForwardWs forward_ws(const engram_ctx* ctx, int64_t T, int max_splits) {
+    ForwardWs w{};
+    const size_t P = ctx->desc.d / kBN;
+    const size_t mb = ((size_t)T + kBM - 1) / kBM, nt = ctx->N / kBN;
+    w.splits = forward_k_splits(ctx, T, max_splits);
+    w.part = ((size_t)T * ctx->desc.hc * P * 3 * sizeof(float) + 255) & ~(size_t)255;
+    w.counter_words = mb + (w.splits > 1 ? mb * nt * 8 : 0);
+    w.counters = (w.counter_words * sizeof(uint32_t) + 255) & ~(size_t)255;
+    w.slots = w.splits > 1 ? mb * nt * w.splits * (size_t)(kBM * kBN) * sizeof(float) : 0;
+    return w;
+}
+
+size_t forward_workspace_bytes(const engram_ctx* ctx, int64_t T, int max_splits) {
+    if (!ctx || T <= 0) return 0;
+    return forward_ws(ctx, T, max_splits).total();
+}
+
+// Points the forward epilogue's fields of `a` into the workspace and zeroes
+// its counters on `s`.
+cudaError_t forward_bind_ws(const engram_ctx* ctx, int64_t T, int max_splits, void* ws,
+                            MmaArgs& a, cudaStream_t s) {
+    const ForwardWs w = forward_ws(ctx, T, max_splits);
+    char* base = static_cast<char*>(ws);
+    a.partials = reinterpret_cast<float*>(base);
+    a.counters = reinterpret_cast<uint32_t*>(base + w.part);
+    a.k_splits = w.splits;
+    if (w.splits > 1) {
+        a.split_counters = a.counters + a.m_blocks;
+        a.split_partials = reinterpret_cast<float*>(base + w.part + w.counters);
+    }
+    return cudaMemsetAsync(a.counters, 0, w.counter_words * sizeof(uint32_t), s);
+}
+
+}  // namespace engram
+
+namespace engram {
+
+// engram_forward with the split-K factor capped at max_splits; the workspace
+// is forward_workspace_bytes(ctx, T, max_splits) bytes.
+engram_status forward_fused(const engram_ctx* ctx, int layer, const uint32_t* d_windows,
+                            int64_t T, uint16_t* d_hidden, void* d_workspace, float* d_gates,
+                            void* stream, int max_splits) {
+    engram_status st = check_layer(ctx, layer, true);
+    if (st || (st = check_T(T))) return st;
+    if (T == 0) return ok();
+    if (!d_windows || !d_hidden || !d_workspace || !aligned16(d_windows) || !aligned16(d_hidden) ||
+        !aligned16(d_workspace))
+        return fail(ENGRAM_EINVAL, "windows / hidden / workspace (16-byte aligned)");
+    const LayerState& L = ctx->layers[layer];
+    MmaArgs a = mma_args(ctx, layer, T);
+    a.windows = reinterpret_cast<const uint4*>(d_windows);
+    a.hidden = d_hidden;
+    a.gates = d_gates;
+    if (L.f16) {
+        a.a_exp_shift = L.a_exp_shift;
+        a.out_scale = ldexpf(1.0f, -(L.a_exp_shift + L.wkv_exp));
+    }
+    const CUtensorMap& tmB = L.f16 ? L.tm_wkv_f16 : L.tm_wkv;
+    a.n_tile_begin = 0;
+    a.n_tiles = ctx->N / kBN;
+    // one launch: key tiles publish their sums and count in per M block; a
+    // value tile's epilogue waits for its block's count before gating
+    cudaError_t e = forward_bind_ws(ctx, T, max_splits, d_workspace, a, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "forward counters");
+    e = launch_forward_phase(a, kEpiForward, L.f16, L.bucket_gather, tmB, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "forward launch");
+    return ok();
+}
+
+}  // namespace engram
 
 extern "C" {
 
@@ -578,12 +685,9 @@ engram_status engram_batch_append(engram_session* const* sessions, const int32_t
 
 // ---- device steps ---------------------------------------------------------------------
 
+
 size_t engram_workspace_bytes(const engram_ctx* ctx, int64_t T) {
-    if (!ctx || T <= 0) return 0;
-    const size_t P = ctx->desc.d / kBN;
-    const size_t part = ((size_t)T * ctx->desc.hc * P * 3 * sizeof(float) + 255) & ~(size_t)255;
-    const size_t counters = (((size_t)T + kBM - 1) / kBM * sizeof(uint32_t) + 255) & ~(size_t)255;
-    return part + counters;
+    return forward_workspace_bytes(ctx, T, 8);
 }
 
 engram_status engram_hash(const engram_ctx* ctx, int layer, const uint32_t* d_windows, int64_t T,
@@ -645,44 +749,17 @@ engram_status engram_gate(const engram_ctx* ctx, int layer, const float* d_kv,
     return ok();
 }
 
+
 engram_status engram_forward(const engram_ctx* ctx, int layer, const uint32_t* d_windows,
                              int64_t T, uint16_t* d_hidden, void* d_workspace, float* d_gates,
                              void* stream) {
-    engram_status st = check_layer(ctx, layer, true);
-    if (st || (st = check_T(T))) return st;
-    if (T == 0) return ok();
-    if (!d_windows || !d_hidden || !d_workspace || !aligned16(d_windows) || !aligned16(d_hidden) ||
-        !aligned16(d_workspace))
-        return fail(ENGRAM_EINVAL, "windows / hidden / workspace (16-byte aligned)");
-    const LayerState& L = ctx->layers[layer];
-    MmaArgs a = mma_args(ctx, layer, T);
-    a.windows = reinterpret_cast<const uint4*>(d_windows);
-    a.hidden = d_hidden;
-    a.partials = static_cast<float*>(d_workspace);
-    a.gates = d_gates;
-    // one launch: key tiles publish their sums and count in per M block; a
-    // value tile's epilogue waits for its block's count before gating
-    const size_t part_bytes = (size_t)T * ctx->desc.hc * (ctx->desc.d / kBN) * 3 * sizeof(float);
-    a.counters = reinterpret_cast<uint32_t*>(static_cast<char*>(d_workspace) +
-                                             ((part_bytes + 255) & ~(size_t)255));
-    if (L.f16) {
-        a.a_exp_shift = L.a_exp_shift;
-        a.out_scale = ldexpf(1.0f, -(L.a_exp_shift + L.wkv_exp));
-    }
-    const CUtensorMap& tmB = L.f16 ? L.tm_wkv_f16 : L.tm_wkv;
-    a.n_tile_begin = 0;
-    a.n_tiles = ctx->N / kBN;
-    cudaError_t e = cudaMemsetAsync(a.counters, 0, sizeof(uint32_t) * a.m_blocks, (cudaStream_t)stream);
-    if (e != cudaSuccess) return cuda_fail(e, "forward counters");
-    e = launch_forward_phase(a, kEpiForward, L.f16, L.bucket_gather, tmB, (cudaStream_t)stream);
-    if (e != cudaSuccess) return cuda_fail(e, "forward launch");
-    return ok();
+    return forward_fused(ctx, layer, d_windows, T, d_hidden, d_workspace, d_gates, stream, 8);
 }
 
 size_t engram_forward_staged_workspace_bytes(const engram_ctx* ctx, int64_t T) {
     if (!ctx || T <= 0) return 0;
     const size_t e = ((size_t)T * ctx->K * sizeof(uint16_t) + 255) & ~(size_t)255;
-    return e + engram_workspace_bytes(ctx, T);
+    return e + forward_workspace_bytes(ctx, T, 8);
 }
 
 engram_status engram_forward_staged(const engram_ctx* ctx, int layer, const uint32_t* d_windows,
@@ -701,10 +778,7 @@ engram_status engram_forward_staged(const engram_ctx* ctx, int layer, const uint
     MmaArgs a = mma_args(ctx, layer, T);
     a.windows = reinterpret_cast<const uint4*>(d_windows);
     a.hidden = d_hidden;
-    a.partials = reinterpret_cast<float*>(rest);
     a.gates = d_gates;
-    const size_t part_bytes = (size_t)T * ctx->desc.hc * (ctx->desc.d / kBN) * 3 * sizeof(float);
-    a.counters = reinterpret_cast<uint32_t*>(rest + ((part_bytes + 255) & ~(size_t)255));
     if (L.f16) {
         a.a_exp_shift = L.a_exp_shift;
         a.out_scale = ldexpf(1.0f, -(L.a_exp_shift + L.wkv_exp));
@@ -721,7 +795,7 @@ engram_status engram_forward_staged(const engram_ctx* ctx, int layer, const uint
     CUtensorMap tmA;
     e = make_tma_16bit(&tmA, e_scratch, (uint64_t)T, (uint64_t)ctx->K, kBM, L.f16);
     if (e != cudaSuccess) return cuda_fail(e, "e tensor map");
-    e = cudaMemsetAsync(a.counters, 0, sizeof(uint32_t) * a.m_blocks, s);
+    e = forward_bind_ws(ctx, T, 8, rest, a, s);
     if (e != cudaSuccess) return cuda_fail(e, "forward counters");
     e = launch_forward_tma(a, L.f16, tmA, L.f16 ? L.tm_wkv_f16 : L.tm_wkv, s);
     if (e != cudaSuccess) return cuda_fail(e, "staged forward launch");

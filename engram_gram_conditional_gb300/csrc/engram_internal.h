@@ -54,6 +54,7 @@ struct MmaArgs {
     int n_tiles;       // N tiles of this launch
     int m_blocks;      // ceil(T / kBM)
     int group_m;       // tile rasterisation: M blocks per group
+    int k_splits;      // split-K factor (>= 1); the tile list holds every (tile, split)
     int hc, d;
     float eps;
     uint32_t* err;
@@ -75,7 +76,12 @@ struct MmaArgs {
     const float* wq;       // [hc][d]
     const float* wk;       // [hc][d]
     float* partials;       // [T][hc][d / kBN][3]
-    uint32_t* counters;    // kEpiForward: finished key tiles per M block (zeroed per call)
+    uint32_t* counters;    // kEpiForward: finished key tile quadrants per M block (zeroed per call)
+    // kEpiForward with k_splits > 1: one 128 x 256 fp32 slot per (M block, N tile,
+    // split), and per (M block, N tile, TMEM quadrant) two counters, arrivals and
+    // partials ready (zeroed per call)
+    float* split_partials;
+    uint32_t* split_counters;
     float* gates;          // [T][hc] or null
     HashParams hp;
 };

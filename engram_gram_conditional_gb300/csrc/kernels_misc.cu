@@ -13,6 +13,8 @@ namespace {
 
 int g_sm_count = 0;
 
+// SMs of the current device (of the first one asked about); 152, a GB300's
+// count, when no device answers.
 int sm_count() {
     if (g_sm_count == 0) {
         int dev = 0, n = 0;
@@ -20,7 +22,7 @@ int sm_count() {
             cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0)
             g_sm_count = n;
         else
-            g_sm_count = 148;
+            return 152;
     }
     return g_sm_count;
 }
@@ -198,8 +200,8 @@ constexpr int kGateThreads = 256;
 
 __global__ void __launch_bounds__(kGateThreads)
 k_gate(const float* __restrict__ kv, const uint4* __restrict__ windows, int64_t T, int hc, int d,
-       float eps, uint16_t* __restrict__ hidden, const float* __restrict__ wq,
-       const float* __restrict__ wk, float* __restrict__ gates) {
+       float eps, uint16_t* __restrict__ hidden, const float* __restrict__ wq, const float* __restrict__ wk,
+       float* __restrict__ gates) {
     __shared__ float red[kGateThreads / 32][8][3];
     __shared__ float gsh[8];
     const int N = (hc + 1) * d;
@@ -347,7 +349,8 @@ cudaError_t launch_gate(const Geometry& g, const float* kv, const uint4* windows
                         cudaStream_t s) {
     if (T == 0) return cudaSuccess;
     const int grid = (int)std::min<int64_t>(T, (int64_t)sm_count() * 8);
-    k_gate<<<grid, kGateThreads, 0, s>>>(kv, windows, T, g.hc, g.d, g.eps, hidden, wq, wk, gates);
+    k_gate<<<grid, kGateThreads, 0, s>>>(kv, windows, T, g.hc, g.d, g.eps,
+                                         hidden, wq, wk, gates);
     return cudaGetLastError();
 }
 

@@ -164,10 +164,6 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
 }
 
 // ---- tcgen05 -------------------------------------------------------------------
-// Named barrier of the four epilogue warps (id 1; id 0 is __syncthreads).
-__device__ __forceinline__ void epilogue_bar() {
-    asm volatile("bar.sync 1, 128;" ::: "memory");
-}
 __device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
     uint32_t v;
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -233,11 +229,140 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
 __device__ __forceinline__ void tmem_wait_ld() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
+// The inverse of tmem_ld32: thread i writes row (lane base + i).
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+        "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
+        "%28, %29, %30, %31, %32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+        "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+        "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+        "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+// Starts loading `bytes` (a multiple of 16, 16-byte aligned) into L2.
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+// Drops a 128-byte line from L2 without writing it back (its contents become
+// undefined): for scratch that nobody reads again.
+__device__ __forceinline__ void discard_l2_line(const void* p) {
+    asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
+}
+
+// Split-K reduction of one TMEM quadrant (32 rows) of an output tile in the
+// forward epilogue.  The splits of a tile count their arrivals per quadrant:
+// every split but the last parks its accumulator in its fp32 slot; the last
+// waits (bounded) until those are written, sums the S partials in split order
+// - its own from TMEM - and writes the sum back into TMEM, so the gate
+// epilogue that follows sees the full K reduction.  The sum does not depend
+// on which split arrives last.  Returns 1 for the warp that holds the sum,
+// 0 for a warp that parked its partial, -1 on a time-out.
+// Slot layout: [32-column chunk c][float4 i][row]: the 32 rows of a warp for
+// one (c, i) are 512 contiguous bytes.
+__device__ __forceinline__ int split_k_quadrant(const MmaArgs& a, int mb, int nt, int ks, int q,
+                                                int lane, uint32_t taddr,
+                                                volatile int* abort_flag, long long lim) {
+    const int S = a.k_splits;
+    const int64_t tile = (int64_t)mb * a.n_tiles + nt;
+    uint32_t* cnt = a.split_counters + (tile * 4 + q) * 2;
+    uint32_t order = 0;
+    if (lane == 0) order = atomicAdd(cnt, 1u);
+    order = __shfl_sync(0xFFFFFFFFu, order, 0);
+    float4* const slots = reinterpret_cast<float4*>(a.split_partials) + tile * S * (kBM * kBN / 4);
+    const int m = q * 32 + lane;
+    if ((int)order < S - 1) {
+        float4* dst = slots + (int64_t)ks * (kBM * kBN / 4);
+#pragma unroll 1
+        for (int c = 0; c < kBN / 32; ++c) {
+            uint32_t r[32];
+            tmem_ld32(taddr + (uint32_t)(c * 32), r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                __stcg(dst + (c * 8 + i) * kBM + m,
+                       make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
+                                   __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3])));
+        }
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) atomicAdd(cnt + 1, 1u);
+        return 0;
+    }
+    int ready = 1;
+    if (lane == 0) {
+        const uint64_t t0 = globaltimer();
+        uint32_t n = 0;
+        while (ld_acquire_u32(cnt + 1) < (uint32_t)(S - 1)) {
+            if ((++n & 63u) == 0u && ((long long)(globaltimer() - t0) > lim || *abort_flag)) {
+                ready = 0;
+                break;
+            }
+        }
+    }
+    ready = __shfl_sync(0xFFFFFFFFu, ready, 0);
+    if (!ready) return -1;
+    __threadfence();
+#pragma unroll 1
+    for (int c = 0; c < kBN / 32; ++c) {
+        uint32_t own[32];
+        tmem_ld32(taddr + (uint32_t)(c * 32), own);
+        tmem_wait_ld();
+        float acc[32];
+#pragma unroll 1
+        for (int k = 0; k < S; ++k) {
+            float v[32];
+            if (k == ks) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(own[j]);
+            } else {
+                const float4* src = slots + (int64_t)k * (kBM * kBN / 4) + c * 8 * kBM + m;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float4 x = __ldcg(src + i * kBM);
+                    v[4 * i] = x.x;
+                    v[4 * i + 1] = x.y;
+                    v[4 * i + 2] = x.z;
+                    v[4 * i + 3] = x.w;
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 32; ++j) acc[j] = k == 0 ? v[j] : acc[j] + v[j];
+        }
+        uint32_t out[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) out[j] = __float_as_uint(acc[j]);
+        tmem_st32(taddr + (uint32_t)(c * 32), out);
+        // the parked lines of this chunk are read: drop them from L2 unwritten
+        __syncwarp();
+        for (int k = 0; k < S; ++k)
+            if (k != ks)
+                discard_l2_line(slots + (int64_t)k * (kBM * kBN / 4) + (c * 8 + (lane >> 2)) * kBM +
+                                q * 32 + (lane & 3) * 8);
+    }
+    tmem_wait_st();
+    return 1;
+}
 
 // Tile order: groups of `group_m` M blocks; inside a group, N-major so the
 // CTAs in flight share wkv tiles in L2 while the group's gathered rows stay
 // L2-resident.
-__device__ __forceinline__ void tile_coords(const MmaArgs& a, int tile, int& mb, int& nt) {
+// With split-K (small M) the order is (N tile, split) outer, M block inner.
+__device__ __forceinline__ void tile_coords(const MmaArgs& a, int tile, int& mb, int& nt,
+                                            int& ks) {
+    if (a.k_splits > 1) {
+        mb = tile % a.m_blocks;
+        const int r = tile / a.m_blocks;
+        ks = r % a.k_splits;
+        nt = r / a.k_splits;
+        return;
+    }
+    ks = 0;
     const int per_group = a.group_m * a.n_tiles;
     const int g = tile / per_group;
     const int first_m = g * a.group_m;
@@ -245,6 +370,26 @@ __device__ __forceinline__ void tile_coords(const MmaArgs& a, int tile, int& mb,
     const int r = tile - g * per_group;
     nt = r / gm;
     mb = first_m + (r - nt * gm);
+}
+
+// Forward epilogue: starts the L2 loads of the hidden slices that row m of
+// `tile` will read (key tile: its branch's 256 columns; value tile: those
+// columns of every branch), so that the epilogue's own loads hit L2.
+__device__ __forceinline__ void prefetch_hidden(const MmaArgs& a, int tile, int m) {
+    int mb, nt, ks;
+    tile_coords(a, tile, mb, nt, ks);
+    const int64_t t = (int64_t)mb * kBM + m;
+    if (t >= a.T) return;
+    const int n0 = (a.n_tile_begin + nt) * kBN;
+    const int key_cols = a.hc * a.d;
+    if (n0 < key_cols) {
+        const int branch = n0 / a.d;
+        prefetch_l2(a.hidden + (t * a.hc + branch) * (int64_t)a.d + (n0 - branch * a.d),
+                    kBN * 2);
+    } else {
+        for (int b = 0; b < a.hc; ++b)
+            prefetch_l2(a.hidden + (t * a.hc + b) * (int64_t)a.d + (n0 - key_cols), kBN * 2);
+    }
 }
 
 // ---- fused A producer ------------------------------------------------------------
@@ -450,7 +595,7 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    const int total = a.m_blocks * a.n_tiles;
+    const int total = a.m_blocks * a.n_tiles * a.k_splits;
     const int KB = a.K / kBK;
     const long long lim = a.wait_limit_ns;
 
@@ -467,10 +612,11 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
             int it = 0;
             bool ok = true;
             for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-                int mb, nt;
-                tile_coords(a, tile, mb, nt);
+                int mb, nt, ks;
+                tile_coords(a, tile, mb, nt, ks);
                 const int n0 = (a.n_tile_begin + nt) * kBN;
-                for (int kb = 0; kb < KB && !a.starve_b; ++kb, ++it) {
+                const int kb_hi = (ks + 1) * KB / a.k_splits;
+                for (int kb = ks * KB / a.k_splits; kb < kb_hi && !a.starve_b; ++kb, ++it) {
                     const int sb = it % kB;
                     if (!mbar_wait(b_empty(sb), ((uint32_t)(it / kB) & 1u) ^ 1u, abort_flag, lim)) {
                         fail();
@@ -505,7 +651,10 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * kBN);
-                for (int kb = 0; kb < KB; ++kb, ++it) {
+                int mb_, nt_, ks;
+                tile_coords(a, tile, mb_, nt_, ks);
+                const int kb_lo = ks * KB / a.k_splits, kb_hi = (ks + 1) * KB / a.k_splits;
+                for (int kb = kb_lo; kb < kb_hi; ++kb, ++it) {
                     const int sa = it % kA, sb = it % kB;
                     if (!mbar_wait(a_full(sa), (uint32_t)(it / kA) & 1u, abort_flag, lim) ||
                         !mbar_wait(b_full(sb), (uint32_t)(it / kB) & 1u, abort_flag, lim)) {
@@ -519,7 +668,7 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
 #pragma unroll
                     for (int k = 0; k < kBK / 16; ++k)  // 16 elements = 32 bytes per MMA
                         umma_f16kind(d_tmem, ad + 2ull * k, bd + 2ull * k, idesc<kF16>(),
-                                     (kb | k) != 0);
+                                     (kb != kb_lo) || (k != 0));
                     umma_commit(a_empty(sa));
                     umma_commit(b_empty(sb));
                 }
@@ -539,18 +688,20 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
             bool ok = true;
             BucketRows R0, R1;
             for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-                int mb, nt;
-                tile_coords(a, tile, mb, nt);
+                int mb, nt, ks;
+                tile_coords(a, tile, mb, nt, ks);
+                // this split's buckets (the host splits K on bucket boundaries)
+                const int b_lo = ks * nbk / a.k_splits, b_hi = (ks + 1) * nbk / a.k_splits;
                 const int64_t t = (int64_t)mb * kBM + pw * kRowsPerProd + (lane & (kRowsPerProd - 1));
                 const uint4 w = t < a.T ? a.windows[t] : make_uint4(kDead, kDead, kDead, kDead);
-                uint32_t row0 = own_bucket_row(a, w, 0);
+                uint32_t row0 = own_bucket_row(a, w, b_lo);
                 uint2 sw0 = own_scale_word(a, row0);
                 load_bucket(a, row0, lane, R0);
                 uint2 sw1 = make_uint2(0x7F7F7F7Fu, 0x7F7F7F7Fu);
                 // buckets in pairs so the two register sets keep static names
                 auto run = [&](int b, const BucketRows& cur, uint2 cur_sw, BucketRows& nxt,
                                uint2& nxt_sw) -> bool {
-                    if (b + 1 < nbk) {  // the next bucket's loads go out first
+                    if (b + 1 < b_hi) {  // the next bucket's loads go out first
                         const uint32_t r = own_bucket_row(a, w, b + 1);
                         nxt_sw = own_scale_word(a, r);
                         load_bucket(a, r, lane, nxt);
@@ -579,9 +730,9 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
                     it += 4;
                     return true;
                 };
-                for (int b = 0; b < nbk && ok; b += 2) {
+                for (int b = b_lo; b < b_hi && ok; b += 2) {
                     ok = run(b, R0, sw0, R1, sw1);
-                    if (ok && b + 1 < nbk) ok = run(b + 1, R1, sw1, R0, sw0);
+                    if (ok && b + 1 < b_hi) ok = run(b + 1, R1, sw1, R0, sw0);
                 }
             }
         } else if (kASrc == kASrcGatherKb) {
@@ -592,8 +743,9 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
             int it = 0;
             bool ok = true;
             for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-                int mb, nt;
-                tile_coords(a, tile, mb, nt);
+                int mb, nt, ks;
+                tile_coords(a, tile, mb, nt, ks);
+                const int kb_lo = ks * KB / a.k_splits, kb_hi = (ks + 1) * KB / a.k_splits;
                 {   // hash: lanes l, l + 16 <-> token, every bucket, into the row-index table
                     const int m = pw * kRowsPerProd + (lane & (kRowsPerProd - 1));
                     const int64_t t = (int64_t)mb * kBM + m;
@@ -615,12 +767,12 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
                 RawKb q[kPrefetch];
 #pragma unroll
                 for (int i = 0; i < kPrefetch; ++i)
-                    if (i < KB) load_kb(a, rows_s, m0, c, i, q[i]);
-                for (int kb0 = 0; kb0 < KB && ok; kb0 += kPrefetch) {
+                    if (kb_lo + i < kb_hi) load_kb(a, rows_s, m0, c, kb_lo + i, q[i]);
+                for (int kb0 = kb_lo; kb0 < kb_hi && ok; kb0 += kPrefetch) {
 #pragma unroll
                     for (int u = 0; u < kPrefetch; ++u) {
                         const int kb = kb0 + u;
-                        if (kb < KB && ok) {
+                        if (kb < kb_hi && ok) {
                             const int s = it % kA;
                             const uint32_t ph = (uint32_t)(it / kA) & 1u;
                             ++it;
@@ -638,7 +790,7 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
                                 fence_proxy_async();
                                 __syncwarp();
                                 if (lane == 0) mbar_arrive(a_full(s));
-                                if (kb + kPrefetch < KB) load_kb(a, rows_s, m0, c, kb + kPrefetch, q[u]);
+                                if (kb + kPrefetch < kb_hi) load_kb(a, rows_s, m0, c, kb + kPrefetch, q[u]);
                             }
                         }
                     }
@@ -652,9 +804,13 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
         const int q = warp & 3;  // TMEM lane quadrant this warp may read
         const int m = q * 32 + lane;
         int tc = 0;
+        if (kMode == kEpiForward && blockIdx.x < total) prefetch_hidden(a, blockIdx.x, m);
         for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++tc) {
-            int mb, nt;
-            tile_coords(a, tile, mb, nt);
+            int mb, nt, ks;
+            tile_coords(a, tile, mb, nt, ks);
+            // the next tile's hidden slices travel to L2 while this one is finished
+            if (kMode == kEpiForward && tile + (int)gridDim.x < total)
+                prefetch_hidden(a, tile + gridDim.x, m);
             const int acc = tc & 1;
             const uint32_t aph = (uint32_t)(tc >> 1) & 1u;
             int full_ok = 1;
@@ -668,14 +824,25 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
             const uint32_t taddr = tmem_base + (uint32_t)(acc * kBN) + ((uint32_t)(q * 32) << 16);
             const int64_t t = (int64_t)mb * kBM + m;
             const int n0 = (a.n_tile_begin + nt) * kBN;
-            if (kMode == kEpiStoreKv) {
+            int holds_sum = 1;
+            if (kMode == kEpiForward && a.k_splits > 1) {
+                holds_sum = split_k_quadrant(a, mb, nt, ks, q, lane, taddr, abort_flag, lim);
+                if (holds_sum < 0) {
+                    if (lane == 0) fail();
+                    break;
+                }
+            }
+            if (!holds_sum) {
+                // partial parked for the split that arrives last
+            } else if (kMode == kEpiStoreKv) {
 #pragma unroll 1
                 for (int c = 0; c < kBN / 32; ++c) {
                     uint32_t r[32];
                     tmem_ld32(taddr + (uint32_t)(c * 32), r);
                     tmem_wait_ld();
                     if (t < a.T) {
-                        float4* dst = reinterpret_cast<float4*>(a.kv + t * a.ldkv + n0 + c * 32);
+                        float4* dst = reinterpret_cast<float4*>(a.kv +
+                                                                t * a.ldkv + n0 + c * 32);
 #pragma unroll
                         for (int i = 0; i < 8; ++i)
                             dst[i] = make_float4(__uint_as_float(r[4 * i]) * a.out_scale,
@@ -732,16 +899,17 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
                     pp[2] = shk;
                 }
                 if (kMode == kEpiForward) {
-                    // publish: every thread's sums, then one count for the M block
+                    // publish: the warp's sums, then one count for its quadrant
                     __threadfence();
-                    epilogue_bar();
-                    if (warp == kWarpEpi && lane == 0) atomicAdd(a.counters + mb, 1u);
+                    __syncwarp();
+                    if (lane == 0) atomicAdd(a.counters + mb, 1u);
                 }
             } else {  // value tile
                 if (kMode == kEpiForward) {
-                    // wait (bounded) until every key tile of this M block has counted in
-                    if (warp == kWarpEpi && lane == 0) {
-                        const uint32_t target = (uint32_t)(a.hc * a.d / kBN);
+                    // wait (bounded) until every quadrant of every key tile of this
+                    // M block has counted in
+                    if (lane == 0) {
+                        const uint32_t target = (uint32_t)(4 * (a.hc * a.d / kBN));
                         const uint64_t t0 = globaltimer();
                         uint32_t n = 0;
                         while (ld_acquire_u32(a.counters + mb) < target) {
@@ -752,7 +920,7 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
                             }
                         }
                     }
-                    epilogue_bar();
+                    __syncwarp();
                     __threadfence();
                 }
                 const int cv = n0 - a.hc * a.d;
@@ -760,17 +928,45 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
                 const int P = a.d / kBN;
                 float g[8];
 #pragma unroll
-                for (int b = 0; b < 8; ++b) {
-                    g[b] = 0.f;
-                    if (b < a.hc && text) {
+                for (int b = 0; b < 8; ++b) g[b] = 0.f;
+                // one branch at a time (its loads all in flight), then the gate
+                // into its static register slot
+#pragma unroll 1
+                for (int b = 0; b < a.hc; ++b) {
+                    if (text) {
+                        // L2 reads (written by other CTAs), summed in tile order
                         const float* pp = a.partials + (t * a.hc + b) * (int64_t)P * 3;
-                        float skk = 0.f, shh = 0.f, shk = 0.f;
-                        for (int p = 0; p < P; ++p) {  // L2 reads: written by other CTAs
-                            skk += __ldcg(pp + 3 * p);
-                            shh += __ldcg(pp + 3 * p + 1);
-                            shk += __ldcg(pp + 3 * p + 2);
+                        float sum[3] = {0.f, 0.f, 0.f};
+                        const int n4 = 3 * P / 4;
+                        // rounds of 9 float4 = 12 (k^2, h^2, h w k) triples; 4 x 9 is a
+                        // multiple of 3, so element 4 j + k of a round is sum (4 j + k) % 3
+                        if (3 * P % 4 == 0) {
+#pragma unroll 1
+                            for (int j0 = 0; j0 < n4; j0 += 9) {
+                                float4 v[9];
+#pragma unroll
+                                for (int j = 0; j < 9; ++j)
+                                    if (j0 + j < n4)
+                                        v[j] = __ldcg(reinterpret_cast<const float4*>(pp) + j0 + j);
+#pragma unroll
+                                for (int j = 0; j < 9; ++j)
+                                    if (j0 + j < n4) {
+                                        const float e[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+                                        for (int k = 0; k < 4; ++k) sum[(4 * j + k) % 3] += e[k];
+                                    }
+                            }
+                        } else {
+                            for (int p = 0; p < P; ++p) {
+                                sum[0] += __ldcg(pp + 3 * p);
+                                sum[1] += __ldcg(pp + 3 * p + 1);
+                                sum[2] += __ldcg(pp + 3 * p + 2);
+                            }
                         }
-                        g[b] = gate_from_sums(skk, shh, shk, a.d, a.eps);
+                        const float gb = gate_from_sums(sum[0], sum[1], sum[2], a.d, a.eps);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            if (j == b) g[j] = gb;
                     }
                 }
                 if (a.gates && n0 == a.hc * a.d && t < a.T) {
@@ -841,7 +1037,7 @@ cudaError_t launch(const MmaArgs& a, const CUtensorMap& tmA, const CUtensorMap& 
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    const int total = a.m_blocks * a.n_tiles;
+    const int total = a.m_blocks * a.n_tiles * a.k_splits;
     if (total == 0) return cudaSuccess;
     const int grid = std::min(total, device_sm_count());
     kern<<<grid, kThreads, kSmem, s>>>(tmA, tmB, a);
@@ -881,6 +1077,7 @@ cudaError_t launch_project(const MmaArgs& a, const CUtensorMap& tmA, const CUten
                            cudaStream_t s) {
     return launch<kASrcTma, false, kEpiStoreKv>(a, tmA, tmB, s);
 }
+
 
 cudaError_t launch_forward_tma(const MmaArgs& a, bool f16, const CUtensorMap& tmA,
                                const CUtensorMap& tmB, cudaStream_t s) {

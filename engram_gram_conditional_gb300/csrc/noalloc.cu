@@ -26,6 +26,12 @@
 
 namespace engram {
 void set_last_error(const std::string& msg);
+// The fused forward with its split-K factor capped at max_splits, and its
+// workspace size (engram_api.cpp).
+engram_status forward_fused(const engram_ctx* ctx, int layer, const uint32_t* d_windows,
+                            int64_t T, uint16_t* d_hidden, void* d_workspace, float* d_gates,
+                            void* stream, int max_splits);
+size_t forward_workspace_bytes(const engram_ctx* ctx, int64_t T, int max_splits);
 }
 
 namespace {
@@ -78,9 +84,11 @@ extern "C" engram_status engram_forward_noalloc(const engram_ctx* ctx, int layer
         return ENGRAM_EINVAL;
     }
     if (T == 0) return engram_forward(ctx, layer, d_windows, 0, d_hidden, nullptr, d_gates, stream);
-    const size_t need = engram_workspace_bytes(ctx, T);
+    // K is never split here: split-K partials of a small batch would need far
+    // more scratch than the gate sums, so such a batch runs on fewer SMs
+    const size_t need = engram::forward_workspace_bytes(ctx, T, 1);
     if (need > kScratchBytes) {
-        const size_t per_token = engram_workspace_bytes(ctx, 1 << 16) >> 16;
+        const size_t per_token = engram::forward_workspace_bytes(ctx, 1 << 16, 1) >> 16;
         engram::set_last_error(
             "engram_forward_noalloc: " + std::to_string(T) + " tokens need " + std::to_string(need) +
             " bytes of scratch, above the built-in 8 MiB (at most " +
@@ -91,5 +99,5 @@ extern "C" engram_status engram_forward_noalloc(const engram_ctx* ctx, int layer
     void* scratch = nullptr;
     engram_status st = scratch_address(&scratch);
     if (st != ENGRAM_OK) return st;
-    return engram_forward(ctx, layer, d_windows, T, d_hidden, scratch, d_gates, stream);
+    return engram::forward_fused(ctx, layer, d_windows, T, d_hidden, scratch, d_gates, stream, 1);
 }

@@ -194,7 +194,13 @@ engram_status engram_session_append(engram_session* s, const int32_t* tokens,
 engram_status engram_batch_append(engram_session* const* sessions, const int32_t* tokens,
                                   const uint8_t* is_image, int64_t n, uint32_t* windows_out);
 
-/* Bytes of device workspace engram_forward needs for T tokens. */
+/* Bytes of device workspace engram_forward needs for T tokens on the current
+ * device.  A batch too small to fill the GPU (fewer than two output tiles of
+ * 128 tokens x 256 outputs per SM) is run with K split over up to 8 CTAs per
+ * tile, and the workspace then also holds the parked fp32 partial tiles:
+ * 128 KB per (128-token block, 256-output tile, split), e.g. 79 MB for 256
+ * tokens at N = 25,600.  Ask again after switching to a device with another
+ * SM count. */
 size_t engram_workspace_bytes(const engram_ctx* ctx, int64_t T);
 
 /* a2: windows (device [T][4]) -> row indices (device [T][nb]). */
@@ -214,7 +220,10 @@ engram_status engram_gate(const engram_ctx* ctx, int layer, const float* d_kv,
                           float* d_gates, void* stream);
 /* a7: the whole step fused: hash, gather and dequantise into the GEMM's
  * shared-memory operand tiles, the tcgen05 projection and the gate as the
- * GEMM epilogue.  Neither the 6,144-vector nor the kv reaches HBM.
+ * GEMM epilogue.  Neither the 6,144-vector nor the kv reaches HBM (except,
+ * for a small batch run with split K, the partial kv tiles that the splits of
+ * a tile hand to the last of them, through L2).  The result does not depend
+ * on the order in which the splits finish.
  * d_workspace: engram_workspace_bytes(ctx, T) bytes of device memory. */
 engram_status engram_forward(const engram_ctx* ctx, int layer, const uint32_t* d_windows,
                              int64_t T, uint16_t* d_hidden, void* d_workspace,
@@ -226,7 +235,8 @@ engram_status engram_forward(const engram_ctx* ctx, int layer, const uint32_t* d
  * operand read from e by TMA and the same gate epilogue (kv stays on chip).
  * Unlike engram_forward, the 6,144-vectors pass through device memory (an
  * L2-resident scratch of 12 KB per token for moderate T); in exchange each
- * table row is read once per call instead of once per output tile.
+ * table row is read once per call instead of once per output tile.  Small
+ * batches split K as engram_forward does.
  * d_workspace: engram_forward_staged_workspace_bytes(ctx, T) bytes. */
 size_t engram_forward_staged_workspace_bytes(const engram_ctx* ctx, int64_t T);
 engram_status engram_forward_staged(const engram_ctx* ctx, int layer, const uint32_t* d_windows,
@@ -242,6 +252,8 @@ engram_status engram_forward_staged(const engram_ctx* ctx, int layer, const uint
  * that loads the library until the process exits.  It makes no cudaMalloc or
  * cudaFree call.  T is limited to what 8 MiB holds (8,737 tokens at hc 4,
  * d 5,120); a larger T returns ENGRAM_EINVAL with the limit in the message.
+ * K is never split here (the partial tiles would not fit), so a small batch
+ * runs on fewer SMs than engram_forward would give it.
  * The first call on a device looks up the buffer's device address (once per
  * device, with that device current); make that first call before any stream
  * capture.  All calls share the buffer: calls whose kernels may overlap on the

@@ -257,6 +257,38 @@ def test_forward_full_geometry_sampled(prefill, entry):
     check_hidden(h, from_dev(d_h, np.uint16), "fused vs chain")
 
 
+@pytest.mark.parametrize("entry", ["fused", "staged"])
+@pytest.mark.parametrize("T", [1, 77, 256, 300, 600])
+def test_small_batches_split_k(prefill, entry, T):
+    # batches whose output tiles do not fill the GPU twice split K over
+    # several CTAs; the last split of each tile quadrant sums the parked
+    # partials and runs the gate epilogue
+    win, _, _ = prefill_windows(prefill, 1, T, spans=[(T // 2, 3)] if T > 8 else [])
+    hidden = synth.hidden_bf16(prefill.w, T)
+    h, gates = run_forward(prefill, win, hidden, staged=entry == "staged")
+    sample = np.unique(np.array([0, T // 2 - 1, T // 2, T // 2 + 3, 127, 128, T - 2, T - 1])
+                       .clip(0, T - 1))
+    ref = O.forward(geom(prefill.w), prefill.w.table_seeds[0], prefill.oparams[0], prefill.W[0],
+                    prefill.wq[0], prefill.wk[0], win, hidden, sample, nthreads=8)
+    check_hidden(h[sample], ref["h_bf16"], f"{entry} split-K T={T}")
+    assert np.abs(gates[sample] - ref["gates"]).max() <= 1e-3
+    image = win[:, 0] == eg.DEAD
+    assert np.array_equal(h[image], hidden[image]) and (gates[image] == 0).all()
+    # every token against the unsplit projection and the gate kernel
+    d_kv = torch.empty((T, prefill.w.N), dtype=torch.float32, device="cuda")
+    eg.engram_project_windows(prefill.model.ctx, 0, to_dev(win), T, d_kv)
+    d_h = to_dev(hidden)
+    d_g = torch.empty((T, prefill.w.hc), dtype=torch.float32, device="cuda")
+    eg.engram_gate(prefill.model.ctx, 0, d_kv, to_dev(win), T, d_h, d_g)
+    eg.engram_sync(prefill.model.ctx)
+    check_hidden(h, from_dev(d_h, np.uint16), f"{entry} split-K vs unsplit chain")
+    assert np.abs(gates - d_g.cpu().numpy()).max() <= 1e-3
+    # the same inputs give the same bits on a second call (the reduction order
+    # does not depend on which split arrives last)
+    h2, g2 = run_forward(prefill, win, hidden, staged=entry == "staged")
+    assert np.array_equal(h, h2) and np.array_equal(gates, g2)
+
+
 def test_forward_edge_cases(tiny):
     ctx = tiny.model.ctx
     eg.engram_forward(ctx, 0, None, 0, None, None)  # T = 0
