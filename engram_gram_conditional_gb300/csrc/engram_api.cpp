@@ -208,6 +208,7 @@ MmaArgs mma_args(const engram_ctx* ctx, int layer, int64_t T) {
     a.m_blocks = (int)((T + kBM - 1) / kBM);
     a.group_m = 16;
     a.k_splits = 1;
+    a.kv_split_stride = 0;
     a.hc = (int)ctx->desc.hc;
     a.d = (int)ctx->desc.d;
     a.eps = (float)ctx->desc.eps;
@@ -254,14 +255,15 @@ int forward_k_splits(const engram_ctx* ctx, int64_t T, int max_splits) {
 }
 
 // Workspace of the forward epilogue, in order: the gate sums [T][hc][d/kBN][3];
-// the counters (finished key-tile quadrants per M block, then with split K two
-// per (M block, N tile, quadrant)), zeroed by each call; with split K the
+// the gates [T][hc]; the counters, zeroed by each call (per (M block, TMEM
+// quadrant) finished key tiles and a gates-ready flag, then with split K per
+// (M block, N tile, quadrant) arrivals and partials ready); with split K the
 // parked partial accumulators, one 128 x 256 fp32 slot per (M block, N tile,
 // split).  Each part starts on a 256-byte boundary.
 struct ForwardWs {
     int splits;
-    size_t part, counters, counter_words, slots;
-    size_t total() const { return part + counters + slots; }
+    size_t part, gbuf, counters, counter_words, slots;
+    size_t total() const { return part + gbuf + counters + slots; }
 };
 
 ForwardWs forward_ws(const engram_ctx* ctx, int64_t T, int max_splits) {
@@ -270,7 +272,8 @@ ForwardWs forward_ws(const engram_ctx* ctx, int64_t T, int max_splits) {
     const size_t mb = ((size_t)T + kBM - 1) / kBM, nt = ctx->N / kBN;
     w.splits = forward_k_splits(ctx, T, max_splits);
     w.part = ((size_t)T * ctx->desc.hc * P * 3 * sizeof(float) + 255) & ~(size_t)255;
-    w.counter_words = mb + (w.splits > 1 ? mb * nt * 8 : 0);
+    w.gbuf = ((size_t)T * ctx->desc.hc * sizeof(float) + 255) & ~(size_t)255;
+    w.counter_words = mb * 8 + (w.splits > 1 ? mb * nt * 8 : 0);
     w.counters = (w.counter_words * sizeof(uint32_t) + 255) & ~(size_t)255;
     w.slots = w.splits > 1 ? mb * nt * w.splits * (size_t)(kBM * kBN) * sizeof(float) : 0;
     return w;
@@ -288,11 +291,12 @@ cudaError_t forward_bind_ws(const engram_ctx* ctx, int64_t T, int max_splits, vo
     const ForwardWs w = forward_ws(ctx, T, max_splits);
     char* base = static_cast<char*>(ws);
     a.partials = reinterpret_cast<float*>(base);
-    a.counters = reinterpret_cast<uint32_t*>(base + w.part);
+    a.gbuf = reinterpret_cast<float*>(base + w.part);
+    a.counters = reinterpret_cast<uint32_t*>(base + w.part + w.gbuf);
     a.k_splits = w.splits;
     if (w.splits > 1) {
-        a.split_counters = a.counters + a.m_blocks;
-        a.split_partials = reinterpret_cast<float*>(base + w.part + w.counters);
+        a.split_counters = a.counters + 8 * (size_t)a.m_blocks;
+        a.split_partials = reinterpret_cast<float*>(base + w.part + w.gbuf + w.counters);
     }
     return cudaMemsetAsync(a.counters, 0, w.counter_words * sizeof(uint32_t), s);
 }
@@ -740,10 +744,11 @@ engram_status engram_gate(const engram_ctx* ctx, int layer, const float* d_kv,
     engram_status st = check_layer(ctx, layer, true);
     if (st || (st = check_T(T))) return st;
     if (T == 0) return ok();
-    if (!d_kv || !d_windows || !d_hidden || !aligned16(d_windows))
-        return fail(ENGRAM_EINVAL, "kv / windows / hidden");
+    if (!d_kv || !d_windows || !d_hidden || !aligned16(d_kv) || !aligned16(d_windows) ||
+        !aligned16(d_hidden))
+        return fail(ENGRAM_EINVAL, "kv / windows / hidden (16-byte aligned)");
     const LayerState& L = ctx->layers[layer];
-    cudaError_t e = launch_gate(geometry(ctx), d_kv, reinterpret_cast<const uint4*>(d_windows), T,
+    cudaError_t e = launch_gate(geometry(ctx), d_kv, 1, 0, reinterpret_cast<const uint4*>(d_windows), T,
                                 d_hidden, L.w.wq, L.w.wk, d_gates, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "gate launch");
     return ok();
@@ -756,9 +761,19 @@ engram_status engram_forward(const engram_ctx* ctx, int layer, const uint32_t* d
     return forward_fused(ctx, layer, d_windows, T, d_hidden, d_workspace, d_gates, stream, 8);
 }
 
+// The staged forward of a batch too small to fill the GPU (K split) runs the
+// projection with a plain kv-store epilogue into per-split fp32 buffers and
+// the gate as its own kernel: the fused gate epilogue's loads wait behind the
+// wkv stream in the SM's memory pipeline, which a single wave of tiles cannot
+// hide, while the separate gate kernel has the whole GPU to itself.
+static int staged_splits(const engram_ctx* ctx, int64_t T) { return forward_k_splits(ctx, T, 8); }
+
 size_t engram_forward_staged_workspace_bytes(const engram_ctx* ctx, int64_t T) {
     if (!ctx || T <= 0) return 0;
     const size_t e = ((size_t)T * ctx->K * sizeof(uint16_t) + 255) & ~(size_t)255;
+    const int splits = staged_splits(ctx, T);
+    if (splits > 1)
+        return e + (((size_t)splits * T * ctx->N * sizeof(float) + 255) & ~(size_t)255);
     return e + forward_workspace_bytes(ctx, T, 8);
 }
 
@@ -795,6 +810,20 @@ engram_status engram_forward_staged(const engram_ctx* ctx, int layer, const uint
     CUtensorMap tmA;
     e = make_tma_16bit(&tmA, e_scratch, (uint64_t)T, (uint64_t)ctx->K, kBM, L.f16);
     if (e != cudaSuccess) return cuda_fail(e, "e tensor map");
+    const int splits = staged_splits(ctx, T);
+    if (splits > 1) {
+        // small batch: split-K projection into per-split kv buffers, then the gate
+        a.k_splits = splits;
+        a.kv = reinterpret_cast<float*>(rest);
+        a.ldkv = ctx->N;
+        a.kv_split_stride = T * (int64_t)ctx->N;
+        e = launch_project_split(a, L.f16, tmA, L.f16 ? L.tm_wkv_f16 : L.tm_wkv, s);
+        if (e != cudaSuccess) return cuda_fail(e, "split projection launch");
+        e = launch_gate(geometry(ctx), a.kv, splits, a.kv_split_stride, a.windows, T, d_hidden,
+                        L.w.wq, L.w.wk, d_gates, s);
+        if (e != cudaSuccess) return cuda_fail(e, "gate launch");
+        return ok();
+    }
     e = forward_bind_ws(ctx, T, 8, rest, a, s);
     if (e != cudaSuccess) return cuda_fail(e, "forward counters");
     e = launch_forward_tma(a, L.f16, tmA, L.f16 ? L.tm_wkv_f16 : L.tm_wkv, s);

@@ -41,10 +41,9 @@ constexpr int kBK = 64;   // reduction slice per pipeline stage (128-byte rows)
 
 enum EpilogueMode : int {
     kEpiStoreKv = 0,   // write kv fp32
-    kEpiKeyPartial = 1,  // key tiles: per-(token, branch, tile) sums
-    kEpiValueUpdate = 2, // value tiles: gates from the sums, hidden += g v
-    kEpiForward = 3      // both in one launch: a value tile's epilogue first waits
-                         // until every key tile of its M block has counted in
+    kEpiForward = 3    // the gate: key tiles publish per-(token, branch, tile) sums
+                       // and the last key tile of each M block quadrant turns them
+                       // into gates; value tiles wait for those, then hidden += g v
 };
 
 struct MmaArgs {
@@ -55,6 +54,7 @@ struct MmaArgs {
     int m_blocks;      // ceil(T / kBM)
     int group_m;       // tile rasterisation: M blocks per group
     int k_splits;      // split-K factor (>= 1); the tile list holds every (tile, split)
+    int64_t kv_split_stride;  // kEpiStoreKv: floats between the kv buffers of two splits
     int hc, d;
     float eps;
     uint32_t* err;
@@ -76,7 +76,10 @@ struct MmaArgs {
     const float* wq;       // [hc][d]
     const float* wk;       // [hc][d]
     float* partials;       // [T][hc][d / kBN][3]
-    uint32_t* counters;    // kEpiForward: finished key tile quadrants per M block (zeroed per call)
+    float* gbuf;           // [T][hc] gates of the call
+    // kEpiForward, per (M block, TMEM quadrant): finished key tiles, then a
+    // gates-ready flag (zeroed per call)
+    uint32_t* counters;
     // kEpiForward with k_splits > 1: one 128 x 256 fp32 slot per (M block, N tile,
     // split), and per (M block, N tile, TMEM quadrant) two counters, arrivals and
     // partials ready (zeroed per call)
@@ -94,9 +97,11 @@ cudaError_t launch_hash(const HashParams& hp, const uint4* windows, int64_t T, u
 cudaError_t launch_gather(const Geometry& g, const uint32_t* rows, int64_t T,
                           const uint8_t* table, const uint8_t* scales, uint64_t nrows,
                           uint16_t* emb, uint32_t* err, cudaStream_t s);
-cudaError_t launch_gate(const Geometry& g, const float* kv, const uint4* windows, int64_t T,
-                        uint16_t* hidden, const float* wq, const float* wk, float* gates,
-                        cudaStream_t s);
+// kv may be the sum of nsplit (<= 8) partial buffers, split_stride floats
+// apart, added in split order.  kv, hidden, wq and wk 16-byte aligned.
+cudaError_t launch_gate(const Geometry& g, const float* kv, int nsplit, int64_t split_stride,
+                        const uint4* windows, int64_t T, uint16_t* hidden, const float* wq,
+                        const float* wk, float* gates, cudaStream_t s);
 // Bind-time scans: out[0] = min, out[1] = max of n E8M0 bytes (out preset by
 // the caller to 255 / 0); out[2] = largest |x| of n BF16 values as its bit
 // pattern without the sign (out[2] preset to 0).
@@ -119,6 +124,10 @@ cudaError_t make_tma_16bit(CUtensorMap* map, const void* base, uint64_t rows, ui
 cudaError_t launch_project(const MmaArgs& a, const CUtensorMap& tmA, const CUtensorMap& tmB,
                            cudaStream_t s);
 cudaError_t launch_forward_phase(const MmaArgs& a, int mode, bool f16, bool bucket,
+                                 const CUtensorMap& tmB, cudaStream_t s);
+// Staged forward for small batches: the projection with a TMA-fed A operand,
+// split over K into a.k_splits partial kv buffers (the gate runs after it).
+cudaError_t launch_project_split(const MmaArgs& a, bool f16, const CUtensorMap& tmA,
                                  const CUtensorMap& tmB, cudaStream_t s);
 // Staged forward, step 2: the whole forward GEMM with a TMA-fed A operand.
 cudaError_t launch_forward_tma(const MmaArgs& a, bool f16, const CUtensorMap& tmA,

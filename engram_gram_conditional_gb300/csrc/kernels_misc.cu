@@ -193,35 +193,71 @@ __global__ void k_gather_stage(const __grid_constant__ HashParams hp, const uint
     }
 }
 
-// a5 standalone: one CTA per token.  Pass 1 reduces, per branch, sum k^2,
-// sum h^2 and sum h w_q w_k k; pass 2 applies hidden += g v with one BF16
-// rounding.  Image rows (c_t == DEAD) are left untouched.
-constexpr int kGateThreads = 256;
+// a5 standalone: one CTA per token.  kv may be the sum of nsplit partial
+// buffers split_stride floats apart (a projection split over K), added in
+// split order.  Pass 1, one branch at a time, reduces sum k^2, sum h^2 and
+// sum h w_q w_k k over the branch's d columns (float4 loads, two per thread
+// in flight per split, then a fixed-order block reduction); pass 2 applies
+// hidden += g v with one BF16 rounding, all branches' loads of a column group
+// before its stores.  Image rows (c_t == DEAD) are left untouched.
+constexpr int kGateThreads = 512;
+constexpr int kGateMaxSplits = 8;
 
-__global__ void __launch_bounds__(kGateThreads)
-k_gate(const float* __restrict__ kv, const uint4* __restrict__ windows, int64_t T, int hc, int d,
-       float eps, uint16_t* __restrict__ hidden, const float* __restrict__ wq, const float* __restrict__ wk,
-       float* __restrict__ gates) {
-    __shared__ float red[kGateThreads / 32][8][3];
+__device__ __forceinline__ float4 kv_sum4(const float4* p, int nsplit, int64_t stride4) {
+    float4 x = __ldcg(p);
+#pragma unroll
+    for (int sp = 1; sp < kGateMaxSplits; ++sp)
+        if (sp < nsplit) {
+            const float4 y = __ldcg(p + sp * stride4);
+            x.x += y.x;
+            x.y += y.y;
+            x.z += y.z;
+            x.w += y.w;
+        }
+    return x;
+}
+
+__device__ __forceinline__ float bf16_bits_to_f32(uint32_t b) { return __uint_as_float(b << 16); }
+
+__global__ void __launch_bounds__(kGateThreads, 2)
+k_gate(const float* __restrict__ kv, int nsplit, int64_t split_stride,
+       const uint4* __restrict__ windows, int64_t T, int hc, int d, float eps,
+       uint16_t* __restrict__ hidden, const float* __restrict__ wq,
+       const float* __restrict__ wk, float* __restrict__ gates) {
+    __shared__ float red[kGateThreads / 32][3];
     __shared__ float gsh[8];
     const int N = (hc + 1) * d;
+    const int n4 = d / 4;
+    const int64_t stride4 = split_stride / 4;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     for (int64_t t = blockIdx.x; t < T; t += gridDim.x) {
-        const bool image = windows[t].x == kDead;
-        if (image) {
+        if (windows[t].x == kDead) {
             if (gates && threadIdx.x < hc) gates[t * hc + threadIdx.x] = 0.0f;
             continue;
         }
-        const float* kvt = kv + t * (int64_t)N;
+        const float4* kvt = reinterpret_cast<const float4*>(kv + t * (int64_t)N);
         uint16_t* ht = hidden + t * (int64_t)hc * d;
         for (int b = 0; b < hc; ++b) {
+            const float4* kb = kvt + (int64_t)b * n4;
+            const uint2* hb = reinterpret_cast<const uint2*>(ht + (int64_t)b * d);
+            const float4* qb = reinterpret_cast<const float4*>(wq + (int64_t)b * d);
+            const float4* wb = reinterpret_cast<const float4*>(wk + (int64_t)b * d);
             float skk = 0.f, shh = 0.f, shk = 0.f;
-            for (int i = threadIdx.x; i < d; i += kGateThreads) {
-                const float k = kvt[(int64_t)b * d + i];
-                const float h = __uint_as_float((uint32_t)ht[(int64_t)b * d + i] << 16);
-                skk += k * k;
-                shh += h * h;
-                shk += h * wq[b * d + i] * wk[b * d + i] * k;
+#pragma unroll 2
+            for (int i = threadIdx.x; i < n4; i += kGateThreads) {
+                const float4 k = kv_sum4(kb + i, nsplit, stride4);
+                const uint2 h2 = hb[i];
+                const float4 q = __ldg(qb + i), w = __ldg(wb + i);
+                const float h[4] = {bf16_bits_to_f32(h2.x & 0xFFFFu), bf16_bits_to_f32(h2.x >> 16),
+                                    bf16_bits_to_f32(h2.y & 0xFFFFu), bf16_bits_to_f32(h2.y >> 16)};
+                const float kk[4] = {k.x, k.y, k.z, k.w};
+                const float qw[4] = {q.x * w.x, q.y * w.y, q.z * w.z, q.w * w.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    skk += kk[e] * kk[e];
+                    shh += h[e] * h[e];
+                    shk += h[e] * qw[e] * kk[e];
+                }
             }
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) {
@@ -230,33 +266,42 @@ k_gate(const float* __restrict__ kv, const uint4* __restrict__ windows, int64_t 
                 shk += __shfl_xor_sync(0xFFFFFFFFu, shk, o);
             }
             if (lane == 0) {
-                red[warp][b][0] = skk;
-                red[warp][b][1] = shh;
-                red[warp][b][2] = shk;
+                red[warp][0] = skk;
+                red[warp][1] = shh;
+                red[warp][2] = shk;
             }
+            __syncthreads();
+            if (threadIdx.x == 0) {
+                float a0 = 0.f, a1 = 0.f, a2 = 0.f;
+                for (int w = 0; w < kGateThreads / 32; ++w) {
+                    a0 += red[w][0];
+                    a1 += red[w][1];
+                    a2 += red[w][2];
+                }
+                const float g = gate_from_sums(a0, a1, a2, d, eps);
+                gsh[b] = g;
+                if (gates) gates[t * hc + b] = g;
+            }
+            __syncthreads();
         }
-        __syncthreads();
-        if (threadIdx.x < hc) {
-            const int b = threadIdx.x;
-            float skk = 0.f, shh = 0.f, shk = 0.f;
-            for (int w = 0; w < kGateThreads / 32; ++w) {
-                skk += red[w][b][0];
-                shh += red[w][b][1];
-                shk += red[w][b][2];
-            }
-            const float g = gate_from_sums(skk, shh, shk, d, eps);
-            gsh[b] = g;
-            if (gates) gates[t * hc + b] = g;
-        }
-        __syncthreads();
-        const float* v = kvt + (int64_t)hc * d;
-        for (int i = threadIdx.x; i < d; i += kGateThreads) {
-            const float vi = v[i];
-            for (int b = 0; b < hc; ++b) {
-                const float h = __uint_as_float((uint32_t)ht[(int64_t)b * d + i] << 16);
-                const float o = h + gsh[b] * vi;
-                ht[(int64_t)b * d + i] = __bfloat16_as_ushort(__float2bfloat16_rn(o));
-            }
+        const float4* v = kvt + (int64_t)hc * n4;
+        for (int i = threadIdx.x; i < n4; i += kGateThreads) {
+            const float4 vi = kv_sum4(v + i, nsplit, stride4);
+            uint2 h2[8];
+#pragma unroll
+            for (int b = 0; b < 8; ++b)
+                if (b < hc) h2[b] = reinterpret_cast<const uint2*>(ht + (int64_t)b * d)[i];
+#pragma unroll
+            for (int b = 0; b < 8; ++b)
+                if (b < hc) {
+                    const float g = gsh[b];
+                    const float o0 = fmaf(g, vi.x, bf16_bits_to_f32(h2[b].x & 0xFFFFu));
+                    const float o1 = fmaf(g, vi.y, bf16_bits_to_f32(h2[b].x >> 16));
+                    const float o2 = fmaf(g, vi.z, bf16_bits_to_f32(h2[b].y & 0xFFFFu));
+                    const float o3 = fmaf(g, vi.w, bf16_bits_to_f32(h2[b].y >> 16));
+                    reinterpret_cast<uint2*>(ht + (int64_t)b * d)[i] =
+                        make_uint2(bf16x2_pack_rn(o0, o1), bf16x2_pack_rn(o2, o3));
+                }
         }
         __syncthreads();
     }
@@ -344,12 +389,14 @@ cudaError_t launch_gather(const Geometry& g, const uint32_t* rows, int64_t T,
     return cudaGetLastError();
 }
 
-cudaError_t launch_gate(const Geometry& g, const float* kv, const uint4* windows, int64_t T,
-                        uint16_t* hidden, const float* wq, const float* wk, float* gates,
-                        cudaStream_t s) {
+cudaError_t launch_gate(const Geometry& g, const float* kv, int nsplit, int64_t split_stride,
+                        const uint4* windows, int64_t T, uint16_t* hidden, const float* wq,
+                        const float* wk, float* gates, cudaStream_t s) {
     if (T == 0) return cudaSuccess;
-    const int grid = (int)std::min<int64_t>(T, (int64_t)sm_count() * 8);
-    k_gate<<<grid, kGateThreads, 0, s>>>(kv, windows, T, g.hc, g.d, g.eps,
+    if (nsplit < 1 || nsplit > kGateMaxSplits || g.d % 4 != 0 || g.hc > 8)
+        return cudaErrorInvalidValue;
+    const int grid = (int)std::min<int64_t>(T, (int64_t)sm_count() * 16);
+    k_gate<<<grid, kGateThreads, 0, s>>>(kv, nsplit, split_stride, windows, T, g.hc, g.d, g.eps,
                                          hidden, wq, wk, gates);
     return cudaGetLastError();
 }

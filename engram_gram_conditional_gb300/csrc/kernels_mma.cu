@@ -164,6 +164,9 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
 }
 
 // ---- tcgen05 -------------------------------------------------------------------
+__device__ __forceinline__ void st_release_u32(uint32_t* p, uint32_t v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
 __device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
     uint32_t v;
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -389,6 +392,50 @@ __device__ __forceinline__ void prefetch_hidden(const MmaArgs& a, int tile, int 
     } else {
         for (int b = 0; b < a.hc; ++b)
             prefetch_l2(a.hidden + (t * a.hc + b) * (int64_t)a.d + (n0 - key_cols), kBN * 2);
+    }
+}
+
+// Gates of row t (every branch), from the per-(branch, column tile) sums the
+// key tiles published, added in tile order.
+__device__ __forceinline__ void row_gates(const MmaArgs& a, int64_t t, float (&g)[8]) {
+    const int P = a.d / kBN;
+#pragma unroll
+    for (int b = 0; b < 8; ++b) g[b] = 0.f;
+    // one branch at a time (its loads all in flight), then the gate into its
+    // static register slot
+#pragma unroll 1
+    for (int b = 0; b < a.hc; ++b) {
+        const float* pp = a.partials + (t * a.hc + b) * (int64_t)P * 3;
+        float sum[3] = {0.f, 0.f, 0.f};
+        const int n4 = 3 * P / 4;
+        // rounds of 9 float4 = 12 (k^2, h^2, h w k) triples; 4 x 9 is a multiple
+        // of 3, so element 4 j + k of a round adds to sum (4 j + k) % 3
+        if (3 * P % 4 == 0) {
+#pragma unroll 1
+            for (int j0 = 0; j0 < n4; j0 += 9) {
+                float4 v[9];
+#pragma unroll
+                for (int j = 0; j < 9; ++j)
+                    if (j0 + j < n4) v[j] = __ldcg(reinterpret_cast<const float4*>(pp) + j0 + j);
+#pragma unroll
+                for (int j = 0; j < 9; ++j)
+                    if (j0 + j < n4) {
+                        const float e[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) sum[(4 * j + k) % 3] += e[k];
+                    }
+            }
+        } else {
+            for (int p = 0; p < P; ++p) {
+                sum[0] += __ldcg(pp + 3 * p);
+                sum[1] += __ldcg(pp + 3 * p + 1);
+                sum[2] += __ldcg(pp + 3 * p + 2);
+            }
+        }
+        const float gb = gate_from_sums(sum[0], sum[1], sum[2], a.d, a.eps);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            if (j == b) g[j] = gb;
     }
 }
 
@@ -841,7 +888,7 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
                     tmem_ld32(taddr + (uint32_t)(c * 32), r);
                     tmem_wait_ld();
                     if (t < a.T) {
-                        float4* dst = reinterpret_cast<float4*>(a.kv +
+                        float4* dst = reinterpret_cast<float4*>(a.kv + ks * a.kv_split_stride +
                                                                 t * a.ldkv + n0 + c * 32);
 #pragma unroll
                         for (int i = 0; i < 8; ++i)
@@ -851,7 +898,7 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
                                                  __uint_as_float(r[4 * i + 3]) * a.out_scale);
                     }
                 }
-            } else if (kMode == kEpiKeyPartial || (kMode == kEpiForward && n0 < a.hc * a.d)) {
+            } else if (kMode == kEpiForward && n0 < a.hc * a.d) {
                 const int branch = n0 / a.d;
                 const int col0 = n0 - branch * a.d;
                 const bool text = t < a.T && a.windows[t].x != kDead;
@@ -899,20 +946,38 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
                     pp[2] = shk;
                 }
                 if (kMode == kEpiForward) {
-                    // publish: the warp's sums, then one count for its quadrant
+                    // publish the warp's sums and count them in for its quadrant;
+                    // the quadrant's last key tile turns the sums into gates and
+                    // raises the quadrant's gates-ready flag
+                    uint32_t* const cnt = a.counters + 2 * (mb * 4 + q);
                     __threadfence();
                     __syncwarp();
-                    if (lane == 0) atomicAdd(a.counters + mb, 1u);
+                    uint32_t done = 0;
+                    if (lane == 0) done = atomicAdd(cnt, 1u) + 1u;
+                    done = __shfl_sync(0xFFFFFFFFu, done, 0);
+                    if (done == (uint32_t)(a.hc * a.d / kBN)) {
+                        __threadfence();
+                        float g[8];
+                        if (text) row_gates(a, t, g);
+                        if (t < a.T) {
+                            for (int b = 0; b < a.hc; ++b) {
+                                const float gb = text ? g[b] : 0.f;
+                                a.gbuf[t * a.hc + b] = gb;
+                                if (a.gates) a.gates[t * a.hc + b] = gb;
+                            }
+                        }
+                        __threadfence();
+                        __syncwarp();
+                        if (lane == 0) st_release_u32(cnt + 1, 1u);
+                    }
                 }
             } else {  // value tile
                 if (kMode == kEpiForward) {
-                    // wait (bounded) until every quadrant of every key tile of this
-                    // M block has counted in
+                    // wait (bounded) for the gates of this M block quadrant
                     if (lane == 0) {
-                        const uint32_t target = (uint32_t)(4 * (a.hc * a.d / kBN));
                         const uint64_t t0 = globaltimer();
                         uint32_t n = 0;
-                        while (ld_acquire_u32(a.counters + mb) < target) {
+                        while (ld_acquire_u32(a.counters + 2 * (mb * 4 + q) + 1) == 0u) {
                             if ((++n & 63u) == 0u &&
                                 ((long long)(globaltimer() - t0) > lim || *abort_flag)) {
                                 fail();
@@ -925,53 +990,26 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
                 }
                 const int cv = n0 - a.hc * a.d;
                 const bool text = t < a.T && a.windows[t].x != kDead;
-                const int P = a.d / kBN;
                 float g[8];
 #pragma unroll
                 for (int b = 0; b < 8; ++b) g[b] = 0.f;
-                // one branch at a time (its loads all in flight), then the gate
-                // into its static register slot
-#pragma unroll 1
-                for (int b = 0; b < a.hc; ++b) {
-                    if (text) {
-                        // L2 reads (written by other CTAs), summed in tile order
-                        const float* pp = a.partials + (t * a.hc + b) * (int64_t)P * 3;
-                        float sum[3] = {0.f, 0.f, 0.f};
-                        const int n4 = 3 * P / 4;
-                        // rounds of 9 float4 = 12 (k^2, h^2, h w k) triples; 4 x 9 is a
-                        // multiple of 3, so element 4 j + k of a round is sum (4 j + k) % 3
-                        if (3 * P % 4 == 0) {
-#pragma unroll 1
-                            for (int j0 = 0; j0 < n4; j0 += 9) {
-                                float4 v[9];
+                if (text) {
+                    if (a.hc == 4) {
+                        const float4 g4 = __ldcg(reinterpret_cast<const float4*>(a.gbuf + t * 4));
+                        g[0] = g4.x;
+                        g[1] = g4.y;
+                        g[2] = g4.z;
+                        g[3] = g4.w;
+                    } else {
 #pragma unroll
-                                for (int j = 0; j < 9; ++j)
-                                    if (j0 + j < n4)
-                                        v[j] = __ldcg(reinterpret_cast<const float4*>(pp) + j0 + j);
-#pragma unroll
-                                for (int j = 0; j < 9; ++j)
-                                    if (j0 + j < n4) {
-                                        const float e[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
-#pragma unroll
-                                        for (int k = 0; k < 4; ++k) sum[(4 * j + k) % 3] += e[k];
-                                    }
-                            }
-                        } else {
-                            for (int p = 0; p < P; ++p) {
-                                sum[0] += __ldcg(pp + 3 * p);
-                                sum[1] += __ldcg(pp + 3 * p + 1);
-                                sum[2] += __ldcg(pp + 3 * p + 2);
-                            }
-                        }
-                        const float gb = gate_from_sums(sum[0], sum[1], sum[2], a.d, a.eps);
-#pragma unroll
-                        for (int j = 0; j < 8; ++j)
-                            if (j == b) g[j] = gb;
+                        for (int b = 0; b < 8; ++b)
+                            if (b < a.hc) g[b] = __ldcg(a.gbuf + t * a.hc + b);
                     }
                 }
-                if (a.gates && n0 == a.hc * a.d && t < a.T) {
-                    for (int b = 0; b < a.hc; ++b) a.gates[t * a.hc + b] = text ? g[b] : 0.f;
-                }
+                // hidden += g v, two branches per round: their eight loads go out
+                // before any store (a store could alias a later load, so loads
+                // issued after it would each wait for memory in turn)
+                uint16_t* const hrow = a.hidden + t * a.hc * (int64_t)a.d + cv;
 #pragma unroll 1
                 for (int c = 0; c < kBN / 32; ++c) {
                     uint32_t r[32];
@@ -979,24 +1017,38 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
                     tmem_wait_ld();
                     if (text) {
 #pragma unroll
-                        for (int b = 0; b < 8; ++b) {
-                            if (b < a.hc) {
-                                uint4* hp = reinterpret_cast<uint4*>(
-                                    a.hidden + (t * a.hc + b) * (int64_t)a.d + cv + c * 32);
+                        for (int b0 = 0; b0 < 8; b0 += 2) {
+                            if (b0 < a.hc) {
+                                uint4 hv[2][4];
 #pragma unroll
-                                for (int i = 0; i < 4; ++i) {
-                                    const uint4 hv = hp[i];
-                                    const uint32_t hw[4] = {hv.x, hv.y, hv.z, hv.w};
-                                    uint32_t o[4];
+                                for (int bb = 0; bb < 2; ++bb)
+                                    if (b0 + bb < a.hc) {
+                                        const uint4* hp = reinterpret_cast<const uint4*>(
+                                            hrow + (int64_t)(b0 + bb) * a.d + c * 32);
 #pragma unroll
-                                    for (int e2 = 0; e2 < 4; ++e2) {
-                                        const float v0 = __uint_as_float(r[8 * i + 2 * e2]) * a.out_scale;
-                                        const float v1 = __uint_as_float(r[8 * i + 2 * e2 + 1]) * a.out_scale;
-                                        o[e2] = bf16x2_pack_rn(fmaf(g[b], v0, bf16_lo(hw[e2])),
-                                                               fmaf(g[b], v1, bf16_hi(hw[e2])));
+                                        for (int i = 0; i < 4; ++i) hv[bb][i] = hp[i];
                                     }
-                                    hp[i] = make_uint4(o[0], o[1], o[2], o[3]);
-                                }
+#pragma unroll
+                                for (int bb = 0; bb < 2; ++bb)
+                                    if (b0 + bb < a.hc) {
+                                        uint4* hp = reinterpret_cast<uint4*>(
+                                            hrow + (int64_t)(b0 + bb) * a.d + c * 32);
+                                        const float gb = g[b0 + bb];
+#pragma unroll
+                                        for (int i = 0; i < 4; ++i) {
+                                            const uint32_t hw[4] = {hv[bb][i].x, hv[bb][i].y,
+                                                                    hv[bb][i].z, hv[bb][i].w};
+                                            uint32_t o[4];
+#pragma unroll
+                                            for (int e2 = 0; e2 < 4; ++e2) {
+                                                const float v0 = __uint_as_float(r[8 * i + 2 * e2]) * a.out_scale;
+                                                const float v1 = __uint_as_float(r[8 * i + 2 * e2 + 1]) * a.out_scale;
+                                                o[e2] = bf16x2_pack_rn(fmaf(gb, v0, bf16_lo(hw[e2])),
+                                                                       fmaf(gb, v1, bf16_hi(hw[e2])));
+                                            }
+                                            hp[i] = make_uint4(o[0], o[1], o[2], o[3]);
+                                        }
+                                    }
                             }
                         }
                     }
@@ -1078,6 +1130,12 @@ cudaError_t launch_project(const MmaArgs& a, const CUtensorMap& tmA, const CUten
     return launch<kASrcTma, false, kEpiStoreKv>(a, tmA, tmB, s);
 }
 
+
+cudaError_t launch_project_split(const MmaArgs& a, bool f16, const CUtensorMap& tmA,
+                                 const CUtensorMap& tmB, cudaStream_t s) {
+    if (f16) return launch<kASrcTma, true, kEpiStoreKv>(a, tmA, tmB, s);
+    return launch<kASrcTma, false, kEpiStoreKv>(a, tmA, tmB, s);
+}
 
 cudaError_t launch_forward_tma(const MmaArgs& a, bool f16, const CUtensorMap& tmA,
                                const CUtensorMap& tmB, cudaStream_t s) {

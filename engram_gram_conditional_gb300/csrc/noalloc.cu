@@ -8,13 +8,14 @@
 // outputs they already own, but cannot hand engram_forward a freshly
 // allocated workspace, and a cudaMalloc/cudaFree inside a hot path would also
 // synchronise the device.  This entry point keeps the forward's scratch (the
-// per-token, per-branch, per-tile gate sums) in a fixed buffer that is part of
-// the library's device image: it is reserved on every GPU that loads the
-// library and stays there until the process exits.
+// per-token, per-branch, per-tile gate sums, the gates and the tile counters)
+// in a fixed buffer that is part of the library's device image: it is
+// reserved on every GPU that loads the library and stays there until the
+// process exits.
 //
-// The buffer is shared by every call in the process.  Nothing in it needs
-// clearing between calls (the key tiles of a call write every sum its value
-// tiles read), but two calls whose kernels overlap on the GPU - on different
+// The buffer is shared by every call in the process.  Each call zeroes its
+// counters on its stream and its key tiles write every sum and gate its value
+// tiles read, but two calls whose kernels overlap on the GPU - on different
 // streams, or from different threads - race on it.  Order such calls on one
 // stream, or use engram_forward with a workspace per stream.
 #include <cuda_runtime.h>

@@ -214,7 +214,8 @@ engram_status engram_gather_dequant(const engram_ctx* ctx, int layer, const uint
 engram_status engram_project(const engram_ctx* ctx, int layer, const uint16_t* d_emb, int64_t T,
                              float* d_kv, void* stream);
 /* a5: gate and update hidden in place; image rows (window slot 0 == DEAD)
- * pass through.  d_gates may be NULL. */
+ * pass through.  d_kv, d_windows and d_hidden 16-byte aligned; d_gates may be
+ * NULL. */
 engram_status engram_gate(const engram_ctx* ctx, int layer, const float* d_kv,
                           const uint32_t* d_windows, int64_t T, uint16_t* d_hidden,
                           float* d_gates, void* stream);
@@ -247,10 +248,10 @@ engram_status engram_forward_staged(const engram_ctx* ctx, int layer, const uint
  * have no counterpart: this is a deployment variant.  A serving engine that
  * reserves the GPU's memory for its own pools, or a plugin host that forbids
  * its plugins to allocate, can pass only the buffers it already owns; this
- * call needs no workspace argument because its scratch (the gate sums) lives
+ * call needs no workspace argument because its scratch (the gate sums and gates) lives
  * in an 8 MiB buffer inside the library's device image, held on every GPU
  * that loads the library until the process exits.  It makes no cudaMalloc or
- * cudaFree call.  T is limited to what 8 MiB holds (8,737 tokens at hc 4,
+ * cudaFree call.  T is limited to what 8 MiB holds (8,592 tokens at hc 4,
  * d 5,120); a larger T returns ENGRAM_EINVAL with the limit in the message.
  * K is never split here (the partial tiles would not fit), so a small batch
  * runs on fewer SMs than engram_forward would give it.

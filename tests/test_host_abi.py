@@ -227,7 +227,7 @@ def test_device_calls_validate_before_launch():
     assert e.value.status == eg.EINVAL
     eg.engram_hash(ctx, 0, None, 0, None)  # T = 0 is a no-op
     # gate sums [T][hc][d/256][3] fp32 and one counter per 128-token block, 256-byte aligned
-    assert eg.engram_workspace_bytes(ctx, 64) == 64 * 2 * 1 * 3 * 4 + 256
+    assert eg.engram_workspace_bytes(ctx, 64) == 64 * 2 * 1 * 3 * 4 + 64 * 2 * 4 + 256
     assert eg.engram_workspace_bytes(ctx, 0) == 0
     eg.engram_ctx_destroy(ctx)
 
