@@ -304,8 +304,9 @@ def main():
         hid_h.append(synth.normal_bf16((T, w.hc, w.d), 1.0, w.seed, 1000 + base_session + i))
     d_win = [torch.from_numpy(x.view(np.int32)).to(dev) for x in win_h]
     d_hid = [torch.from_numpy(x.view(np.int16)).to(dev) for x in hid_h]
-    d_ws = torch.empty(eg.engram_forward_staged_workspace_bytes(ctx, T), dtype=torch.uint8,
-                       device=dev)
+    # one workspace serves both entries: it holds the larger of the two
+    d_ws = torch.empty(max(eg.engram_forward_staged_workspace_bytes(ctx, T),
+                           eg.engram_workspace_bytes(ctx, T)), dtype=torch.uint8, device=dev)
     sptr = stream.cuda_stream
 
     def step(i):

@@ -126,10 +126,12 @@ struct LayerState {
     bool bound = false;
     engram_layer_weights w{};
     CUtensorMap tm_wkv{};          // the caller's BF16 wkv
+    CUtensorMap tm_wkv_half{};     // the same with 128-row boxes (CTA-pair kernels)
     // FP16 operand path of the fused kernels (see engram_layer_info)
     bool f16 = false;
     uint16_t* wkv_f16 = nullptr;   // library-owned copy, wkv x 2^wkv_exp
     CUtensorMap tm_wkv_f16{};
+    CUtensorMap tm_wkv_f16_half{};
     int wkv_exp = 0;
     int a_exp_shift = 0;
     uint32_t scale_min = 0, scale_max = 0;
@@ -209,6 +211,7 @@ MmaArgs mma_args(const engram_ctx* ctx, int layer, int64_t T) {
     a.group_m = 16;
     a.k_splits = 1;
     a.kv_split_stride = 0;
+    a.b_tiled = L.f16 ? 1 : 0;  // the FP16 wkv copy is tiled, the caller's BF16 wkv is not
     a.hc = (int)ctx->desc.hc;
     a.d = (int)ctx->desc.d;
     a.eps = (float)ctx->desc.eps;
@@ -487,8 +490,10 @@ engram_status engram_layer_bind(engram_ctx* ctx, int layer, const engram_layer_w
         if (e != cudaSuccess) return cuda_fail(e, "cudaMemset");
         ctx->device = dev;
     }
-    CUtensorMap tm;
+    CUtensorMap tm, tm_half;
     e = make_tma_16bit(&tm, w->wkv, (uint64_t)ctx->N, (uint64_t)ctx->K, kBN, false);
+    if (e == cudaSuccess)
+        e = make_tma_16bit(&tm_half, w->wkv, (uint64_t)ctx->N, (uint64_t)ctx->K, kBN / 2, false);
     if (e != cudaSuccess) return cuda_fail(e, "wkv tensor map");
 
     // Operand path of the fused kernels.  FP16 operands hold the same values
@@ -535,10 +540,16 @@ engram_status engram_layer_bind(engram_ctx* ctx, int layer, const engram_layer_w
             L.wkv_f16 = nullptr;
             return fail(ENGRAM_ENOMEM, "cudaMalloc of the FP16 wkv copy");
         }
-        e = launch_bf16_to_f16(w->wkv, L.wkv_f16, (uint64_t)ctx->N * ctx->K, ldexpf(1.0f, wexp), 0);
+        // the copy is stored as 128 x 64 tiles, each 16 KB contiguous: one
+        // tensor map over them, viewed as [N K / 64][64] with 128-row boxes,
+        // feeds both the single-CTA (two boxes per stage) and the pair kernels
+        e = launch_wkv_to_f16_tiles(w->wkv, L.wkv_f16, (uint64_t)ctx->N, (uint64_t)ctx->K,
+                                    ldexpf(1.0f, wexp), 0);
         if (e == cudaSuccess) e = cudaDeviceSynchronize();
         if (e == cudaSuccess)
-            e = make_tma_16bit(&L.tm_wkv_f16, L.wkv_f16, (uint64_t)ctx->N, (uint64_t)ctx->K, kBN, true);
+            e = make_tma_16bit(&L.tm_wkv_f16, L.wkv_f16, (uint64_t)ctx->N * ctx->K / kBK, kBK,
+                               kBN / 2, true);
+        if (e == cudaSuccess) L.tm_wkv_f16_half = L.tm_wkv_f16;
         if (e != cudaSuccess) {
             cudaFree(L.wkv_f16);
             L.wkv_f16 = nullptr;
@@ -556,6 +567,7 @@ engram_status engram_layer_bind(engram_ctx* ctx, int layer, const engram_layer_w
     L.scale_max = smax;
     L.w = bw;
     L.tm_wkv = tm;
+    L.tm_wkv_half = tm_half;
     L.bound = true;
     return ok();
 }
@@ -733,6 +745,7 @@ engram_status engram_project(const engram_ctx* ctx, int layer, const uint16_t* d
     a.n_tiles = ctx->N / kBN;
     a.kv = d_kv;
     a.ldkv = ctx->N;
+    a.b_tiled = 0;  // the caller's BF16 wkv, row-major
     e = launch_project(a, tmA, ctx->layers[layer].tm_wkv, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "project launch");
     return ok();
@@ -767,6 +780,10 @@ engram_status engram_forward(const engram_ctx* ctx, int layer, const uint32_t* d
 // wkv stream in the SM's memory pipeline, which a single wave of tiles cannot
 // hide, while the separate gate kernel has the whole GPU to itself.
 static int staged_splits(const engram_ctx* ctx, int64_t T) { return forward_k_splits(ctx, T, 8); }
+
+// The staged GEMMs run on CTA pairs (256-token tiles) unless the batch holds a
+// single 128-token block, which would leave half of every pair idle.
+static bool use_pairs(const MmaArgs& a) { return a.m_blocks >= 2; }
 
 size_t engram_forward_staged_workspace_bytes(const engram_ctx* ctx, int64_t T) {
     if (!ctx || T <= 0) return 0;
@@ -817,7 +834,9 @@ engram_status engram_forward_staged(const engram_ctx* ctx, int layer, const uint
         a.kv = reinterpret_cast<float*>(rest);
         a.ldkv = ctx->N;
         a.kv_split_stride = T * (int64_t)ctx->N;
-        e = launch_project_split(a, L.f16, tmA, L.f16 ? L.tm_wkv_f16 : L.tm_wkv, s);
+        e = use_pairs(a)
+                ? launch_project_split_pair(a, L.f16, tmA, L.f16 ? L.tm_wkv_f16_half : L.tm_wkv_half, s)
+                : launch_project_split(a, L.f16, tmA, L.f16 ? L.tm_wkv_f16 : L.tm_wkv, s);
         if (e != cudaSuccess) return cuda_fail(e, "split projection launch");
         e = launch_gate(geometry(ctx), a.kv, splits, a.kv_split_stride, a.windows, T, d_hidden,
                         L.w.wq, L.w.wk, d_gates, s);
@@ -826,7 +845,8 @@ engram_status engram_forward_staged(const engram_ctx* ctx, int layer, const uint
     }
     e = forward_bind_ws(ctx, T, 8, rest, a, s);
     if (e != cudaSuccess) return cuda_fail(e, "forward counters");
-    e = launch_forward_tma(a, L.f16, tmA, L.f16 ? L.tm_wkv_f16 : L.tm_wkv, s);
+    e = use_pairs(a) ? launch_forward_tma_pair(a, L.f16, tmA, L.f16 ? L.tm_wkv_f16_half : L.tm_wkv_half, s)
+                     : launch_forward_tma(a, L.f16, tmA, L.f16 ? L.tm_wkv_f16 : L.tm_wkv, s);
     if (e != cudaSuccess) return cuda_fail(e, "staged forward launch");
     return ok();
 }

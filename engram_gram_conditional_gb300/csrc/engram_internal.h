@@ -54,6 +54,7 @@ struct MmaArgs {
     int m_blocks;      // ceil(T / kBM)
     int group_m;       // tile rasterisation: M blocks per group
     int k_splits;      // split-K factor (>= 1); the tile list holds every (tile, split)
+    int b_tiled;       // wkv map over 128 x 64 tiles (the FP16 copy), else row-major [N][K]
     int64_t kv_split_stride;  // kEpiStoreKv: floats between the kv buffers of two splits
     int hc, d;
     float eps;
@@ -112,9 +113,11 @@ cudaError_t launch_gather_stage(const HashParams& hp, const uint4* windows, int6
                                 const uint8_t* table, const uint8_t* scales, uint64_t nrows,
                                 bool f16, int exp_shift, uint16_t* e, uint32_t* err,
                                 cudaStream_t s);
-// dst[i] = fp16(bf16 src[i] * scale), round to nearest even.
-cudaError_t launch_bf16_to_f16(const uint16_t* src, uint16_t* dst, uint64_t n, float scale,
-                               cudaStream_t s);
+// FP16 copy of the BF16 wkv [N][K] (N % 128 == 0, K % 64 == 0), values x
+// scale rounded to nearest even, stored as 128 x 64 tiles: element (n, k) at
+// ((n / 128) (K / 64) + k / 64) 8192 + (n % 128) 64 + k % 64.
+cudaError_t launch_wkv_to_f16_tiles(const uint16_t* src, uint16_t* dst, uint64_t N, uint64_t K,
+                                   float scale, cudaStream_t s);
 
 // kernels_mma.cu
 // Host-side TMA descriptor for a row-major 16-bit (BF16 or FP16) matrix
@@ -129,6 +132,13 @@ cudaError_t launch_forward_phase(const MmaArgs& a, int mode, bool f16, bool buck
 // split over K into a.k_splits partial kv buffers (the gate runs after it).
 cudaError_t launch_project_split(const MmaArgs& a, bool f16, const CUtensorMap& tmA,
                                  const CUtensorMap& tmB, cudaStream_t s);
+// The same two GEMMs on CTA pairs (clusters of two SMs, tcgen05 cta_group::2):
+// each pair computes 256-token x 256-output tiles, each CTA holding half of the
+// wkv tile, so tmB_half is a wkv tensor map with 128-row boxes.
+cudaError_t launch_project_split_pair(const MmaArgs& a, bool f16, const CUtensorMap& tmA,
+                                      const CUtensorMap& tmB_half, cudaStream_t s);
+cudaError_t launch_forward_tma_pair(const MmaArgs& a, bool f16, const CUtensorMap& tmA,
+                                   const CUtensorMap& tmB_half, cudaStream_t s);
 // Staged forward, step 2: the whole forward GEMM with a TMA-fed A operand.
 cudaError_t launch_forward_tma(const MmaArgs& a, bool f16, const CUtensorMap& tmA,
                                const CUtensorMap& tmB, cudaStream_t s);

@@ -348,12 +348,19 @@ __global__ void k_absmax_bf16(const uint16_t* __restrict__ x, uint64_t n, uint32
     if ((threadIdx.x & 31) == 0) atomicMax(out, m);
 }
 
-__global__ void k_bf16_to_f16(const uint16_t* __restrict__ src, uint16_t* __restrict__ dst,
-                              uint64_t n, float scale) {
-    for (uint64_t i = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; i < n;
+// FP16 copy of wkv [N][K] in 128 x 64 tiles: the tile of rows [128 nb, 128 nb
+// + 128) and columns [64 kb, 64 kb + 64) is 16 KB of contiguous row-major
+// memory at tile index nb (K / 64) + kb.  A TMA box of one tile then reads
+// 16 contiguous KB instead of 128 rows of 128 bytes spread over 1.5 MB.
+__global__ void k_wkv_to_f16_tiles(const uint16_t* __restrict__ src, uint16_t* __restrict__ dst,
+                                   uint64_t N, uint64_t K, float scale) {
+    const uint64_t n_el = N * K, KB = K / 64;
+    for (uint64_t i = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; i < n_el;
          i += (uint64_t)gridDim.x * blockDim.x) {
+        const uint64_t n = i / K, k = i - n * K;
+        const uint64_t o = (((n >> 7) * KB + (k >> 6)) * 128 + (n & 127)) * 64 + (k & 63);
         const float v = __uint_as_float((uint32_t)src[i] << 16) * scale;
-        dst[i] = __half_as_ushort(__float2half_rn(v));
+        dst[o] = __half_as_ushort(__float2half_rn(v));
     }
 }
 
@@ -414,10 +421,10 @@ cudaError_t launch_absmax_bf16(const uint16_t* x, uint64_t n, uint32_t* out, cud
     return cudaGetLastError();
 }
 
-cudaError_t launch_bf16_to_f16(const uint16_t* src, uint16_t* dst, uint64_t n, float scale,
-                               cudaStream_t s) {
-    if (n == 0) return cudaSuccess;
-    k_bf16_to_f16<<<grid_for((int64_t)n, 256, 8), 256, 0, s>>>(src, dst, n, scale);
+cudaError_t launch_wkv_to_f16_tiles(const uint16_t* src, uint16_t* dst, uint64_t N, uint64_t K,
+                                   float scale, cudaStream_t s) {
+    if (N == 0 || K == 0 || N % 128 != 0 || K % 64 != 0) return cudaErrorInvalidValue;
+    k_wkv_to_f16_tiles<<<grid_for((int64_t)(N * K), 256, 8), 256, 0, s>>>(src, dst, N, K, scale);
     return cudaGetLastError();
 }
 

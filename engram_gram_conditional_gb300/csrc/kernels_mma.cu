@@ -49,7 +49,7 @@ namespace {
 constexpr int kThreads = 512;  // four warpgroups
 constexpr int kProdWarps = 8;  // A producers: warps 0..7, 16 token rows each
 constexpr int kRowsPerProd = kBM / kProdWarps;
-constexpr int kWarpProd = 0, kWarpEpi = 8, kWarpTma = 12, kWarpMma = 13;
+constexpr int kWarpProd = 0, kWarpEpi = 8, kWarpTma = 12, kWarpMma = 13, kWarpTmaA = 14;
 // Register split (setmaxnreg): launch budget 512 x 128 = 65,536 registers;
 // 128 x (2 x 144 + 168 + 56) = 65,536 - the four shares add up to it exactly
 // (and each scheduler holds one warp of each group: 32 x 512 = 16,384).
@@ -68,19 +68,29 @@ constexpr int kTmemCols = 2 * kBN;
 
 // Source of the A operand.
 enum ASource : int {
-    kASrcTma = 0,           // TMA tiles of a BF16 emb matrix (unfused projection)
+    kASrcTma = 0,           // TMA tiles of a 16-bit operand matrix (unfused projection)
     kASrcGatherKb = 1,      // fused: k-block gather of 64-byte row slices
     kASrcGatherBucket = 2,  // fused: bucket gather of whole 256-byte rows
+    kASrcTmaPair = 3,       // TMA tiles, a CTA pair per 256 x 256 tile (cta_group::2)
 };
+
+// CTA pair (cluster of two SMs): the pair computes a 256-token x 256-output
+// tile with tcgen05.mma.cta_group::2.  Each CTA stages its own 128 tokens of A
+// and its own half (128 rows) of the wkv tile, so an SM takes in 32 KB per
+// k-block instead of 48 KB; the accumulator rows of each CTA land in its own
+// TMEM.  The even CTA issues the MMAs.
+constexpr int kBStageHalf = kBStage / 2;  // 16 KB
 
 // Shared-memory layout of each variant.
 template <int kASrc>
 struct Layout {
-    static constexpr int kA = kASrc == kASrcGatherBucket ? 8 : 4;  // A ring stages
-    static constexpr int kB = kASrc == kASrcGatherBucket ? 3 : 4;  // B ring stages
+    static constexpr bool kPair = kASrc == kASrcTmaPair;
+    static constexpr int kA = kASrc == kASrcGatherBucket ? 8 : 4;              // A ring stages
+    static constexpr int kB = kASrc == kASrcGatherBucket ? 3 : kPair ? 8 : 4;  // B ring stages
+    static constexpr int kBStageBytes = kPair ? kBStageHalf : kBStage;
     static constexpr int kOffA = 0;
     static constexpr int kOffB = kOffA + kA * kAStage;
-    static constexpr int kOffRows = kOffB + kB * kBStage;
+    static constexpr int kOffRows = kOffB + kB * kBStageBytes;
     static constexpr int kRowsBytes = kASrc == kASrcGatherKb ? kBM * kRowStride * 4 : 0;
     static constexpr int kOffBar = kOffRows + kRowsBytes;
     // a_full[kA], a_empty[kA], b_full[kB], b_empty[kB], tfull[2], tempty[2]
@@ -94,11 +104,11 @@ struct Layout {
 
 // Instruction descriptor, kind::f16: F32 accumulate (bits 4-5 = 1), A and B
 // both BF16 (bits 7-9 = 1, 10-12 = 1) or both FP16 (0, 0), both K-major,
-// N >> 3 at bit 17, M >> 4 at bit 24.
-template <bool kF16>
+// N >> 3 at bit 17, M >> 4 at bit 24 (M = 128 for one CTA, 256 for a pair).
+template <bool kF16, int kM = kBM>
 __host__ __device__ constexpr uint32_t idesc() {
     return (1u << 4) | (kF16 ? 0u : (1u << 7) | (1u << 10)) | ((uint32_t)(kBN >> 3) << 17) |
-           ((uint32_t)(kBM >> 4) << 24);
+           ((uint32_t)(kM >> 4) << 24);
 }
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -150,6 +160,16 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
                                             int x, int y) {
     asm volatile(
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+        "l"((uint64_t)map), "r"(bar), "r"(x), "r"(y)
+        : "memory");
+}
+// CTA-pair form: the completion is signalled on `bar`, a shared::cluster
+// address that may lie in the other CTA of the pair.
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                                 int x, int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes "
         "[%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
         "l"((uint64_t)map), "r"(bar), "r"(x), "r"(y)
         : "memory");
@@ -215,6 +235,77 @@ __device__ __forceinline__ void umma_commit(uint32_t bar) {
         "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
         : "memory");
 }
+// ---- CTA pair (cluster of two) ------------------------------------------------------
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// Every thread of both CTAs; orders barrier inits and teardown across the pair.
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
+                 ::: "memory");
+}
+// Shared::cluster address of the same shared variable in CTA `rank` of the pair.
+__device__ __forceinline__ uint32_t map_rank(uint32_t saddr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// mbar_wait for a barrier that the other CTA of the pair also arrives on.
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
+                                                  volatile int* abort_flag, long long limit_ns) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    for (uint32_t n = 1;; ++n) {
+        if (mbar_try_wait_cluster(bar, parity)) return true;
+        if ((n & 31u) == 0u) {
+            if (*abort_flag) return false;
+            if ((long long)(globaltimer() - t0) > limit_ns) return false;
+        }
+    }
+}
+// TMEM of both CTAs, allocated collectively by one warp of each.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t slot, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void umma_f16kind_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                                  uint32_t idesc_bits, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc_bits), "r"(accumulate)
+        : "memory");
+}
+// Arrives on the barrier at this offset in both CTAs once the issued MMAs finish.
+__device__ __forceinline__ void umma_commit_pair(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
+        "[%0], %1;" ::"r"(bar), "h"((uint16_t)3)
+        : "memory");
+}
+
 // 32 lanes x 32 consecutive 32-bit columns: thread i gets row (lane base + i).
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile(
@@ -356,11 +447,11 @@ __device__ __forceinline__ int split_k_quadrant(const MmaArgs& a, int mb, int nt
 // CTAs in flight share wkv tiles in L2 while the group's gathered rows stay
 // L2-resident.
 // With split-K (small M) the order is (N tile, split) outer, M block inner.
-__device__ __forceinline__ void tile_coords(const MmaArgs& a, int tile, int& mb, int& nt,
-                                            int& ks) {
+__device__ __forceinline__ void tile_coords(const MmaArgs& a, int m_units, int tile, int& mb,
+                                            int& nt, int& ks) {
     if (a.k_splits > 1) {
-        mb = tile % a.m_blocks;
-        const int r = tile / a.m_blocks;
+        mb = tile % m_units;
+        const int r = tile / m_units;
         ks = r % a.k_splits;
         nt = r / a.k_splits;
         return;
@@ -369,18 +460,16 @@ __device__ __forceinline__ void tile_coords(const MmaArgs& a, int tile, int& mb,
     const int per_group = a.group_m * a.n_tiles;
     const int g = tile / per_group;
     const int first_m = g * a.group_m;
-    const int gm = min(a.group_m, a.m_blocks - first_m);
+    const int gm = min(a.group_m, m_units - first_m);
     const int r = tile - g * per_group;
     nt = r / gm;
     mb = first_m + (r - nt * gm);
 }
 
 // Forward epilogue: starts the L2 loads of the hidden slices that row m of
-// `tile` will read (key tile: its branch's 256 columns; value tile: those
+// the tile (M block mb, N tile nt) will read (key tile: its branch's 256 columns; value tile: those
 // columns of every branch), so that the epilogue's own loads hit L2.
-__device__ __forceinline__ void prefetch_hidden(const MmaArgs& a, int tile, int m) {
-    int mb, nt, ks;
-    tile_coords(a, tile, mb, nt, ks);
+__device__ __forceinline__ void prefetch_hidden(const MmaArgs& a, int mb, int nt, int m) {
     const int64_t t = (int64_t)mb * kBM + m;
     if (t >= a.T) return;
     const int n0 = (a.n_tile_begin + nt) * kBN;
@@ -596,7 +685,11 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
       const __grid_constant__ MmaArgs a) {
     using L = Layout<kASrc>;
     constexpr int kA = L::kA, kB = L::kB;
-    constexpr bool kFusedA = kASrc != kASrcTma;
+    constexpr bool kPair = L::kPair;
+    constexpr bool kFusedA = kASrc != kASrcTma && !kPair;
+    // in a pair, the even CTA issues the MMAs; the odd one only feeds them
+    const uint32_t rank = kPair ? cluster_ctarank() : 0u;
+    const bool issuer = rank == 0u;
     extern __shared__ uint8_t smem_dyn[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~(uintptr_t)1023);
@@ -612,11 +705,13 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
     auto tempty = [&](int acc) { return bar0 + 8u * (uint32_t)(2 * kA + 2 * kB + 2 + acc); };
     const uint32_t a_base = sbase + L::kOffA;
     auto a_stage = [&](int s) { return a_base + (uint32_t)(s * kAStage); };
-    auto b_stage = [&](int s) { return sbase + L::kOffB + (uint32_t)(s * kBStage); };
+    auto b_stage = [&](int s) { return sbase + L::kOffB + (uint32_t)(s * L::kBStageBytes); };
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffFlag);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffTmem);
 
     if (threadIdx.x == 0) {
+        // in a pair, the issuer's full barriers take the bytes of both CTAs'
+        // copies (the odd CTA's own full barriers stay unused)
         for (int s = 0; s < kA; ++s) {
             mbar_init(a_full(s), kFusedA ? (uint32_t)kProdWarps : 1u);  // producer warps or TMA
             mbar_init(a_empty(s), 1u);
@@ -627,7 +722,7 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
         }
         for (int acc = 0; acc < 2; ++acc) {
             mbar_init(tfull(acc), 1u);
-            mbar_init(tempty(acc), 4u);
+            mbar_init(tempty(acc), kPair ? 8u : 4u);  // epilogue warps (of both CTAs)
         }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -636,15 +731,35 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
         asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmB) : "memory");
         if (!kFusedA) asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmA) : "memory");
     }
-    if (warp == kWarpMma) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    if (warp == kWarpMma) {
+        if constexpr (kPair)
+            tmem_alloc_pair(smem_u32(tmem_slot), kTmemCols);
+        else
+            tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    }
     tc_fence_before();
     __syncthreads();
+    if constexpr (kPair) cluster_sync();  // both CTAs' barriers exist before either signals the other
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    const int total = a.m_blocks * a.n_tiles * a.k_splits;
+    // work items: (M unit, N tile, split); a CTA pair shares one item sequence
+    // and its M unit is two M blocks, this CTA's being 2 mu + rank
+    const int m_units = kPair ? (a.m_blocks + 1) / 2 : a.m_blocks;
+    const int total = m_units * a.n_tiles * a.k_splits;
+    const int item0 = kPair ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+    const int istep = kPair ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+    auto coords = [&](int tile, int& mb, int& nt, int& ks) {
+        tile_coords(a, m_units, tile, mb, nt, ks);
+        if constexpr (kPair) mb = 2 * mb + (int)rank;
+    };
     const int KB = a.K / kBK;
     const long long lim = a.wait_limit_ns;
+    // With a TMA-fed A, each N tile walks its k-blocks from its own starting
+    // point, so that the CTAs in flight do not all read the same A k-block
+    // (the operand matrix of a small batch is shared by every N tile) at the
+    // same moment.  Gathered A operands come in order.
+    auto k_rotation = [&](int nt, int nkb) { return kFusedA ? 0 : (nt * 13) % nkb; };
 
     auto fail = [&]() {
         *abort_flag = 1;
@@ -654,57 +769,94 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
     if (warp >= kWarpTma) {
         setmaxnreg_dec<kRegsCtl>();
     }
-    if (warp == kWarpTma) {
+    if (warp == kWarpTma || (!kFusedA && warp == kWarpTmaA)) {
+        // TMA producers: warp 12 loads the wkv tiles, warp 14 the A tiles of
+        // the TMA-fed variants, each running ahead on its own ring
+        const bool do_b = warp == kWarpTma;
         if (lane == 0) {
             int it = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+            for (int tile = item0; tile < total && ok; tile += istep) {
                 int mb, nt, ks;
-                tile_coords(a, tile, mb, nt, ks);
+                coords(tile, mb, nt, ks);
                 const int n0 = (a.n_tile_begin + nt) * kBN;
-                const int kb_hi = (ks + 1) * KB / a.k_splits;
-                for (int kb = ks * KB / a.k_splits; kb < kb_hi && !a.starve_b; ++kb, ++it) {
+                const int kb_lo = ks * KB / a.k_splits, nkb = (ks + 1) * KB / a.k_splits - kb_lo;
+                const int rot = k_rotation(nt, nkb);
+                for (int j = 0; j < nkb && !a.starve_b; ++j, ++it) {
+                    const int kb = kb_lo + (j + rot) % nkb;
                     const int sb = it % kB;
-                    if (!mbar_wait(b_empty(sb), ((uint32_t)(it / kB) & 1u) ^ 1u, abort_flag, lim)) {
-                        fail();
-                        ok = false;
-                        break;
-                    }
-                    mbar_expect_tx(b_full(sb), kBStage);
-                    tma_load_2d(b_stage(sb), &tmB, b_full(sb), kb * kBK, n0);
-                    if (!kFusedA) {
+                    if (do_b) {
+                        if (!mbar_wait(b_empty(sb), ((uint32_t)(it / kB) & 1u) ^ 1u, abort_flag, lim)) {
+                            fail();
+                            ok = false;
+                            break;
+                        }
+                        // wkv rows [r, r + 128) of k-block kb: in the tiled FP16 copy,
+                        // box row ((r / 128) KB + kb) 128 at column 0
+                        auto b_x = [&](int r) { return a.b_tiled ? 0 : kb * kBK; };
+                        auto b_y = [&](int r) { return a.b_tiled ? ((r >> 7) * KB + kb) * 128 : r; };
+                        if constexpr (kPair) {
+                            // each CTA loads its half of the wkv tile (rows n0 + 128
+                            // rank) and signals the issuer, who expects both halves
+                            const int r = n0 + (int)rank * (kBN / 2);
+                            if (issuer) mbar_expect_tx(b_full(sb), 2 * L::kBStageBytes);
+                            tma_load_2d_pair(b_stage(sb), &tmB, map_rank(b_full(sb), 0), b_x(r), b_y(r));
+                        } else {
+                            mbar_expect_tx(b_full(sb), L::kBStageBytes);
+                            if (a.b_tiled) {  // two 128-row boxes, the second 16 KB further
+                                tma_load_2d(b_stage(sb), &tmB, b_full(sb), b_x(n0), b_y(n0));
+                                tma_load_2d(b_stage(sb) + kBStageHalf, &tmB, b_full(sb), b_x(n0 + 128),
+                                            b_y(n0 + 128));
+                            } else {
+                                tma_load_2d(b_stage(sb), &tmB, b_full(sb), kb * kBK, n0);
+                            }
+                        }
+                    } else {
                         const int sa = it % kA;
                         if (!mbar_wait(a_empty(sa), ((uint32_t)(it / kA) & 1u) ^ 1u, abort_flag, lim)) {
                             fail();
                             ok = false;
                             break;
                         }
-                        mbar_expect_tx(a_full(sa), kAStage);
-                        tma_load_2d(a_stage(sa), &tmA, a_full(sa), kb * kBK, mb * kBM);
+                        if constexpr (kPair) {
+                            if (issuer) mbar_expect_tx(a_full(sa), 2 * kAStage);
+                            tma_load_2d_pair(a_stage(sa), &tmA, map_rank(a_full(sa), 0), kb * kBK,
+                                             mb * kBM);
+                        } else {
+                            mbar_expect_tx(a_full(sa), kAStage);
+                            tma_load_2d(a_stage(sa), &tmA, a_full(sa), kb * kBK, mb * kBM);
+                        }
                     }
                 }
             }
         }
     } else if (warp == kWarpMma) {
-        if (lane == 0) {
+        // waits on barriers that the other CTA of a pair arrives on use cluster scope
+        auto wait = [&](uint32_t bar, uint32_t parity) {
+            return kPair ? mbar_wait_cluster(bar, parity, abort_flag, lim)
+                         : mbar_wait(bar, parity, abort_flag, lim);
+        };
+        if (lane == 0 && issuer) {
             int it = 0, tc = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++tc) {
+            for (int tile = item0; tile < total && ok; tile += istep, ++tc) {
                 const int acc = tc & 1;
                 const uint32_t aph = (uint32_t)(tc >> 1) & 1u;
-                if (!mbar_wait(tempty(acc), aph ^ 1u, abort_flag, lim)) {
+                if (!wait(tempty(acc), aph ^ 1u)) {
                     fail();
                     break;
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * kBN);
                 int mb_, nt_, ks;
-                tile_coords(a, tile, mb_, nt_, ks);
-                const int kb_lo = ks * KB / a.k_splits, kb_hi = (ks + 1) * KB / a.k_splits;
-                for (int kb = kb_lo; kb < kb_hi; ++kb, ++it) {
+                coords(tile, mb_, nt_, ks);
+                const int kb_lo = ks * KB / a.k_splits, nkb = (ks + 1) * KB / a.k_splits - kb_lo;
+                const int rot = k_rotation(nt_, nkb);
+                for (int j = 0; j < nkb; ++j, ++it) {
+                    const int kb = kb_lo + (j + rot) % nkb;
                     const int sa = it % kA, sb = it % kB;
-                    if (!mbar_wait(a_full(sa), (uint32_t)(it / kA) & 1u, abort_flag, lim) ||
-                        !mbar_wait(b_full(sb), (uint32_t)(it / kB) & 1u, abort_flag, lim)) {
+                    if (!wait(a_full(sa), (uint32_t)(it / kA) & 1u) ||
+                        !wait(b_full(sb), (uint32_t)(it / kB) & 1u)) {
                         fail();
                         ok = false;
                         break;
@@ -713,17 +865,32 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
                     const uint64_t ad = sdesc_sw128(a_stage(sa));
                     const uint64_t bd = sdesc_sw128(b_stage(sb));
 #pragma unroll
-                    for (int k = 0; k < kBK / 16; ++k)  // 16 elements = 32 bytes per MMA
-                        umma_f16kind(d_tmem, ad + 2ull * k, bd + 2ull * k, idesc<kF16>(),
-                                     (kb != kb_lo) || (k != 0));
-                    umma_commit(a_empty(sa));
-                    umma_commit(b_empty(sb));
+                    for (int k = 0; k < kBK / 16; ++k) {  // 16 elements = 32 bytes per MMA
+                        if constexpr (kPair)
+                            umma_f16kind_pair(d_tmem, ad + 2ull * k, bd + 2ull * k,
+                                              idesc<kF16, 2 * kBM>(), (j != 0) || (k != 0));
+                        else
+                            umma_f16kind(d_tmem, ad + 2ull * k, bd + 2ull * k, idesc<kF16>(),
+                                         (j != 0) || (k != 0));
+                    }
+                    if constexpr (kPair) {  // frees the stage in both CTAs
+                        umma_commit_pair(a_empty(sa));
+                        umma_commit_pair(b_empty(sb));
+                    } else {
+                        umma_commit(a_empty(sa));
+                        umma_commit(b_empty(sb));
+                    }
                 }
-                if (ok) umma_commit(tfull(acc));
+                if (ok) {
+                    if constexpr (kPair)
+                        umma_commit_pair(tfull(acc));
+                    else
+                        umma_commit(tfull(acc));
+                }
             }
         }
     } else if (warp >= kWarpTma) {
-        // warps 14, 15: idle
+        // warp 15 (and 14 with a gathered A): idle
     } else if (warp < kWarpEpi) {
         setmaxnreg_inc<kRegsProd>();
         if (kASrc == kASrcGatherBucket) {
@@ -734,9 +901,9 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
             int it = 0;
             bool ok = true;
             BucketRows R0, R1;
-            for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+            for (int tile = item0; tile < total && ok; tile += istep) {
                 int mb, nt, ks;
-                tile_coords(a, tile, mb, nt, ks);
+                coords(tile, mb, nt, ks);
                 // this split's buckets (the host splits K on bucket boundaries)
                 const int b_lo = ks * nbk / a.k_splits, b_hi = (ks + 1) * nbk / a.k_splits;
                 const int64_t t = (int64_t)mb * kBM + pw * kRowsPerProd + (lane & (kRowsPerProd - 1));
@@ -789,9 +956,9 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
             uint32_t* rows_s = reinterpret_cast<uint32_t*>(smem + L::kOffRows);
             int it = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+            for (int tile = item0; tile < total && ok; tile += istep) {
                 int mb, nt, ks;
-                tile_coords(a, tile, mb, nt, ks);
+                coords(tile, mb, nt, ks);
                 const int kb_lo = ks * KB / a.k_splits, kb_hi = (ks + 1) * KB / a.k_splits;
                 {   // hash: lanes l, l + 16 <-> token, every bucket, into the row-index table
                     const int m = pw * kRowsPerProd + (lane & (kRowsPerProd - 1));
@@ -851,13 +1018,20 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
         const int q = warp & 3;  // TMEM lane quadrant this warp may read
         const int m = q * 32 + lane;
         int tc = 0;
-        if (kMode == kEpiForward && blockIdx.x < total) prefetch_hidden(a, blockIdx.x, m);
-        for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++tc) {
+        if (kMode == kEpiForward && item0 < total) {
             int mb, nt, ks;
-            tile_coords(a, tile, mb, nt, ks);
+            coords(item0, mb, nt, ks);
+            if (mb < a.m_blocks) prefetch_hidden(a, mb, nt, m);
+        }
+        for (int tile = item0; tile < total; tile += istep, ++tc) {
+            int mb, nt, ks;
+            coords(tile, mb, nt, ks);
             // the next tile's hidden slices travel to L2 while this one is finished
-            if (kMode == kEpiForward && tile + (int)gridDim.x < total)
-                prefetch_hidden(a, tile + gridDim.x, m);
+            if (kMode == kEpiForward && tile + istep < total) {
+                int mb2, nt2, ks2;
+                coords(tile + istep, mb2, nt2, ks2);
+                if (mb2 < a.m_blocks) prefetch_hidden(a, mb2, nt2, m);
+            }
             const int acc = tc & 1;
             const uint32_t aph = (uint32_t)(tc >> 1) & 1u;
             int full_ok = 1;
@@ -871,8 +1045,9 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
             const uint32_t taddr = tmem_base + (uint32_t)(acc * kBN) + ((uint32_t)(q * 32) << 16);
             const int64_t t = (int64_t)mb * kBM + m;
             const int n0 = (a.n_tile_begin + nt) * kBN;
-            int holds_sum = 1;
-            if (kMode == kEpiForward && a.k_splits > 1) {
+            // an odd pair CTA past the last M block has no rows to write
+            int holds_sum = mb < a.m_blocks ? 1 : 0;
+            if (holds_sum && kMode == kEpiForward && a.k_splits > 1) {
                 holds_sum = split_k_quadrant(a, mb, nt, ks, q, lane, taddr, abort_flag, lim);
                 if (holds_sum < 0) {
                     if (lane == 0) fail();
@@ -1056,7 +1231,12 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(tempty(acc));
+            if (lane == 0) {
+                if constexpr (kPair)  // the issuer's barrier counts the epilogue warps of both CTAs
+                    mbar_arrive_cluster(map_rank(tempty(acc), 0));
+                else
+                    mbar_arrive(tempty(acc));
+            }
         }
     }
 
@@ -1069,9 +1249,14 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
         }
         __syncthreads();
     }
+    // a pair leaves together: no arrival or multicast may target a CTA that exited
+    if constexpr (kPair) cluster_sync();
     if (warp == kWarpMma) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, kTmemCols);
+        if constexpr (kPair)
+            tmem_dealloc_pair(tmem_base, kTmemCols);
+        else
+            tmem_dealloc(tmem_base, kTmemCols);
     }
 }
 
@@ -1088,6 +1273,30 @@ cudaError_t launch(const MmaArgs& a, const CUtensorMap& tmA, const CUtensorMap& 
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
         if (e != cudaSuccess) return e;
         attr_set = true;
+    }
+    if (kASrc == kASrcTmaPair) {
+        // clusters of two; no more pairs than can be resident at once, since
+        // the forward epilogue's tiles wait on tiles of other CTAs
+        const int units = (a.m_blocks + 1) / 2 * a.n_tiles * a.k_splits;
+        if (units == 0) return cudaSuccess;
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = kSmem;
+        cfg.stream = s;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        cfg.gridDim = dim3(2 * (device_sm_count() / 2));
+        int resident = 0;
+        cudaError_t e = cudaOccupancyMaxActiveClusters(&resident, kern, &cfg);
+        if (e != cudaSuccess) return e;
+        if (resident < 1) return cudaErrorLaunchOutOfResources;
+        cfg.gridDim = dim3(2 * std::min(units, std::min(resident, device_sm_count() / 2)));
+        return cudaLaunchKernelEx(&cfg, kern, tmA, tmB, a);
     }
     const int total = a.m_blocks * a.n_tiles * a.k_splits;
     if (total == 0) return cudaSuccess;
@@ -1135,6 +1344,18 @@ cudaError_t launch_project_split(const MmaArgs& a, bool f16, const CUtensorMap& 
                                  const CUtensorMap& tmB, cudaStream_t s) {
     if (f16) return launch<kASrcTma, true, kEpiStoreKv>(a, tmA, tmB, s);
     return launch<kASrcTma, false, kEpiStoreKv>(a, tmA, tmB, s);
+}
+
+cudaError_t launch_project_split_pair(const MmaArgs& a, bool f16, const CUtensorMap& tmA,
+                                      const CUtensorMap& tmB_half, cudaStream_t s) {
+    if (f16) return launch<kASrcTmaPair, true, kEpiStoreKv>(a, tmA, tmB_half, s);
+    return launch<kASrcTmaPair, false, kEpiStoreKv>(a, tmA, tmB_half, s);
+}
+
+cudaError_t launch_forward_tma_pair(const MmaArgs& a, bool f16, const CUtensorMap& tmA,
+                                   const CUtensorMap& tmB_half, cudaStream_t s) {
+    if (f16) return launch<kASrcTmaPair, true, kEpiForward>(a, tmA, tmB_half, s);
+    return launch<kASrcTmaPair, false, kEpiForward>(a, tmA, tmB_half, s);
 }
 
 cudaError_t launch_forward_tma(const MmaArgs& a, bool f16, const CUtensorMap& tmA,
