@@ -44,6 +44,8 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="mine", choices=["mine", "reference"])
     ap.add_argument("--no-extras", action="store_true", help="skip decode / gather / project lines")
+    ap.add_argument("--no-host", action="store_true",
+                    help="skip the host-table line (pins 17 GB of host memory)")
     ap.add_argument("--cpu-sample", type=int, default=256,
                     help="oracle tokens for cpu_baseline (0: skip)")
     ap.add_argument("--small", action="store_true",
@@ -417,6 +419,11 @@ def main():
                                sptr, stream))
         except Exception as exc:  # extras never hide the main line
             line["extras_error"] = repr(exc)
+        if not args.no_host:
+            try:
+                line["host_table"] = host_pipeline(model, wq, wk, tmap, peaks, dev, stream)
+            except Exception as exc:
+                line["host_table"] = {"error": repr(exc)}
     if dist.rank == 0 and dist.world == 1 and args.cpu_sample > 0:
         line["cpu_baseline"] = cpu_baseline(args, w, W, wq, wk, win_h[0], hid_h[0])
     model.close()
@@ -463,7 +470,19 @@ def extras(args, w, W, wq, wk, tmap, win0, d_win0, model, peaks, dev, sptr, stre
                       "tc_frac": fl / ms_p / 1e9 / peaks["bf16"]}
     out["project_windows"] = {"ms": ms_pw, "tflops": fl / ms_pw / 1e9,
                               "tc_frac": fl / ms_pw / 1e9 / peaks["bf16"]}
-    del d_rows, d_emb, d_kv
+    # hidden-independent pre-pass: hash + gather + projection as soon as the
+    # tokens are known (kv fp32 to HBM, off the layer's critical path), then at
+    # the layer entry only the gate runs on the stored kv
+    d_h = torch.from_numpy(synth.normal_bf16((T, w.hc, w.d), 1.0, w.seed, 4242).view(np.int16)).to(dev)
+    for _ in range(3):
+        eg.engram_gate(ctx, 0, d_kv, d_win0, T, d_h, None, sptr)
+    ms_g = timed(lambda i: eg.engram_gate(ctx, 0, d_kv, d_win0, T, d_h, None, sptr), 50, stream)
+    gate_bytes = T * (w.N * 4 + 2 * w.hc * w.d * 2)
+    out["prepass"] = {"tokens": T, "prepass_ms": ms_pw, "layer_entry_gate_ms": ms_g,
+                      "kv_bytes": T * w.N * 4,
+                      "gate_GB_per_s": gate_bytes / ms_g / 1e6,
+                      "gate_frac": gate_bytes / ms_g / 1e6 / peaks["hbm"]}
+    del d_rows, d_emb, d_kv, d_h
 
     # decode: 256 sessions x 1 token per step, 384M-row table resident in HBM
     wd = synth.WORKLOADS["decode_256"]
@@ -495,6 +514,19 @@ def extras(args, w, W, wq, wk, tmap, win0, d_win0, model, peaks, dev, sptr, stre
             "sessions": S, "steps": wd.steps, "table_rows": dm.rows(0),
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm"], "unit": "GB/s",
                          "frac": gbs / peaks["hbm"], "bytes_per_step": bytes_step}}
+    # the decode step as a pre-pass (as soon as the step's tokens are known)
+    # plus the gate at the layer entry
+    d_kvd = torch.empty((S, w.N), dtype=torch.float32, device=dev)
+    for i in range(3):
+        eg.engram_project_windows(dm.ctx, 0, d_wins[i], S, d_kvd, sptr)
+        eg.engram_gate(dm.ctx, 0, d_kvd, d_wins[i], S, d_h, None, sptr)
+    ms_pwd = timed(lambda i: eg.engram_project_windows(dm.ctx, 0, d_wins[i % wd.steps], S, d_kvd,
+                                                       sptr), wd.steps, stream)
+    ms_gd = timed(lambda i: eg.engram_gate(dm.ctx, 0, d_kvd, d_wins[i % wd.steps], S, d_h, None,
+                                           sptr), wd.steps, stream)
+    eg.engram_sync(dm.ctx, sptr)
+    out["decode_prepass"] = {"sessions": S, "prepass_ms": ms_pwd, "layer_entry_gate_ms": ms_gd}
+    del d_kvd
 
     # gather: unfused engram_gather_dequant over the 384M-row table, 50,032 tokens
     Tg = 50_032
@@ -516,6 +548,109 @@ def extras(args, w, W, wq, wk, tmap, win0, d_win0, model, peaks, dev, sptr, stre
         eg.engram_session_destroy(s)
     dm.close()
     return out
+
+
+def host_pipeline(model, wq, wk, tmap, peaks, dev, stream):
+    """The host-table workload: 8 sessions x 1,024 tokens per step, the MXFP8
+    table (64M rows, 17 GB) in pinned host memory read through UVA.  Reports the
+    host link (a pinned host-to-device copy), the row gather over it, the GEMM
+    on the staged rows, and the staged forward run serially or pipelined: the
+    rows of step i + 1 staged on a side stream while step i's GEMM runs."""
+    import dataclasses
+
+    import torch
+
+    import engram_gram_conditional_gb300 as eg
+    import synth
+    from engram_gram_conditional_gb300.layer import EngramLayerSet
+
+    with open("/proc/meminfo") as f:
+        info = {ln.split(":")[0]: int(ln.split()[1]) * 1024 for ln in f if ":" in ln}
+    if info.get("MemAvailable", 0) < 48 * 2**30:
+        return {"skipped": "less than 48 GB of host memory available for the pinned table"}
+    wh = dataclasses.replace(synth.WORKLOADS["host_table_8x1024"], bucket_bases=[2_666_666])
+    hm = EngramLayerSet.from_workload(wh, tmap, device=dev)
+    try:
+        hm.bind(0, wh.table_seeds[0], model.tensors[0]["wkv"], wq, wk, host_table=True)
+        T = wh.sessions * wh.tokens_per_session
+        nbatch = 4
+        wins, hids = [], []
+        for b in range(nbatch):
+            parts = []
+            for i in range(wh.sessions):
+                s = eg.engram_session_create(hm.ctx)
+                parts.append(eg.engram_session_append(
+                    s, synth.session_tokens(wh, b * wh.sessions + i, wh.tokens_per_session)))
+                eg.engram_session_destroy(s)
+            wins.append(torch.from_numpy(np.concatenate(parts).view(np.int32)).to(dev))
+            hids.append(torch.from_numpy(
+                synth.normal_bf16((T, wh.hc, wh.d), 1.0, wh.seed, 9000 + b).view(np.int16)).to(dev))
+        wsb = eg.engram_forward_staged_workspace_bytes(hm.ctx, T)
+        ws = [torch.empty(wsb, dtype=torch.uint8, device=dev) for _ in range(2)]
+        sptr = stream.cuda_stream
+        side = torch.cuda.Stream(device=dev)
+
+        # the host link: a pinned 1 GiB host-to-device copy
+        hbuf = torch.empty(1 << 30, dtype=torch.uint8, pin_memory=True)
+        dbuf = torch.empty(1 << 30, dtype=torch.uint8, device=dev)
+        with torch.cuda.stream(stream):
+            for _ in range(2):
+                dbuf.copy_(hbuf, non_blocking=True)
+            ms_h2d = timed(lambda i: dbuf.copy_(hbuf, non_blocking=True), 5, stream)
+        del hbuf, dbuf
+
+        def stage(i, st):
+            eg.engram_stage_rows(hm.ctx, 0, wins[i % nbatch], T, ws[i % 2], st)
+
+        def gemm(i):
+            eg.engram_forward_staged_rows(hm.ctx, 0, wins[i % nbatch], T, hids[i % nbatch],
+                                          ws[i % 2], None, sptr)
+
+        for i in range(3):
+            eg.engram_forward_staged(hm.ctx, 0, wins[i % nbatch], T, hids[i % nbatch], ws[0], None,
+                                     sptr)
+        ms_stage = timed(lambda i: stage(0, sptr), 10, stream)
+        ms_gemm = timed(lambda i: gemm(0), 10, stream)
+        steps = 12
+        ms_serial = timed(lambda i: eg.engram_forward_staged(
+            hm.ctx, 0, wins[i % nbatch], T, hids[i % nbatch], ws[0], None, sptr), steps, stream)
+
+        # pipelined: stage(i + 1) on the side stream overlaps gemm(i) on the main one
+        staged = [torch.cuda.Event() for _ in range(2)]
+        done = [torch.cuda.Event() for _ in range(2)]
+
+        def pipelined():
+            torch.cuda.synchronize()
+            ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            ev0.record(stream)
+            side.wait_event(ev0)
+            stage(0, side.cuda_stream)
+            staged[0].record(side)
+            for i in range(steps):
+                if i + 1 < steps:
+                    if i >= 1:
+                        side.wait_event(done[(i + 1) % 2])  # step i - 1 used that workspace
+                    stage(i + 1, side.cuda_stream)
+                    staged[(i + 1) % 2].record(side)
+                stream.wait_event(staged[i % 2])
+                gemm(i)
+                done[i % 2].record(stream)
+            ev1.record(stream)
+            torch.cuda.synchronize()
+            return ev0.elapsed_time(ev1) / steps
+
+        pipelined()
+        ms_pipe = pipelined()
+        eg.engram_sync(hm.ctx, sptr)
+        link_bytes = T * wh.nb * 264  # codes and scales read over the link per step
+        return {"tokens_per_step": T, "table_rows": hm.rows(0), "table": "pinned host, UVA",
+                "h2d_GB_per_s": (1 << 30) / ms_h2d / 1e6,
+                "stage_ms": ms_stage, "stage_link_GB_per_s": link_bytes / ms_stage / 1e6,
+                "gemm_ms": ms_gemm, "serial_ms_per_step": ms_serial,
+                "pipelined_ms_per_step": ms_pipe,
+                "pipelined_tokens_per_s": T / (ms_pipe / 1000.0)}
+    finally:
+        hm.close()
 
 
 def cpu_baseline(args, w, W, wq, wk, win, hidden):

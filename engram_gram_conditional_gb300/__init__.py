@@ -34,7 +34,8 @@ EXPORTS = (
     "engram_session_destroy", "engram_session_append", "engram_batch_append",
     "engram_workspace_bytes", "engram_hash", "engram_gather_dequant", "engram_project",
     "engram_gate", "engram_forward", "engram_forward_noalloc", "engram_forward_staged",
-    "engram_forward_staged_workspace_bytes", "engram_project_windows",
+    "engram_forward_staged_workspace_bytes", "engram_stage_rows", "engram_forward_staged_rows",
+    "engram_project_windows",
     "engram_sync", "engram_ctx_set_wait_limit", "engram_debug_starve_operand",
     "engram_last_error",
 )
@@ -108,6 +109,8 @@ def lib() -> C.CDLL:
             "engram_project_windows": [vp, C.c_int, vp, i64, vp, vp],
             "engram_forward_noalloc": [vp, C.c_int, vp, i64, vp, vp, vp],
             "engram_forward_staged": [vp, C.c_int, vp, i64, vp, vp, vp, vp],
+            "engram_stage_rows": [vp, C.c_int, vp, i64, vp, vp],
+            "engram_forward_staged_rows": [vp, C.c_int, vp, i64, vp, vp, vp, vp],
             "engram_sync": [vp, vp],
             "engram_ctx_set_wait_limit": [vp, i64],
             "engram_debug_starve_operand": [vp, C.c_int],
@@ -292,6 +295,17 @@ def engram_forward_staged(ctx, layer, d_windows, T, d_hidden, d_workspace, d_gat
                           stream=None):
     _check(lib().engram_forward_staged(ctx, layer, _ptr(d_windows), T, _ptr(d_hidden),
                                        _ptr(d_workspace), _ptr(d_gates), _stream(stream)))
+
+
+def engram_stage_rows(ctx, layer, d_windows, T, d_workspace, stream=None):
+    _check(lib().engram_stage_rows(ctx, layer, _ptr(d_windows), T, _ptr(d_workspace),
+                                   _stream(stream)))
+
+
+def engram_forward_staged_rows(ctx, layer, d_windows, T, d_hidden, d_workspace, d_gates=None,
+                               stream=None):
+    _check(lib().engram_forward_staged_rows(ctx, layer, _ptr(d_windows), T, _ptr(d_hidden),
+                                            _ptr(d_workspace), _ptr(d_gates), _stream(stream)))
 
 
 def engram_forward_noalloc(ctx, layer, d_windows, T, d_hidden, d_gates=None, stream=None):

@@ -794,9 +794,27 @@ size_t engram_forward_staged_workspace_bytes(const engram_ctx* ctx, int64_t T) {
     return e + forward_workspace_bytes(ctx, T, 8);
 }
 
-engram_status engram_forward_staged(const engram_ctx* ctx, int layer, const uint32_t* d_windows,
-                                    int64_t T, uint16_t* d_hidden, void* d_workspace,
-                                    float* d_gates, void* stream) {
+engram_status engram_stage_rows(const engram_ctx* ctx, int layer, const uint32_t* d_windows,
+                                int64_t T, void* d_workspace, void* stream) {
+    engram_status st = check_layer(ctx, layer, true);
+    if (st || (st = check_T(T))) return st;
+    if (T == 0) return ok();
+    if (!d_windows || !d_workspace || !aligned16(d_windows) || !aligned16(d_workspace))
+        return fail(ENGRAM_EINVAL, "windows / workspace (16-byte aligned)");
+    const LayerState& L = ctx->layers[layer];
+    // gather and dequantise every (token, bucket) row once into e
+    cudaError_t e = launch_gather_stage(hash_params(ctx, layer),
+                                        reinterpret_cast<const uint4*>(d_windows), T,
+                                        (int)ctx->desc.row_dim, L.w.table, L.w.scales, L.rows,
+                                        L.f16, L.a_exp_shift, static_cast<uint16_t*>(d_workspace),
+                                        ctx->d_err, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "staged gather launch");
+    return ok();
+}
+
+engram_status engram_forward_staged_rows(const engram_ctx* ctx, int layer,
+                                         const uint32_t* d_windows, int64_t T, uint16_t* d_hidden,
+                                         void* d_workspace, float* d_gates, void* stream) {
     engram_status st = check_layer(ctx, layer, true);
     if (st || (st = check_T(T))) return st;
     if (T == 0) return ok();
@@ -818,14 +836,9 @@ engram_status engram_forward_staged(const engram_ctx* ctx, int layer, const uint
     a.n_tile_begin = 0;
     a.n_tiles = ctx->N / kBN;
     cudaStream_t s = (cudaStream_t)stream;
-    // 1: gather and dequantise every (token, bucket) row once into e
-    cudaError_t e = launch_gather_stage(hash_params(ctx, layer), a.windows, T,
-                                        (int)ctx->desc.row_dim, L.w.table, L.w.scales, L.rows,
-                                        L.f16, L.a_exp_shift, e_scratch, ctx->d_err, s);
-    if (e != cudaSuccess) return cuda_fail(e, "staged gather launch");
-    // 2: the forward GEMM reading e through TMA
+    // the forward GEMM reading e through TMA
     CUtensorMap tmA;
-    e = make_tma_16bit(&tmA, e_scratch, (uint64_t)T, (uint64_t)ctx->K, kBM, L.f16);
+    cudaError_t e = make_tma_16bit(&tmA, e_scratch, (uint64_t)T, (uint64_t)ctx->K, kBM, L.f16);
     if (e != cudaSuccess) return cuda_fail(e, "e tensor map");
     const int splits = staged_splits(ctx, T);
     if (splits > 1) {
@@ -849,6 +862,21 @@ engram_status engram_forward_staged(const engram_ctx* ctx, int layer, const uint
                      : launch_forward_tma(a, L.f16, tmA, L.f16 ? L.tm_wkv_f16 : L.tm_wkv, s);
     if (e != cudaSuccess) return cuda_fail(e, "staged forward launch");
     return ok();
+}
+
+engram_status engram_forward_staged(const engram_ctx* ctx, int layer, const uint32_t* d_windows,
+                                    int64_t T, uint16_t* d_hidden, void* d_workspace,
+                                    float* d_gates, void* stream) {
+    engram_status st = check_layer(ctx, layer, true);
+    if (st || (st = check_T(T))) return st;
+    if (T == 0) return ok();
+    if (!d_windows || !d_hidden || !d_workspace || !aligned16(d_windows) || !aligned16(d_hidden) ||
+        !aligned16(d_workspace))
+        return fail(ENGRAM_EINVAL, "windows / hidden / workspace (16-byte aligned)");
+    st = engram_stage_rows(ctx, layer, d_windows, T, d_workspace, stream);
+    if (st) return st;
+    return engram_forward_staged_rows(ctx, layer, d_windows, T, d_hidden, d_workspace, d_gates,
+                                      stream);
 }
 
 engram_status engram_project_windows(const engram_ctx* ctx, int layer, const uint32_t* d_windows,

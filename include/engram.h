@@ -244,6 +244,23 @@ engram_status engram_forward_staged(const engram_ctx* ctx, int layer, const uint
                                     int64_t T, uint16_t* d_hidden, void* d_workspace,
                                     float* d_gates, void* stream);
 
+/* The two steps of engram_forward_staged as separate calls, so that a caller
+ * can gather the rows of the next step while the current step's GEMM runs:
+ * the host-table pipeline (the vLLM page, CPU offload: rows read from pinned
+ * host memory through UVA cross the host link, while the GEMM reads HBM).
+ * engram_stage_rows hashes the windows and gathers and dequantises the rows
+ * into the operand matrix e at the start of d_workspace
+ * (engram_forward_staged_workspace_bytes(ctx, T) bytes, 16-byte aligned).
+ * engram_forward_staged_rows then runs the GEMM and the gate on that
+ * workspace; it must see the same layer, windows and T, ordered after the
+ * staging (same stream, or an event).  Keep one workspace per step in flight:
+ * staging step i+1 into the workspace of step i races with step i's GEMM. */
+engram_status engram_stage_rows(const engram_ctx* ctx, int layer, const uint32_t* d_windows,
+                                int64_t T, void* d_workspace, void* stream);
+engram_status engram_forward_staged_rows(const engram_ctx* ctx, int layer,
+                                         const uint32_t* d_windows, int64_t T, uint16_t* d_hidden,
+                                         void* d_workspace, float* d_gates, void* stream);
+
 /* engram_forward for callers that cannot allocate device memory.  The pages
  * have no counterpart: this is a deployment variant.  A serving engine that
  * reserves the GPU's memory for its own pools, or a plugin host that forbids

@@ -289,6 +289,38 @@ def test_small_batches_split_k(prefill, entry, T):
     assert np.array_equal(h, h2) and np.array_equal(gates, g2)
 
 
+@pytest.mark.parametrize("T", [77, 256, 2048])
+def test_staged_in_two_calls_matches_one_call(prefill, T):
+    # engram_stage_rows + engram_forward_staged_rows is engram_forward_staged
+    # split in two: the same kernels on the same inputs, bit for bit; the two
+    # steps of two batches are interleaved on two streams and two workspaces
+    win, _, _ = prefill_windows(prefill, 1, T, spans=[(T // 3, 5)])
+    win2, _, _ = prefill_windows(prefill, 2, T // 2 + 1)
+    win2 = win2[:T]
+    hidden = synth.hidden_bf16(prefill.w, T)
+    ctx = prefill.model.ctx
+    ref1, g1 = run_forward(prefill, win, hidden, staged=True)
+    ref2, g2 = run_forward(prefill, win2, hidden, staged=True)
+    wsb = eg.engram_forward_staged_workspace_bytes(ctx, T)
+    ws = [torch.empty(wsb, dtype=torch.uint8, device="cuda") for _ in range(2)]
+    d_w = [to_dev(win), to_dev(win2)]
+    d_h = [to_dev(hidden), to_dev(hidden)]
+    d_g = [torch.full((T, prefill.w.hc), float("nan"), device="cuda") for _ in range(2)]
+    main, side = torch.cuda.current_stream(), torch.cuda.Stream()
+    staged = [torch.cuda.Event() for _ in range(2)]
+    side.wait_stream(main)
+    for i in range(2):
+        eg.engram_stage_rows(ctx, 0, d_w[i], T, ws[i], side.cuda_stream)
+        staged[i].record(side)
+    for i in range(2):
+        main.wait_event(staged[i])
+        eg.engram_forward_staged_rows(ctx, 0, d_w[i], T, d_h[i], ws[i], d_g[i], main.cuda_stream)
+    eg.engram_sync(ctx)
+    assert np.array_equal(from_dev(d_h[0], np.uint16), ref1)
+    assert np.array_equal(from_dev(d_h[1], np.uint16), ref2)
+    assert np.array_equal(d_g[0].cpu().numpy(), g1) and np.array_equal(d_g[1].cpu().numpy(), g2)
+
+
 def test_forward_edge_cases(tiny):
     ctx = tiny.model.ctx
     eg.engram_forward(ctx, 0, None, 0, None, None)  # T = 0

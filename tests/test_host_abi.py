@@ -212,6 +212,9 @@ def test_device_calls_validate_before_launch():
         (eg.engram_gate, (0, 16, 16, 4, 16)),
         (eg.engram_forward, (0, 16, 4, 16, 16)),
         (eg.engram_project_windows, (0, 16, 4, 16)),
+        (eg.engram_forward_staged, (0, 16, 4, 16, 16)),
+        (eg.engram_stage_rows, (0, 16, 4, 16)),
+        (eg.engram_forward_staged_rows, (0, 16, 4, 16, 16)),
     ]:
         with pytest.raises(eg.EngramError) as e:
             fn(ctx, *args)
@@ -226,7 +229,8 @@ def test_device_calls_validate_before_launch():
         eg.engram_hash(ctx, 0, 8, 1, 16)  # misaligned windows
     assert e.value.status == eg.EINVAL
     eg.engram_hash(ctx, 0, None, 0, None)  # T = 0 is a no-op
-    # gate sums [T][hc][d/256][3] fp32 and one counter per 128-token block, 256-byte aligned
+    # gate sums [T][hc][d/256][3] fp32, gates [T][hc] and the counters (two per
+    # 128-token block and TMEM quadrant), each 256-byte aligned
     assert eg.engram_workspace_bytes(ctx, 64) == 64 * 2 * 1 * 3 * 4 + 64 * 2 * 4 + 256
     assert eg.engram_workspace_bytes(ctx, 0) == 0
     eg.engram_ctx_destroy(ctx)
