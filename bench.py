@@ -547,6 +547,32 @@ def extras(args, w, W, wq, wk, tmap, win0, d_win0, model, peaks, dev, sptr, stre
     for s in sess + [sg]:
         eg.engram_session_destroy(s)
     dm.close()
+
+    # the BF16-table variant (rows stored dequantised, 512 B, no scales) at the
+    # prefill size: the staged forward and the standalone gather
+    bm = EngramLayerSet.from_workload(w, tmap, device=dev)
+    try:
+        bm.bind(0, w.table_seeds[0], model.tensors[0]["wkv"], wq, wk, flags=eg.BIND_TABLE_BF16)
+        d_hb = torch.from_numpy(synth.normal_bf16((T, w.hc, w.d), 1.0, w.seed, 5151).view(np.int16)).to(dev)
+        d_wsb = torch.empty(eg.engram_forward_staged_workspace_bytes(bm.ctx, T), dtype=torch.uint8,
+                            device=dev)
+        for _ in range(3):
+            eg.engram_forward_staged(bm.ctx, 0, d_win0, T, d_hb, d_wsb, None, sptr)
+        ms_b = timed(lambda i: eg.engram_forward_staged(bm.ctx, 0, d_win0, T, d_hb, d_wsb, None,
+                                                        sptr), 20, stream)
+        d_rb = torch.empty((T, w.nb), dtype=torch.int32, device=dev)
+        d_eb = torch.empty((T, w.K), dtype=torch.int16, device=dev)
+        eg.engram_hash(bm.ctx, 0, d_win0, T, d_rb, sptr)
+        for _ in range(3):
+            eg.engram_gather_dequant(bm.ctx, 0, d_rb, T, d_eb, sptr)
+        ms_bg = timed(lambda i: eg.engram_gather_dequant(bm.ctx, 0, d_rb, T, d_eb, sptr), 20, stream)
+        eg.engram_sync(bm.ctx, sptr)
+        gb_b = T * (w.nb * 4 + w.nb * w.row_dim * 2 + w.K * 2)
+        out["bf16_table"] = {"tokens": T, "table_rows": bm.rows(0), "row_bytes": w.row_dim * 2,
+                             "staged_ms": ms_b, "staged_tflops": fl / ms_b / 1e9,
+                             "gather_ms": ms_bg, "gather_GB_per_s": gb_b / ms_bg / 1e6}
+    finally:
+        bm.close()
     return out
 
 

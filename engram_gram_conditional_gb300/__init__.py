@@ -29,7 +29,7 @@ OK, EINVAL, ENOMEM, ECUDA, ESTATE, ETIMEOUT, EUNSUPPORTED, EBOUNDS = range(8)
 EXPORTS = (
     "engram_ctx_create", "engram_ctx_destroy", "engram_layer_params",
     "engram_layer_set_multipliers", "engram_layer_bind", "engram_layer_info",
-    "engram_table_fill",
+    "engram_table_fill", "engram_table_fill_bf16",
     "engram_session_create", "engram_session_fork", "engram_session_reset",
     "engram_session_destroy", "engram_session_append", "engram_batch_append",
     "engram_workspace_bytes", "engram_hash", "engram_gather_dequant", "engram_project",
@@ -58,6 +58,7 @@ class CtxDesc(C.Structure):
 
 
 BIND_BF16_OPERANDS = 1
+BIND_TABLE_BF16 = 2
 
 
 class LayerWeights(C.Structure):
@@ -71,7 +72,7 @@ class LayerInfo(C.Structure):
     _fields_ = [
         ("rows", C.c_uint64), ("bound", C.c_int32), ("fp16_operands", C.c_int32),
         ("scale_min", C.c_uint32), ("scale_max", C.c_uint32), ("wkv_exp", C.c_int32),
-        ("a_exp_shift", C.c_int32), ("bucket_gather", C.c_int32),
+        ("a_exp_shift", C.c_int32), ("bucket_gather", C.c_int32), ("table_bf16", C.c_int32),
     ]
 
 
@@ -95,6 +96,7 @@ def lib() -> C.CDLL:
             "engram_layer_bind": [vp, C.c_int, C.POINTER(LayerWeights)],
             "engram_layer_info": [vp, C.c_int, C.POINTER(LayerInfo)],
             "engram_table_fill": [vp, C.c_uint64, vp, vp, C.c_uint64, C.c_uint64, vp],
+            "engram_table_fill_bf16": [vp, C.c_uint64, vp, C.c_uint64, C.c_uint64, vp],
             "engram_session_create": [vp, C.POINTER(vp)],
             "engram_session_fork": [vp, C.POINTER(vp)],
             "engram_session_reset": [vp],
@@ -211,6 +213,11 @@ def engram_layer_info(ctx, layer: int) -> dict:
 def engram_table_fill(ctx, seed: int, data, scale, row_begin: int, row_end: int, stream=None):
     _check(lib().engram_table_fill(ctx, seed, _ptr(data), _ptr(scale), row_begin, row_end,
                                    _stream(stream)))
+
+
+def engram_table_fill_bf16(ctx, seed: int, data, row_begin: int, row_end: int, stream=None):
+    _check(lib().engram_table_fill_bf16(ctx, seed, _ptr(data), row_begin, row_end,
+                                        _stream(stream)))
 
 
 # ---- sessions -------------------------------------------------------------------------

@@ -136,6 +136,7 @@ struct LayerState {
     int a_exp_shift = 0;
     uint32_t scale_min = 0, scale_max = 0;
     bool bucket_gather = false;    // whole 256-wide rows gathered once per tile and bucket
+    bool table_bf16 = false;       // BF16 rows without scales (ENGRAM_BIND_TABLE_BF16)
 };
 
 struct engram_ctx {
@@ -320,6 +321,8 @@ engram_status forward_fused(const engram_ctx* ctx, int layer, const uint32_t* d_
         !aligned16(d_workspace))
         return fail(ENGRAM_EINVAL, "windows / hidden / workspace (16-byte aligned)");
     const LayerState& L = ctx->layers[layer];
+    if (L.table_bf16)
+        return fail(ENGRAM_EUNSUPPORTED, "BF16-table layers run through engram_forward_staged");
     MmaArgs a = mma_args(ctx, layer, T);
     a.windows = reinterpret_cast<const uint4*>(d_windows);
     a.hidden = d_hidden;
@@ -452,12 +455,15 @@ engram_status engram_layer_set_multipliers(engram_ctx* ctx, int layer, const uin
 engram_status engram_layer_bind(engram_ctx* ctx, int layer, const engram_layer_weights* w) {
     engram_status st = check_layer(ctx, layer, false);
     if (st) return st;
-    if (!w || !w->table || !w->scales || !w->wkv || !w->wq || !w->wk)
+    const bool tbf16 = w && (w->flags & ENGRAM_BIND_TABLE_BF16);
+    if (!w || !w->table || (!tbf16 && !w->scales) || !w->wkv || !w->wq || !w->wk)
         return fail(ENGRAM_EINVAL, "null weight pointer");
+    if (w->flags & ~(ENGRAM_BIND_BF16_OPERANDS | ENGRAM_BIND_TABLE_BF16))
+        return fail(ENGRAM_EINVAL, "unknown bind flag");
     LayerState& L = ctx->layers[layer];
     if (w->rows != L.rows) return fail(ENGRAM_EINVAL, "table rows differ from the layer's row count");
-    if (!aligned16(w->table) || !aligned16(w->scales) || !aligned16(w->wkv) || !aligned16(w->wq) ||
-        !aligned16(w->wk))
+    if (!aligned16(w->table) || (!tbf16 && !aligned16(w->scales)) || !aligned16(w->wkv) ||
+        !aligned16(w->wq) || !aligned16(w->wk))
         return fail(ENGRAM_EINVAL, "weights must be 16-byte aligned");
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -467,7 +473,9 @@ engram_status engram_layer_bind(engram_ctx* ctx, int layer, const engram_layer_w
     // The table may live in pinned host memory read through UVA.
     engram_layer_weights bw = *w;
     bool host_table = false;
+    if (tbf16) bw.scales = nullptr;  // BF16 rows carry no scales
     for (const uint8_t** p : {&bw.table, &bw.scales}) {
+        if (!*p) continue;
         cudaPointerAttributes attr{};
         e = cudaPointerGetAttributes(&attr, *p);
         if (e != cudaSuccess) {
@@ -507,14 +515,16 @@ engram_status engram_layer_bind(engram_ctx* ctx, int layer, const engram_layer_w
     e = cudaMemcpy(ctx->d_err + 1, init, sizeof init, cudaMemcpyHostToDevice);
     if (e != cudaSuccess) return cuda_fail(e, "bind scan init");
     const uint64_t nscale = L.rows * (ctx->desc.row_dim / 32);
-    e = launch_scale_range(bw.scales, nscale, ctx->d_err + 1, 0);
+    if (!tbf16) e = launch_scale_range(bw.scales, nscale, ctx->d_err + 1, 0);
     if (e == cudaSuccess)
         e = launch_absmax_bf16(w->wkv, (uint64_t)ctx->N * ctx->K, ctx->d_err + 3, 0);
     uint32_t res[3] = {0, 0, 0};
     if (e == cudaSuccess) e = cudaMemcpy(res, ctx->d_err + 1, sizeof res, cudaMemcpyDeviceToHost);
     if (e != cudaSuccess) return cuda_fail(e, "bind scans");
     const uint32_t smin = res[0], smax = res[1], wabs = res[2];
-    const bool want_f16 = !(w->flags & ENGRAM_BIND_BF16_OPERANDS);
+    // BF16 table rows are copied into BF16 operands (the fused kernels, which
+    // decode MXFP8 in their producers, do not take them)
+    const bool want_f16 = !(w->flags & ENGRAM_BIND_BF16_OPERANDS) && !tbf16;
     const bool scales_fit = smax != 255u && smax >= smin && smax - smin <= 22u;
     const bool w_finite = wabs < 0x7F80u;
     if (L.wkv_f16) {
@@ -562,6 +572,7 @@ engram_status engram_layer_bind(engram_ctx* ctx, int layer, const engram_layer_w
     // 256-wide rows are gathered whole, once per tile and bucket; other widths
     // per 64-column k-block.
     L.bucket_gather = L.f16 && ctx->desc.row_dim == 256;
+    L.table_bf16 = tbf16;
     (void)host_table;
     L.scale_min = smin;
     L.scale_max = smax;
@@ -585,6 +596,7 @@ engram_status engram_layer_info(const engram_ctx* ctx, int layer, engram_layer_i
     out->wkv_exp = L.wkv_exp;
     out->a_exp_shift = L.a_exp_shift;
     out->bucket_gather = L.bucket_gather ? 1 : 0;
+    out->table_bf16 = L.table_bf16 ? 1 : 0;
     return ok();
 }
 
@@ -596,6 +608,17 @@ engram_status engram_table_fill(const engram_ctx* ctx, uint64_t seed, uint8_t* d
     if (!aligned16(data)) return fail(ENGRAM_EINVAL, "data must be 16-byte aligned");
     cudaError_t e = launch_table_fill(seed, data, scale, row_begin, row_end,
                                       (int)ctx->desc.row_dim, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "table fill launch");
+    return ok();
+}
+
+engram_status engram_table_fill_bf16(const engram_ctx* ctx, uint64_t seed, uint16_t* data,
+                                     uint64_t row_begin, uint64_t row_end, void* stream) {
+    if (!ctx || !data) return fail(ENGRAM_EINVAL, "null argument");
+    if (row_end < row_begin) return fail(ENGRAM_EINVAL, "row_end < row_begin");
+    if (!aligned16(data)) return fail(ENGRAM_EINVAL, "data must be 16-byte aligned");
+    cudaError_t e = launch_table_fill_bf16(seed, data, row_begin, row_end,
+                                           (int)ctx->desc.row_dim, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "table fill launch");
     return ok();
 }
@@ -725,7 +748,8 @@ engram_status engram_gather_dequant(const engram_ctx* ctx, int layer, const uint
     if (T == 0) return ok();
     if (!d_rows || !d_emb || !aligned16(d_emb)) return fail(ENGRAM_EINVAL, "rows / emb");
     const LayerState& L = ctx->layers[layer];
-    cudaError_t e = launch_gather(geometry(ctx), d_rows, T, L.w.table, L.w.scales, L.rows, d_emb,
+    cudaError_t e = launch_gather(geometry(ctx), d_rows, T, L.w.table, L.w.scales, L.rows,
+                                  L.table_bf16, d_emb,
                                   ctx->d_err, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "gather launch");
     return ok();
@@ -806,7 +830,8 @@ engram_status engram_stage_rows(const engram_ctx* ctx, int layer, const uint32_t
     cudaError_t e = launch_gather_stage(hash_params(ctx, layer),
                                         reinterpret_cast<const uint4*>(d_windows), T,
                                         (int)ctx->desc.row_dim, L.w.table, L.w.scales, L.rows,
-                                        L.f16, L.a_exp_shift, static_cast<uint16_t*>(d_workspace),
+                                        L.table_bf16, L.f16, L.a_exp_shift,
+                                        static_cast<uint16_t*>(d_workspace),
                                         ctx->d_err, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "staged gather launch");
     return ok();
@@ -887,6 +912,8 @@ engram_status engram_project_windows(const engram_ctx* ctx, int layer, const uin
     if (!d_windows || !d_kv || !aligned16(d_windows) || !aligned16(d_kv))
         return fail(ENGRAM_EINVAL, "windows / kv (16-byte aligned)");
     const LayerState& L = ctx->layers[layer];
+    if (L.table_bf16)
+        return fail(ENGRAM_EUNSUPPORTED, "BF16-table layers: engram_gather_dequant + engram_project");
     MmaArgs a = mma_args(ctx, layer, T);
     a.windows = reinterpret_cast<const uint4*>(d_windows);
     a.kv = d_kv;

@@ -93,11 +93,15 @@ struct MmaArgs {
 // kernels_misc.cu
 cudaError_t launch_table_fill(uint64_t seed, uint8_t* data, uint8_t* scale, uint64_t row_begin,
                               uint64_t row_end, int row_dim, cudaStream_t s);
+// The same rows stored as BF16 values (the dequantised MXFP8 values, exact).
+cudaError_t launch_table_fill_bf16(uint64_t seed, uint16_t* data, uint64_t row_begin,
+                                   uint64_t row_end, int row_dim, cudaStream_t s);
 cudaError_t launch_hash(const HashParams& hp, const uint4* windows, int64_t T, uint32_t* rows,
                         cudaStream_t s);
+// table_bf16: BF16 rows [R][row_dim] without scales (scales unused).
 cudaError_t launch_gather(const Geometry& g, const uint32_t* rows, int64_t T,
                           const uint8_t* table, const uint8_t* scales, uint64_t nrows,
-                          uint16_t* emb, uint32_t* err, cudaStream_t s);
+                          bool table_bf16, uint16_t* emb, uint32_t* err, cudaStream_t s);
 // kv may be the sum of nsplit (<= 8) partial buffers, split_stride floats
 // apart, added in split order.  kv, hidden, wq and wk 16-byte aligned.
 cudaError_t launch_gate(const Geometry& g, const float* kv, int nsplit, int64_t split_stride,
@@ -111,8 +115,8 @@ cudaError_t launch_absmax_bf16(const uint16_t* x, uint64_t n, uint32_t* out, cud
 // Staged forward, step 1: windows -> operand rows e [T][K] (FP16 or BF16).
 cudaError_t launch_gather_stage(const HashParams& hp, const uint4* windows, int64_t T, int row_dim,
                                 const uint8_t* table, const uint8_t* scales, uint64_t nrows,
-                                bool f16, int exp_shift, uint16_t* e, uint32_t* err,
-                                cudaStream_t s);
+                                bool table_bf16, bool f16, int exp_shift, uint16_t* e,
+                                uint32_t* err, cudaStream_t s);
 // FP16 copy of the BF16 wkv [N][K] (N % 128 == 0, K % 64 == 0), values x
 // scale rounded to nearest even, stored as 128 x 64 tiles: element (n, k) at
 // ((n / 128) (K / 64) + k / 64) 8192 + (n % 128) 64 + k % 64.

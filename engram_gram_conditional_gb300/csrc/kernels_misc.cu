@@ -87,6 +87,35 @@ __global__ void k_table_fill(uint64_t seed, uint8_t* __restrict__ data,
     }
 }
 
+// The same table stored as BF16 rows without scales: every value is the
+// dequantised MXFP8 value E4M3(code) x 2^(scale - 127), which BF16 holds
+// exactly, so a BF16-table layer computes the same forward as the MXFP8 one.
+__global__ void k_table_fill_bf16(uint64_t seed, uint16_t* __restrict__ data, uint64_t row_begin,
+                                  uint64_t nrows, int row_dim) {
+    const uint32_t k0 = (uint32_t)seed, k1 = (uint32_t)(seed >> 32);
+    const int cpr = row_dim / 8;
+    const uint64_t items = nrows * (uint64_t)cpr;
+    for (uint64_t i = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; i < items;
+         i += (uint64_t)gridDim.x * blockDim.x) {
+        const uint64_t row = row_begin + i / cpr;
+        const uint32_t chunk = (uint32_t)(i % cpr);
+        const uint4 o = philox4x32_10(make_uint4((uint32_t)row, (uint32_t)(row >> 32), chunk, 0u),
+                                      k0, k1);
+        uint32_t w[2] = {0u, 0u};
+#pragma unroll
+        for (int l = 0; l < 8; ++l) {
+            const uint32_t idx = (lane16(o, l) * 254u) >> 16;
+            const uint32_t code = idx < 127u ? idx : idx + 1u;
+            w[l >> 2] |= code << (8 * (l & 3));
+        }
+        const uint4 sv = philox4x32_10(make_uint4((uint32_t)row, (uint32_t)(row >> 32), 0u, 1u),
+                                       k0, k1);
+        const uint32_t se = 119u + ((lane16(sv, (int)(chunk / 4)) * 9u) >> 16);
+        *reinterpret_cast<uint4*>(data + row * (uint64_t)row_dim + chunk * 8u) =
+            decode8(w[0], w[1], e8m0_to_f32(se));
+    }
+}
+
 // a2: one thread per (token, bucket).
 __global__ void k_hash(const __grid_constant__ HashParams hp, const uint4* __restrict__ windows,
                        int64_t T, uint32_t* __restrict__ rows) {
@@ -101,9 +130,12 @@ __global__ void k_hash(const __grid_constant__ HashParams hp, const uint4* __res
 
 // a3: one thread per 16 columns of one (token, bucket) row: a 16-byte load of
 // codes, one scale byte, two 16-byte stores of BF16.
+// With table_bf16 the table holds BF16 rows (row_dim x 2 bytes, no scales)
+// and the decode is a copy.
 __global__ void k_gather(const uint32_t* __restrict__ rows, int64_t T, int nb, int row_dim,
                          const uint8_t* __restrict__ table, const uint8_t* __restrict__ scales,
-                         uint64_t nrows, uint16_t* __restrict__ emb, uint32_t* err) {
+                         uint64_t nrows, int table_bf16, uint16_t* __restrict__ emb,
+                         uint32_t* err) {
     const int cpr = row_dim / 16;
     const int groups = row_dim / 32;
     const int64_t items = T * nb * (int64_t)cpr;
@@ -117,7 +149,11 @@ __global__ void k_gather(const uint32_t* __restrict__ rows, int64_t T, int nb, i
             atomicOr(err, kErrBounds);
             row = kMasked;
         }
-        if (row != kMasked) {
+        if (row != kMasked && table_bf16) {
+            const uint4* src = reinterpret_cast<const uint4*>(table + (uint64_t)row * row_dim * 2) + chunk * 2;
+            out0 = __ldg(src);
+            out1 = __ldg(src + 1);
+        } else if (row != kMasked) {
             const uint4 c = __ldg(reinterpret_cast<const uint4*>(table + (uint64_t)row * row_dim) + chunk);
             const float sf = e8m0_to_f32(__ldg(scales + (uint64_t)row * groups + chunk / 2));
             out0 = decode8(c.x, c.y, sf);
@@ -137,7 +173,7 @@ template <bool kF16>
 __global__ void k_gather_stage(const __grid_constant__ HashParams hp, const uint4* __restrict__ windows,
                                int64_t T, int row_dim, const uint8_t* __restrict__ table,
                                const uint8_t* __restrict__ scales, uint64_t nrows, int exp_shift,
-                               uint16_t* __restrict__ e, uint32_t* err) {
+                               int table_bf16, uint16_t* __restrict__ e, uint32_t* err) {
     const int lpr = row_dim / 16;              // lanes per row
     const int rpw = 32 / lpr;                  // rows per warp pass
     const int lane = threadIdx.x & 31;
@@ -162,7 +198,11 @@ __global__ void k_gather_stage(const __grid_constant__ HashParams hp, const uint
         row = __shfl_sync(0xFFFFFFFFu, row, sub * lpr);
         if (!live_item) continue;
         uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
-        if (row != kMasked) {
+        if (row != kMasked && !kF16 && table_bf16) {  // BF16 rows: a copy
+            const uint4* src = reinterpret_cast<const uint4*>(table + (uint64_t)row * row_dim * 2) + chunk * 2;
+            lo = __ldg(src);
+            hi = __ldg(src + 1);
+        } else if (row != kMasked) {
             const uint4 c = __ldg(reinterpret_cast<const uint4*>(table + (uint64_t)row * row_dim) + chunk);
             const uint32_t se = __ldg(scales + (uint64_t)row * (row_dim / 32) + chunk / 2);
             if (kF16) {
@@ -366,6 +406,17 @@ __global__ void k_wkv_to_f16_tiles(const uint16_t* __restrict__ src, uint16_t* _
 
 }  // namespace
 
+cudaError_t launch_table_fill_bf16(uint64_t seed, uint16_t* data, uint64_t row_begin,
+                                   uint64_t row_end, int row_dim, cudaStream_t s) {
+    const uint64_t nrows = row_end - row_begin;
+    if (nrows == 0) return cudaSuccess;
+    const int threads = 256;
+    const int grid = grid_for((int64_t)std::min<uint64_t>(nrows * (row_dim / 8), 1ull << 40),
+                              threads, 16);
+    k_table_fill_bf16<<<grid, threads, 0, s>>>(seed, data, row_begin, nrows, row_dim);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_table_fill(uint64_t seed, uint8_t* data, uint8_t* scale, uint64_t row_begin,
                               uint64_t row_end, int row_dim, cudaStream_t s) {
     const uint64_t nrows = row_end - row_begin;
@@ -387,12 +438,13 @@ cudaError_t launch_hash(const HashParams& hp, const uint4* windows, int64_t T, u
 
 cudaError_t launch_gather(const Geometry& g, const uint32_t* rows, int64_t T,
                           const uint8_t* table, const uint8_t* scales, uint64_t nrows,
-                          uint16_t* emb, uint32_t* err, cudaStream_t s) {
+                          bool table_bf16, uint16_t* emb, uint32_t* err, cudaStream_t s) {
     if (T == 0) return cudaSuccess;
     const int threads = 256;
     const int64_t items = T * g.nb * (int64_t)(g.row_dim / 16);
     k_gather<<<grid_for(items, threads, 16), threads, 0, s>>>(rows, T, g.nb, g.row_dim, table,
-                                                              scales, nrows, emb, err);
+                                                              scales, nrows, table_bf16 ? 1 : 0,
+                                                              emb, err);
     return cudaGetLastError();
 }
 
@@ -430,19 +482,20 @@ cudaError_t launch_wkv_to_f16_tiles(const uint16_t* src, uint16_t* dst, uint64_t
 
 cudaError_t launch_gather_stage(const HashParams& hp, const uint4* windows, int64_t T, int row_dim,
                                 const uint8_t* table, const uint8_t* scales, uint64_t nrows,
-                                bool f16, int exp_shift, uint16_t* e, uint32_t* err,
-                                cudaStream_t s) {
+                                bool table_bf16, bool f16, int exp_shift, uint16_t* e,
+                                uint32_t* err, cudaStream_t s) {
     if (T == 0) return cudaSuccess;
+    if (table_bf16 && f16) return cudaErrorInvalidValue;  // BF16 rows feed BF16 operands
     const int threads = 256;
     const int64_t rows_per_warp = 32 / (row_dim / 16);
     const int64_t warps = (T * hp.nb + rows_per_warp - 1) / rows_per_warp;
     const int grid = grid_for(warps * 32, threads, 8);
     if (f16)
         k_gather_stage<true><<<grid, threads, 0, s>>>(hp, windows, T, row_dim, table, scales, nrows,
-                                                      exp_shift, e, err);
+                                                      exp_shift, 0, e, err);
     else
         k_gather_stage<false><<<grid, threads, 0, s>>>(hp, windows, T, row_dim, table, scales, nrows,
-                                                       exp_shift, e, err);
+                                                       exp_shift, table_bf16 ? 1 : 0, e, err);
     return cudaGetLastError();
 }
 

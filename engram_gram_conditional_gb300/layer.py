@@ -9,8 +9,8 @@ from __future__ import annotations
 import numpy as np
 import torch
 
-from . import (engram_ctx_create, engram_ctx_destroy, engram_layer_bind, engram_layer_params,
-               engram_table_fill)
+from . import (BIND_TABLE_BF16, engram_ctx_create, engram_ctx_destroy, engram_layer_bind,
+               engram_layer_params, engram_table_fill, engram_table_fill_bf16)
 
 
 def _round16(n: int) -> int:
@@ -52,16 +52,21 @@ class EngramLayerSet:
 
     def bind(self, layer: int, table_seed: int, wkv, wq, wk, host_table: bool = False,
              stream=None, flags: int = 0):
-        """Allocate and fill the layer's MXFP8 table, upload wkv / w_q / w_k, bind."""
+        """Allocate and fill the layer's table, upload wkv / w_q / w_k, bind.
+
+        The table is MXFP8 (codes and E8M0 scales), or with flags containing
+        BIND_TABLE_BF16 the same rows stored as BF16 values without scales."""
         rows = self.rows(layer)
         rd = self.geom["row_dim"]
-        if host_table:
-            table = torch.empty(_round16(rows * rd), dtype=torch.uint8, pin_memory=True)
-            scales = torch.empty(_round16(rows * rd // 32), dtype=torch.uint8, pin_memory=True)
+        where = dict(pin_memory=True) if host_table else dict(device=self.device)
+        if flags & BIND_TABLE_BF16:
+            table = torch.empty(_round16(rows * rd * 2), dtype=torch.uint8, **where)
+            scales = None
+            engram_table_fill_bf16(self.ctx, table_seed, table, 0, rows, stream)
         else:
-            table = torch.empty(_round16(rows * rd), dtype=torch.uint8, device=self.device)
-            scales = torch.empty(_round16(rows * rd // 32), dtype=torch.uint8, device=self.device)
-        engram_table_fill(self.ctx, table_seed, table, scales, 0, rows, stream)
+            table = torch.empty(_round16(rows * rd), dtype=torch.uint8, **where)
+            scales = torch.empty(_round16(rows * rd // 32), dtype=torch.uint8, **where)
+            engram_table_fill(self.ctx, table_seed, table, scales, 0, rows, stream)
         d_wkv = _as_device(wkv, torch.int16, self.device).view(self.N, self.K)
         d_wq = _as_device(wq, torch.float32, self.device).view(-1)
         d_wk = _as_device(wk, torch.float32, self.device).view(-1)

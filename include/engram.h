@@ -109,14 +109,23 @@ typedef struct engram_ctx_desc {
  * (the E8M0 exponent range, see engram_layer_info): bind again after
  * rewriting a table. */
 #define ENGRAM_BIND_BF16_OPERANDS 1u /* flags: fused kernels decode to BF16 only */
+/* flags: the table holds BF16 rows [rows][row_dim] (2 x row_dim bytes each,
+ * the already dequantised values) and no scales (scales may be NULL): the
+ * second storage format of the pages ([zhuai], the w8a8 repository's BF16
+ * table).  The gathers copy the rows; the operands are BF16.  Such a layer
+ * runs through engram_gather_dequant, engram_forward_staged and its two
+ * steps; engram_forward, engram_forward_noalloc and engram_project_windows,
+ * whose kernels decode MXFP8 rows while they gather, return
+ * ENGRAM_EUNSUPPORTED. */
+#define ENGRAM_BIND_TABLE_BF16 2u
 typedef struct engram_layer_weights {
-    const uint8_t* table;   /* [rows][row_dim] E4M3 codes                     */
-    const uint8_t* scales;  /* [rows][row_dim / 32] E8M0 exponents            */
+    const uint8_t* table;   /* [rows][row_dim] E4M3 codes (BF16 table: bf16 [rows][row_dim]) */
+    const uint8_t* scales;  /* [rows][row_dim / 32] E8M0 exponents (BF16 table: unused) */
     uint64_t rows;          /* must equal the layer's row count (engram_layer_params) */
     const uint16_t* wkv;    /* bf16 [N][K], device                            */
     const float* wq;        /* fp32 [hc][d], device                           */
     const float* wk;        /* fp32 [hc][d], device                           */
-    uint32_t flags;         /* 0 or ENGRAM_BIND_BF16_OPERANDS                  */
+    uint32_t flags;         /* 0, ENGRAM_BIND_BF16_OPERANDS, ENGRAM_BIND_TABLE_BF16 */
 } engram_layer_weights;
 
 /* How a bound layer runs.  The fused kernels feed the tensor cores FP16
@@ -137,6 +146,7 @@ typedef struct engram_layer_info_t {
     int32_t bucket_gather;          /* 1: each 256-wide table row is loaded whole,
                                        once per output tile (FP16 path, row_dim
                                        256); 0: 64-column slices per k-block     */
+    int32_t table_bf16;             /* 1: bound with ENGRAM_BIND_TABLE_BF16        */
 } engram_layer_info_t;
 engram_status engram_layer_info(const engram_ctx* ctx, int layer, engram_layer_info_t* out);
 
@@ -175,6 +185,13 @@ engram_status engram_layer_bind(engram_ctx* ctx, int layer, const engram_layer_w
 engram_status engram_table_fill(const engram_ctx* ctx, uint64_t seed, uint8_t* data,
                                 uint8_t* scale, uint64_t row_begin, uint64_t row_end,
                                 void* stream);
+/* The same rows for a BF16-table layer: data bf16 [rows][row_dim] (16-byte
+ * aligned), value = E4M3(code) x 2^(scale - 127) of engram_table_fill's code
+ * and scale for the same (seed, row, column), which BF16 holds exactly.  A
+ * layer bound to this table computes the same forward as one bound to the
+ * MXFP8 table of the same seed. */
+engram_status engram_table_fill_bf16(const engram_ctx* ctx, uint64_t seed, uint16_t* data,
+                                     uint64_t row_begin, uint64_t row_end, void* stream);
 
 /* Sessions: a hash history (the last three compressed ids and a count).
  * "第四步": every token enters the history exactly once; prefill appends a

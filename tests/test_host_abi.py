@@ -29,7 +29,7 @@ def built():
 def header_functions():
     src = open(os.path.join(ROOT, "include", "engram.h")).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"\b(engram_[a-z_]+)\s*\(", src)))
+    return sorted(set(re.findall(r"\b(engram_[a-z0-9_]+)\s*\(", src)))
 
 
 def test_library_exports_every_declared_function():
