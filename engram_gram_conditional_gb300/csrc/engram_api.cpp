@@ -131,7 +131,7 @@ struct LayerState {
     bool f16 = false;
     uint16_t* wkv_f16 = nullptr;   // library-owned copy, wkv x 2^wkv_exp
     CUtensorMap tm_wkv_f16{};
-    CUtensorMap tm_wkv_f16_half{};
+    CUtensorMap tm_wkv_f16_2k{};   // the tiled FP16 copy with 256-row boxes (2 k-blocks)
     int wkv_exp = 0;
     int a_exp_shift = 0;
     uint32_t scale_min = 0, scale_max = 0;
@@ -213,6 +213,7 @@ MmaArgs mma_args(const engram_ctx* ctx, int layer, int64_t T) {
     a.k_splits = 1;
     a.kv_split_stride = 0;
     a.b_tiled = L.f16 ? 1 : 0;  // the FP16 wkv copy is tiled, the caller's BF16 wkv is not
+    a.a_tiled = 0;
     a.hc = (int)ctx->desc.hc;
     a.d = (int)ctx->desc.d;
     a.eps = (float)ctx->desc.eps;
@@ -559,7 +560,9 @@ engram_status engram_layer_bind(engram_ctx* ctx, int layer, const engram_layer_w
         if (e == cudaSuccess)
             e = make_tma_16bit(&L.tm_wkv_f16, L.wkv_f16, (uint64_t)ctx->N * ctx->K / kBK, kBK,
                                kBN / 2, true);
-        if (e == cudaSuccess) L.tm_wkv_f16_half = L.tm_wkv_f16;
+        if (e == cudaSuccess)
+            e = make_tma_16bit(&L.tm_wkv_f16_2k, L.wkv_f16, (uint64_t)ctx->N * ctx->K / kBK, kBK,
+                               kBN, true);
         if (e != cudaSuccess) {
             cudaFree(L.wkv_f16);
             L.wkv_f16 = nullptr;
@@ -805,13 +808,17 @@ engram_status engram_forward(const engram_ctx* ctx, int layer, const uint32_t* d
 // hide, while the separate gate kernel has the whole GPU to itself.
 static int staged_splits(const engram_ctx* ctx, int64_t T) { return forward_k_splits(ctx, T, 8); }
 
-// The staged GEMMs run on CTA pairs (256-token tiles) unless the batch holds a
-// single 128-token block, which would leave half of every pair idle.
-static bool use_pairs(const MmaArgs& a) { return a.m_blocks >= 2; }
+
+// Bytes of the staged operand matrix e: whole 128-token blocks (the FP16
+// operand is stored in 128 x 64 tiles).
+static size_t staged_e_bytes(const engram_ctx* ctx, int64_t T) {
+    const size_t rows = ((size_t)T + kBM - 1) / kBM * kBM;
+    return (rows * ctx->K * sizeof(uint16_t) + 255) & ~(size_t)255;
+}
 
 size_t engram_forward_staged_workspace_bytes(const engram_ctx* ctx, int64_t T) {
     if (!ctx || T <= 0) return 0;
-    const size_t e = ((size_t)T * ctx->K * sizeof(uint16_t) + 255) & ~(size_t)255;
+    const size_t e = staged_e_bytes(ctx, T);
     const int splits = staged_splits(ctx, T);
     if (splits > 1)
         return e + (((size_t)splits * T * ctx->N * sizeof(float) + 255) & ~(size_t)255);
@@ -848,8 +855,7 @@ engram_status engram_forward_staged_rows(const engram_ctx* ctx, int layer,
         return fail(ENGRAM_EINVAL, "windows / hidden / workspace (16-byte aligned)");
     const LayerState& L = ctx->layers[layer];
     uint16_t* e_scratch = static_cast<uint16_t*>(d_workspace);
-    char* rest = static_cast<char*>(d_workspace) +
-                 (((size_t)T * ctx->K * sizeof(uint16_t) + 255) & ~(size_t)255);
+    char* rest = static_cast<char*>(d_workspace) + staged_e_bytes(ctx, T);
     MmaArgs a = mma_args(ctx, layer, T);
     a.windows = reinterpret_cast<const uint4*>(d_windows);
     a.hidden = d_hidden;
@@ -861,20 +867,35 @@ engram_status engram_forward_staged_rows(const engram_ctx* ctx, int layer,
     a.n_tile_begin = 0;
     a.n_tiles = ctx->N / kBN;
     cudaStream_t s = (cudaStream_t)stream;
-    // the forward GEMM reading e through TMA
-    CUtensorMap tmA;
-    cudaError_t e = make_tma_16bit(&tmA, e_scratch, (uint64_t)T, (uint64_t)ctx->K, kBM, L.f16);
-    if (e != cudaSuccess) return cuda_fail(e, "e tensor map");
+    // the forward GEMM reading e through TMA.  FP16: e is tiled; on CTA pairs
+    // each TMA box holds two k-blocks (the split ranges are even), otherwise
+    // one; BF16: e is row-major [T][K]; pairs from two 128-token blocks on
     const int splits = staged_splits(ctx, T);
+    const int KB = ctx->K / kBK;
+    // (a single 128-token block runs on one CTA per tile: half of a pair would idle)
+    const bool two_k = L.f16 && a.m_blocks >= 2 && (KB / splits) % 2 == 0 && KB % splits == 0;
+    CUtensorMap tmA;
+    cudaError_t e;
+    if (L.f16) {
+        a.a_tiled = 1;
+        e = make_tma_16bit(&tmA, e_scratch, (uint64_t)a.m_blocks * KB * kBM, kBK,
+                           two_k ? 2 * kBM : kBM, true);
+    } else {
+        e = make_tma_16bit(&tmA, e_scratch, (uint64_t)T, (uint64_t)ctx->K, kBM, false);
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "e tensor map");
+    // wkv: FP16 tiled (2-k-block boxes for pairs), or the caller's BF16
+    const bool pairs = L.f16 ? two_k : a.m_blocks >= 2;
+    const CUtensorMap& tmB = L.f16 ? (pairs ? L.tm_wkv_f16_2k : L.tm_wkv_f16)
+                                   : (pairs ? L.tm_wkv_half : L.tm_wkv);
     if (splits > 1) {
         // small batch: split-K projection into per-split kv buffers, then the gate
         a.k_splits = splits;
         a.kv = reinterpret_cast<float*>(rest);
         a.ldkv = ctx->N;
         a.kv_split_stride = T * (int64_t)ctx->N;
-        e = use_pairs(a)
-                ? launch_project_split_pair(a, L.f16, tmA, L.f16 ? L.tm_wkv_f16_half : L.tm_wkv_half, s)
-                : launch_project_split(a, L.f16, tmA, L.f16 ? L.tm_wkv_f16 : L.tm_wkv, s);
+        e = pairs ? launch_project_split_pair(a, L.f16, tmA, tmB, s)
+                  : launch_project_split(a, L.f16, tmA, tmB, s);
         if (e != cudaSuccess) return cuda_fail(e, "split projection launch");
         e = launch_gate(geometry(ctx), a.kv, splits, a.kv_split_stride, a.windows, T, d_hidden,
                         L.w.wq, L.w.wk, d_gates, s);
@@ -883,8 +904,8 @@ engram_status engram_forward_staged_rows(const engram_ctx* ctx, int layer,
     }
     e = forward_bind_ws(ctx, T, 8, rest, a, s);
     if (e != cudaSuccess) return cuda_fail(e, "forward counters");
-    e = use_pairs(a) ? launch_forward_tma_pair(a, L.f16, tmA, L.f16 ? L.tm_wkv_f16_half : L.tm_wkv_half, s)
-                     : launch_forward_tma(a, L.f16, tmA, L.f16 ? L.tm_wkv_f16 : L.tm_wkv, s);
+    e = pairs ? launch_forward_tma_pair(a, L.f16, tmA, tmB, s)
+              : launch_forward_tma(a, L.f16, tmA, tmB, s);
     if (e != cudaSuccess) return cuda_fail(e, "staged forward launch");
     return ok();
 }

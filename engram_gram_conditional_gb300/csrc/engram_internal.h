@@ -55,6 +55,7 @@ struct MmaArgs {
     int group_m;       // tile rasterisation: M blocks per group
     int k_splits;      // split-K factor (>= 1); the tile list holds every (tile, split)
     int b_tiled;       // wkv map over 128 x 64 tiles (the FP16 copy), else row-major [N][K]
+    int a_tiled;       // TMA-fed A in 128 x 64 tiles (the staged FP16 operand), else [T][K]
     int64_t kv_split_stride;  // kEpiStoreKv: floats between the kv buffers of two splits
     int hc, d;
     float eps;
@@ -112,7 +113,10 @@ cudaError_t launch_gate(const Geometry& g, const float* kv, int nsplit, int64_t 
 // pattern without the sign (out[2] preset to 0).
 cudaError_t launch_scale_range(const uint8_t* scales, uint64_t n, uint32_t* out, cudaStream_t s);
 cudaError_t launch_absmax_bf16(const uint16_t* x, uint64_t n, uint32_t* out, cudaStream_t s);
-// Staged forward, step 1: windows -> operand rows e [T][K] (FP16 or BF16).
+// Staged forward, step 1: windows -> operand rows e: FP16 in 128 x 64 tiles
+// (element (t, k) at ((t / 128) (K / 64) + k / 64) 8192 + (t % 128) 64 + k % 64;
+// rows of the last 128-token block past T are not written), or BF16 row-major
+// [T][K].
 cudaError_t launch_gather_stage(const HashParams& hp, const uint4* windows, int64_t T, int row_dim,
                                 const uint8_t* table, const uint8_t* scales, uint64_t nrows,
                                 bool table_bf16, bool f16, int exp_shift, uint16_t* e,

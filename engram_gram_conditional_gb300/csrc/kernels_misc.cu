@@ -166,7 +166,8 @@ __global__ void k_gather(const uint32_t* __restrict__ rows, int64_t T, int nb, i
 }
 
 // Staged forward, step 1: windows -> dequantised operand rows in a scratch
-// matrix e [T][K] (FP16 scaled by 2^(s - 127 + exp_shift), or BF16).  Each table
+// matrix e (FP16 scaled by 2^(s - 127 + exp_shift) in 128 x 64 tiles, or BF16
+// row-major [T][K]).  Each table
 // row is read whole: row_dim / 16 lanes per row, 16 codes and their scale per
 // lane; the first lane of a row hashes its (token, bucket) pair.
 template <bool kF16>
@@ -227,7 +228,13 @@ __global__ void k_gather_stage(const __grid_constant__ HashParams hp, const uint
                 hi = decode8(c.z, c.w, sf);
             }
         }
-        uint4* dst = reinterpret_cast<uint4*>(e + t * (int64_t)K + (int64_t)b * row_dim + 16 * chunk);
+        // column k of row t: row-major, or (kF16) in 128 x 64 tiles, tile
+        // (t / 128) (K / 64) + k / 64, so that two k-blocks of a 128-token
+        // block are 32 contiguous KB (one TMA box)
+        const int64_t k = (int64_t)b * row_dim + 16 * chunk;
+        const int64_t off = kF16 ? ((((t >> 7) * (K >> 6) + (k >> 6)) << 7) + (t & 127)) * 64 + (k & 63)
+                                 : t * (int64_t)K + k;
+        uint4* dst = reinterpret_cast<uint4*>(e + off);
         dst[0] = lo;
         dst[1] = hi;
     }

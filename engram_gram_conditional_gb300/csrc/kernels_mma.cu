@@ -81,15 +81,26 @@ enum ASource : int {
 // TMEM.  The even CTA issues the MMAs.
 constexpr int kBStageHalf = kBStage / 2;  // 16 KB
 
+// k-blocks per pipeline stage.  A TMA copy costs the SM about the same time
+// (some 0.2 us of its copy engine) whether it moves 16 or 32 KB, so the
+// FP16 pair kernel, whose operands are both stored in 128 x 64 tiles, loads
+// two k-blocks of each operand with one 32 KB box per stage.
+template <int kASrc, bool kF16>
+__host__ __device__ constexpr int k_blocks_per_stage() {
+    return kASrc == kASrcTmaPair && kF16 ? 2 : 1;
+}
+
 // Shared-memory layout of each variant.
-template <int kASrc>
+template <int kASrc, int kKS = 1>
 struct Layout {
     static constexpr bool kPair = kASrc == kASrcTmaPair;
-    static constexpr int kA = kASrc == kASrcGatherBucket ? 8 : 4;              // A ring stages
-    static constexpr int kB = kASrc == kASrcGatherBucket ? 3 : kPair ? 8 : 4;  // B ring stages
-    static constexpr int kBStageBytes = kPair ? kBStageHalf : kBStage;
+    // ring stages (each kKS k-blocks)
+    static constexpr int kA = kASrc == kASrcGatherBucket ? 8 : kKS == 2 ? 2 : 4;
+    static constexpr int kB = kASrc == kASrcGatherBucket ? 3 : kKS == 2 ? 4 : kPair ? 8 : 4;
+    static constexpr int kAStageBytes = kAStage * kKS;
+    static constexpr int kBStageBytes = (kPair ? kBStageHalf : kBStage) * kKS;
     static constexpr int kOffA = 0;
-    static constexpr int kOffB = kOffA + kA * kAStage;
+    static constexpr int kOffB = kOffA + kA * kAStageBytes;
     static constexpr int kOffRows = kOffB + kB * kBStageBytes;
     static constexpr int kRowsBytes = kASrc == kASrcGatherKb ? kBM * kRowStride * 4 : 0;
     static constexpr int kOffBar = kOffRows + kRowsBytes;
@@ -683,7 +694,8 @@ template <int kASrc, bool kF16, int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
 k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
       const __grid_constant__ MmaArgs a) {
-    using L = Layout<kASrc>;
+    constexpr int kKS = k_blocks_per_stage<kASrc, kF16>();
+    using L = Layout<kASrc, kKS>;
     constexpr int kA = L::kA, kB = L::kB;
     constexpr bool kPair = L::kPair;
     constexpr bool kFusedA = kASrc != kASrcTma && !kPair;
@@ -704,7 +716,7 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
     auto tfull = [&](int acc) { return bar0 + 8u * (uint32_t)(2 * kA + 2 * kB + acc); };
     auto tempty = [&](int acc) { return bar0 + 8u * (uint32_t)(2 * kA + 2 * kB + 2 + acc); };
     const uint32_t a_base = sbase + L::kOffA;
-    auto a_stage = [&](int s) { return a_base + (uint32_t)(s * kAStage); };
+    auto a_stage = [&](int s) { return a_base + (uint32_t)(s * L::kAStageBytes); };
     auto b_stage = [&](int s) { return sbase + L::kOffB + (uint32_t)(s * L::kBStageBytes); };
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffFlag);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffTmem);
@@ -780,10 +792,13 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
                 int mb, nt, ks;
                 coords(tile, mb, nt, ks);
                 const int n0 = (a.n_tile_begin + nt) * kBN;
+                // stages of kKS k-blocks (the host keeps every split's range a
+                // multiple of kKS)
                 const int kb_lo = ks * KB / a.k_splits, nkb = (ks + 1) * KB / a.k_splits - kb_lo;
-                const int rot = k_rotation(nt, nkb);
-                for (int j = 0; j < nkb && !a.starve_b; ++j, ++it) {
-                    const int kb = kb_lo + (j + rot) % nkb;
+                const int nst = nkb / kKS;
+                const int rot = k_rotation(nt, nst);
+                for (int j = 0; j < nst && !a.starve_b; ++j, ++it) {
+                    const int kb = kb_lo + ((j + rot) % nst) * kKS;  // first k-block of the stage
                     const int sb = it % kB;
                     if (do_b) {
                         if (!mbar_wait(b_empty(sb), ((uint32_t)(it / kB) & 1u) ^ 1u, abort_flag, lim)) {
@@ -792,7 +807,8 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
                             break;
                         }
                         // wkv rows [r, r + 128) of k-block kb: in the tiled FP16 copy,
-                        // box row ((r / 128) KB + kb) 128 at column 0
+                        // box row ((r / 128) KB + kb) 128 at column 0 (a box of kKS
+                        // tiles holds the stage's kKS k-blocks)
                         auto b_x = [&](int r) { return a.b_tiled ? 0 : kb * kBK; };
                         auto b_y = [&](int r) { return a.b_tiled ? ((r >> 7) * KB + kb) * 128 : r; };
                         if constexpr (kPair) {
@@ -818,13 +834,16 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
                             ok = false;
                             break;
                         }
+                        // the operand of M block mb, k-block kb: row-major [T][K], or
+                        // in 128 x 64 tiles at box row (mb KB + kb) 128
+                        const int ax = a.a_tiled ? 0 : kb * kBK;
+                        const int ay = a.a_tiled ? (mb * KB + kb) * 128 : mb * kBM;
                         if constexpr (kPair) {
-                            if (issuer) mbar_expect_tx(a_full(sa), 2 * kAStage);
-                            tma_load_2d_pair(a_stage(sa), &tmA, map_rank(a_full(sa), 0), kb * kBK,
-                                             mb * kBM);
+                            if (issuer) mbar_expect_tx(a_full(sa), 2 * L::kAStageBytes);
+                            tma_load_2d_pair(a_stage(sa), &tmA, map_rank(a_full(sa), 0), ax, ay);
                         } else {
-                            mbar_expect_tx(a_full(sa), kAStage);
-                            tma_load_2d(a_stage(sa), &tmA, a_full(sa), kb * kBK, mb * kBM);
+                            mbar_expect_tx(a_full(sa), L::kAStageBytes);
+                            tma_load_2d(a_stage(sa), &tmA, a_full(sa), ax, ay);
                         }
                     }
                 }
@@ -851,9 +870,8 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
                 int mb_, nt_, ks;
                 coords(tile, mb_, nt_, ks);
                 const int kb_lo = ks * KB / a.k_splits, nkb = (ks + 1) * KB / a.k_splits - kb_lo;
-                const int rot = k_rotation(nt_, nkb);
-                for (int j = 0; j < nkb; ++j, ++it) {
-                    const int kb = kb_lo + (j + rot) % nkb;
+                const int nst = nkb / kKS;
+                for (int j = 0; j < nst; ++j, ++it) {
                     const int sa = it % kA, sb = it % kB;
                     if (!wait(a_full(sa), (uint32_t)(it / kA) & 1u) ||
                         !wait(b_full(sb), (uint32_t)(it / kB) & 1u)) {
@@ -862,16 +880,20 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t ad = sdesc_sw128(a_stage(sa));
-                    const uint64_t bd = sdesc_sw128(b_stage(sb));
 #pragma unroll
-                    for (int k = 0; k < kBK / 16; ++k) {  // 16 elements = 32 bytes per MMA
-                        if constexpr (kPair)
-                            umma_f16kind_pair(d_tmem, ad + 2ull * k, bd + 2ull * k,
-                                              idesc<kF16, 2 * kBM>(), (j != 0) || (k != 0));
-                        else
-                            umma_f16kind(d_tmem, ad + 2ull * k, bd + 2ull * k, idesc<kF16>(),
-                                         (j != 0) || (k != 0));
+                    for (int kk = 0; kk < kKS; ++kk) {  // the stage's k-blocks, one tile apart
+                        const uint64_t ad = sdesc_sw128(a_stage(sa) + kk * (L::kAStageBytes / kKS));
+                        const uint64_t bd = sdesc_sw128(b_stage(sb) + kk * (L::kBStageBytes / kKS));
+#pragma unroll
+                        for (int k = 0; k < kBK / 16; ++k) {  // 16 elements = 32 bytes per MMA
+                            const uint32_t accum = (j != 0) || (kk != 0) || (k != 0);
+                            if constexpr (kPair)
+                                umma_f16kind_pair(d_tmem, ad + 2ull * k, bd + 2ull * k,
+                                                  idesc<kF16, 2 * kBM>(), accum);
+                            else
+                                umma_f16kind(d_tmem, ad + 2ull * k, bd + 2ull * k, idesc<kF16>(),
+                                             accum);
+                        }
                     }
                     if constexpr (kPair) {  // frees the stage in both CTAs
                         umma_commit_pair(a_empty(sa));
@@ -1268,7 +1290,7 @@ cudaError_t launch(const MmaArgs& a, const CUtensorMap& tmA, const CUtensorMap& 
                    cudaStream_t s) {
     static bool attr_set = false;
     auto kern = k_mma<kASrc, kF16, kMode>;
-    constexpr int kSmem = Layout<kASrc>::kBytes;
+    constexpr int kSmem = Layout<kASrc, k_blocks_per_stage<kASrc, kF16>()>::kBytes;
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
         if (e != cudaSuccess) return e;
