@@ -210,6 +210,7 @@ MmaArgs mma_args(const engram_ctx* ctx, int layer, int64_t T) {
     a.K = ctx->K;
     a.m_blocks = (int)((T + kBM - 1) / kBM);
     a.group_m = 16;
+    a.key_tiles = 0;
     a.k_splits = 1;
     a.kv_split_stride = 0;
     a.b_tiled = L.f16 ? 1 : 0;  // the FP16 wkv copy is tiled, the caller's BF16 wkv is not
@@ -297,6 +298,10 @@ cudaError_t forward_bind_ws(const engram_ctx* ctx, int64_t T, int max_splits, vo
     char* base = static_cast<char*>(ws);
     a.partials = reinterpret_cast<float*>(base);
     a.gbuf = reinterpret_cast<float*>(base + w.part);
+    // tile order: the key tiles of every group of 16 M blocks (pair units)
+    // before any value tile, so that a value tile does not wait for gates of
+    // key tiles that run after it (with one group this is the plain order)
+    a.key_tiles = (int)(ctx->desc.hc * ctx->desc.d / kBN);
     a.counters = reinterpret_cast<uint32_t*>(base + w.part + w.gbuf);
     a.k_splits = w.splits;
     if (w.splits > 1) {

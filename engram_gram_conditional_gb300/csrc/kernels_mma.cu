@@ -454,9 +454,9 @@ __device__ __forceinline__ int split_k_quadrant(const MmaArgs& a, int mb, int nt
     return 1;
 }
 
-// Tile order: groups of `group_m` M blocks; inside a group, N-major so the
-// CTAs in flight share wkv tiles in L2 while the group's gathered rows stay
-// L2-resident.
+// Tile order: groups of `group_m` M blocks (or pair units); inside a group,
+// N-major so the CTAs in flight share wkv tiles in L2 while the group's
+// gathered rows stay L2-resident.
 // With split-K (small M) the order is (N tile, split) outer, M block inner.
 __device__ __forceinline__ void tile_coords(const MmaArgs& a, int m_units, int tile, int& mb,
                                             int& nt, int& ks) {
@@ -468,13 +468,26 @@ __device__ __forceinline__ void tile_coords(const MmaArgs& a, int m_units, int t
         return;
     }
     ks = 0;
-    const int per_group = a.group_m * a.n_tiles;
+    // the forward's key tiles (N tiles [0, key_tiles)) all come before its
+    // value tiles, so that a value tile finds its gates long computed
+    int base_nt = 0, ntiles = a.n_tiles;
+    if (a.key_tiles > 0) {
+        const int key_items = m_units * a.key_tiles;
+        if (tile < key_items) {
+            ntiles = a.key_tiles;
+        } else {
+            tile -= key_items;
+            base_nt = a.key_tiles;
+            ntiles = a.n_tiles - a.key_tiles;
+        }
+    }
+    const int per_group = a.group_m * ntiles;
     const int g = tile / per_group;
     const int first_m = g * a.group_m;
     const int gm = min(a.group_m, m_units - first_m);
     const int r = tile - g * per_group;
-    nt = r / gm;
-    mb = first_m + (r - nt * gm);
+    nt = base_nt + r / gm;
+    mb = first_m + (r - (r / gm) * gm);
 }
 
 // Forward epilogue: starts the L2 loads of the hidden slices that row m of

@@ -135,3 +135,26 @@ def test_full_geometry_prefill_sampled():
         assert np.abs(gates[sample] - ref["gates"]).max() <= 1e-3
     finally:
         s.close()
+
+
+def test_bf16_table_in_pinned_host_memory_two_step():
+    # a BF16 table read through UVA, staged and run with the two-step API
+    s = setup_workload("tiny", host_table=True, flags=eg.BIND_TABLE_BF16)
+    try:
+        t = s.model.tensors[0]["table"]
+        assert not t.is_cuda and t.is_pinned()
+        win, _, _ = prefill_windows(s, 2, 90, spans=[(40, 3)])
+        T = win.shape[0]
+        hidden = synth.hidden_bf16(s.w, T)
+        ctx = s.model.ctx
+        ws = torch.empty(eg.engram_forward_staged_workspace_bytes(ctx, T), dtype=torch.uint8,
+                         device="cuda")
+        d_w, d_h = to_dev(win), to_dev(hidden)
+        eg.engram_stage_rows(ctx, 0, d_w, T, ws)
+        eg.engram_forward_staged_rows(ctx, 0, d_w, T, d_h, ws)
+        eg.engram_sync(ctx)
+        ref = O.forward(geom(s.w), s.w.table_seeds[0], s.oparams[0], s.W[0], s.wq[0], s.wk[0], win,
+                        hidden, np.arange(T), nthreads=4)
+        check_hidden(from_dev(d_h, np.uint16), ref["h_bf16"], "bf16 host table")
+    finally:
+        s.close()
