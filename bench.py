@@ -419,6 +419,10 @@ def main():
                                sptr, stream))
         except Exception as exc:  # extras never hide the main line
             line["extras_error"] = repr(exc)
+        try:
+            line["long_prefill"] = long_prefill(tmap, peaks, dev, stream)
+        except Exception as exc:
+            line["long_prefill"] = {"error": repr(exc)}
         if not args.no_host:
             try:
                 line["host_table"] = host_pipeline(model, wq, wk, tmap, peaks, dev, stream)
@@ -574,6 +578,49 @@ def extras(args, w, W, wq, wk, tmap, win0, d_win0, model, peaks, dev, sptr, stre
     finally:
         bm.close()
     return out
+
+
+def long_prefill(tmap, peaks, dev, stream):
+    """The long-prefill workload: one history of 50,032 tokens with three image
+    spans of 1,024 tokens, appended once and run through layers L1 and L14
+    (64M-row tables, primes of L14 after L1's, random-init wkv per layer) with
+    the staged forward.  FLOPs count the 46,960 text rows."""
+    import torch
+
+    import engram_gram_conditional_gb300 as eg
+    import synth
+    from engram_gram_conditional_gb300.layer import EngramLayerSet
+
+    wl = synth.WORKLOADS["prefill_50k_2layer"]
+    lm = EngramLayerSet.from_workload(wl, tmap, device=dev)
+    try:
+        for l in range(2):
+            q, k = synth.wq_wk(wl, l)
+            lm.bind(l, wl.table_seeds[l], synth.wkv_bf16(wl, l), q, k)
+        T = wl.tokens_per_session
+        sess = eg.engram_session_create(lm.ctx)
+        win = eg.engram_session_append(sess, synth.session_tokens(wl, 0, T),
+                                       synth.image_flags(T, wl.image_spans))
+        eg.engram_session_destroy(sess)
+        text = int((win[:, 0] != eg.DEAD).sum())
+        d_win = torch.from_numpy(win.view(np.int32)).to(dev)
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(wl.seed + 50032)
+        d_h = torch.randn((T, wl.hc, wl.d), generator=gen, device=dev).to(torch.bfloat16)
+        ws = torch.empty(eg.engram_forward_staged_workspace_bytes(lm.ctx, T), dtype=torch.uint8,
+                         device=dev)
+        sptr = stream.cuda_stream
+        for l in range(2):
+            eg.engram_forward_staged(lm.ctx, l, d_win, T, d_h, ws, None, sptr)
+        ms = timed(lambda i: eg.engram_forward_staged(lm.ctx, i % 2, d_win, T, d_h, ws, None, sptr),
+                   6, stream)
+        eg.engram_sync(lm.ctx, sptr)
+        fl = 2.0 * wl.N * wl.K * text
+        return {"tokens": T, "text_tokens": text, "layers": 2, "table_rows": [lm.rows(0), lm.rows(1)],
+                "ms_per_layer": ms, "tokens_per_s_per_layer": T / (ms / 1000.0),
+                "tflops": fl / ms / 1e9, "tc_frac": fl / ms / 1e9 / peaks["bf16"]}
+    finally:
+        lm.close()
 
 
 def host_pipeline(model, wq, wk, tmap, peaks, dev, stream):
