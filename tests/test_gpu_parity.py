@@ -321,6 +321,27 @@ def test_staged_in_two_calls_matches_one_call(prefill, T):
     assert np.array_equal(d_g[0].cpu().numpy(), g1) and np.array_equal(d_g[1].cpu().numpy(), g2)
 
 
+@pytest.mark.parametrize("flags", [0, eg.BIND_BF16_OPERANDS])
+def test_staged_pairs_with_an_odd_block_count(flags):
+    # 2,176 tokens = 17 blocks of 128: the last CTA pair has no second block,
+    # its odd CTA reads zero-filled operand rows and writes nothing
+    s = setup_workload("prefill_2048", flags=flags)
+    try:
+        T = 2176
+        win, _, _ = prefill_windows(s, 2, T // 2, spans=[(500, 6)])
+        hidden = synth.hidden_bf16(s.w, T)
+        h, gates = run_forward(s, win, hidden, staged=True)
+        sample = np.array([0, 255, 256, 2047, 2048, 2049, 2100, 2175, 500, 506, 1588])
+        ref = O.forward(geom(s.w), s.w.table_seeds[0], s.oparams[0], s.W[0], s.wq[0], s.wk[0],
+                        win, hidden, sample, nthreads=8)
+        check_hidden(h[sample], ref["h_bf16"], f"2176 tokens flags={flags}")
+        assert np.abs(gates[sample] - ref["gates"]).max() <= 1e-3
+        image = win[:, 0] == eg.DEAD
+        assert image.sum() == 12 and np.array_equal(h[image], hidden[image])
+    finally:
+        s.close()
+
+
 def test_forward_edge_cases(tiny):
     ctx = tiny.model.ctx
     eg.engram_forward(ctx, 0, None, 0, None, None)  # T = 0
