@@ -240,14 +240,8 @@ __global__ void k_gather_stage(const __grid_constant__ HashParams hp, const uint
     }
 }
 
-// a5 standalone: one CTA per token.  kv may be the sum of nsplit partial
-// buffers split_stride floats apart (a projection split over K), added in
-// split order.  Pass 1, one branch at a time, reduces sum k^2, sum h^2 and
-// sum h w_q w_k k over the branch's d columns (float4 loads, two per thread
-// in flight per split, then a fixed-order block reduction); pass 2 applies
-// hidden += g v with one BF16 rounding, all branches' loads of a column group
-// before its stores.  Image rows (c_t == DEAD) are left untouched.
-constexpr int kGateThreads = 512;
+// a5 standalone.  kv may be the sum of nsplit partial buffers split_stride
+// floats apart (a projection split over K), added in split order.
 constexpr int kGateMaxSplits = 8;
 
 __device__ __forceinline__ float4 kv_sum4(const float4* p, int nsplit, int64_t stride4) {
@@ -266,91 +260,88 @@ __device__ __forceinline__ float4 kv_sum4(const float4* p, int nsplit, int64_t s
 
 __device__ __forceinline__ float bf16_bits_to_f32(uint32_t b) { return __uint_as_float(b << 16); }
 
-__global__ void __launch_bounds__(kGateThreads, 2)
-k_gate(const float* __restrict__ kv, int nsplit, int64_t split_stride,
-       const uint4* __restrict__ windows, int64_t T, int hc, int d, float eps,
-       uint16_t* __restrict__ hidden, const float* __restrict__ wq,
-       const float* __restrict__ wk, float* __restrict__ gates) {
-    __shared__ float red[kGateThreads / 32][3];
-    __shared__ float gsh[8];
-    const int N = (hc + 1) * d;
+// One CTA per (token, branch b).  Pass 1 reduces sum k^2, sum h^2 and
+// sum h w_q w_k k over the branch's d columns (float4 loads, four per thread
+// in flight per split, then a fixed-order block reduction) into the gate;
+// pass 2 applies h_b += g_b v with one BF16 rounding.  The branches of a token
+// are separate CTAs (each reads v itself), so no pass waits on another branch
+// and a batch of T tokens gives T hc CTAs of two short passes each.  Image
+// rows (c_t == DEAD) are left untouched.
+constexpr int kGateBranchThreads = 256;
+
+__global__ void __launch_bounds__(kGateBranchThreads)
+k_gate_branch(const float* __restrict__ kv, int nsplit, int64_t split_stride,
+              const uint4* __restrict__ windows, int hc, int d, float eps,
+              uint16_t* __restrict__ hidden, const float* __restrict__ wq,
+              const float* __restrict__ wk, float* __restrict__ gates) {
+    __shared__ float red[kGateBranchThreads / 32][3];
+    __shared__ float gsh;
+    const int64_t t = blockIdx.x / hc;
+    const int b = (int)(blockIdx.x - t * hc);
+    if (windows[t].x == kDead) {
+        if (gates && threadIdx.x == 0) gates[t * hc + b] = 0.0f;
+        return;
+    }
     const int n4 = d / 4;
     const int64_t stride4 = split_stride / 4;
+    const float4* kvt = reinterpret_cast<const float4*>(kv + t * (int64_t)(hc + 1) * d);
+    const float4* kb = kvt + (int64_t)b * n4;
+    const float4* vb = kvt + (int64_t)hc * n4;
+    uint2* hb = reinterpret_cast<uint2*>(hidden + (t * hc + b) * (int64_t)d);
+    const float4* qb = reinterpret_cast<const float4*>(wq + (int64_t)b * d);
+    const float4* wb = reinterpret_cast<const float4*>(wk + (int64_t)b * d);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    for (int64_t t = blockIdx.x; t < T; t += gridDim.x) {
-        if (windows[t].x == kDead) {
-            if (gates && threadIdx.x < hc) gates[t * hc + threadIdx.x] = 0.0f;
-            continue;
+    float skk = 0.f, shh = 0.f, shk = 0.f;
+#pragma unroll 4
+    for (int i = threadIdx.x; i < n4; i += kGateBranchThreads) {
+        const float4 k = kv_sum4(kb + i, nsplit, stride4);
+        const uint2 h2 = hb[i];
+        const float4 q = __ldg(qb + i), w = __ldg(wb + i);
+        const float h[4] = {bf16_bits_to_f32(h2.x & 0xFFFFu), bf16_bits_to_f32(h2.x >> 16),
+                            bf16_bits_to_f32(h2.y & 0xFFFFu), bf16_bits_to_f32(h2.y >> 16)};
+        const float kk[4] = {k.x, k.y, k.z, k.w};
+        const float qw[4] = {q.x * w.x, q.y * w.y, q.z * w.z, q.w * w.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            skk += kk[e] * kk[e];
+            shh += h[e] * h[e];
+            shk += h[e] * qw[e] * kk[e];
         }
-        const float4* kvt = reinterpret_cast<const float4*>(kv + t * (int64_t)N);
-        uint16_t* ht = hidden + t * (int64_t)hc * d;
-        for (int b = 0; b < hc; ++b) {
-            const float4* kb = kvt + (int64_t)b * n4;
-            const uint2* hb = reinterpret_cast<const uint2*>(ht + (int64_t)b * d);
-            const float4* qb = reinterpret_cast<const float4*>(wq + (int64_t)b * d);
-            const float4* wb = reinterpret_cast<const float4*>(wk + (int64_t)b * d);
-            float skk = 0.f, shh = 0.f, shk = 0.f;
-#pragma unroll 2
-            for (int i = threadIdx.x; i < n4; i += kGateThreads) {
-                const float4 k = kv_sum4(kb + i, nsplit, stride4);
-                const uint2 h2 = hb[i];
-                const float4 q = __ldg(qb + i), w = __ldg(wb + i);
-                const float h[4] = {bf16_bits_to_f32(h2.x & 0xFFFFu), bf16_bits_to_f32(h2.x >> 16),
-                                    bf16_bits_to_f32(h2.y & 0xFFFFu), bf16_bits_to_f32(h2.y >> 16)};
-                const float kk[4] = {k.x, k.y, k.z, k.w};
-                const float qw[4] = {q.x * w.x, q.y * w.y, q.z * w.z, q.w * w.w};
+    }
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    skk += kk[e] * kk[e];
-                    shh += h[e] * h[e];
-                    shk += h[e] * qw[e] * kk[e];
-                }
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                skk += __shfl_xor_sync(0xFFFFFFFFu, skk, o);
-                shh += __shfl_xor_sync(0xFFFFFFFFu, shh, o);
-                shk += __shfl_xor_sync(0xFFFFFFFFu, shk, o);
-            }
-            if (lane == 0) {
-                red[warp][0] = skk;
-                red[warp][1] = shh;
-                red[warp][2] = shk;
-            }
-            __syncthreads();
-            if (threadIdx.x == 0) {
-                float a0 = 0.f, a1 = 0.f, a2 = 0.f;
-                for (int w = 0; w < kGateThreads / 32; ++w) {
-                    a0 += red[w][0];
-                    a1 += red[w][1];
-                    a2 += red[w][2];
-                }
-                const float g = gate_from_sums(a0, a1, a2, d, eps);
-                gsh[b] = g;
-                if (gates) gates[t * hc + b] = g;
-            }
-            __syncthreads();
+    for (int o = 16; o > 0; o >>= 1) {
+        skk += __shfl_xor_sync(0xFFFFFFFFu, skk, o);
+        shh += __shfl_xor_sync(0xFFFFFFFFu, shh, o);
+        shk += __shfl_xor_sync(0xFFFFFFFFu, shk, o);
+    }
+    if (lane == 0) {
+        red[warp][0] = skk;
+        red[warp][1] = shh;
+        red[warp][2] = shk;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float a0 = 0.f, a1 = 0.f, a2 = 0.f;
+        for (int w = 0; w < kGateBranchThreads / 32; ++w) {
+            a0 += red[w][0];
+            a1 += red[w][1];
+            a2 += red[w][2];
         }
-        const float4* v = kvt + (int64_t)hc * n4;
-        for (int i = threadIdx.x; i < n4; i += kGateThreads) {
-            const float4 vi = kv_sum4(v + i, nsplit, stride4);
-            uint2 h2[8];
-#pragma unroll
-            for (int b = 0; b < 8; ++b)
-                if (b < hc) h2[b] = reinterpret_cast<const uint2*>(ht + (int64_t)b * d)[i];
-#pragma unroll
-            for (int b = 0; b < 8; ++b)
-                if (b < hc) {
-                    const float g = gsh[b];
-                    const float o0 = fmaf(g, vi.x, bf16_bits_to_f32(h2[b].x & 0xFFFFu));
-                    const float o1 = fmaf(g, vi.y, bf16_bits_to_f32(h2[b].x >> 16));
-                    const float o2 = fmaf(g, vi.z, bf16_bits_to_f32(h2[b].y & 0xFFFFu));
-                    const float o3 = fmaf(g, vi.w, bf16_bits_to_f32(h2[b].y >> 16));
-                    reinterpret_cast<uint2*>(ht + (int64_t)b * d)[i] =
-                        make_uint2(bf16x2_pack_rn(o0, o1), bf16x2_pack_rn(o2, o3));
-                }
-        }
-        __syncthreads();
+        const float g = gate_from_sums(a0, a1, a2, d, eps);
+        gsh = g;
+        if (gates) gates[t * hc + b] = g;
+    }
+    __syncthreads();
+    const float g = gsh;
+#pragma unroll 4
+    for (int i = threadIdx.x; i < n4; i += kGateBranchThreads) {
+        const float4 vi = kv_sum4(vb + i, nsplit, stride4);
+        const uint2 h2 = hb[i];
+        const float o0 = fmaf(g, vi.x, bf16_bits_to_f32(h2.x & 0xFFFFu));
+        const float o1 = fmaf(g, vi.y, bf16_bits_to_f32(h2.x >> 16));
+        const float o2 = fmaf(g, vi.z, bf16_bits_to_f32(h2.y & 0xFFFFu));
+        const float o3 = fmaf(g, vi.w, bf16_bits_to_f32(h2.y >> 16));
+        hb[i] = make_uint2(bf16x2_pack_rn(o0, o1), bf16x2_pack_rn(o2, o3));
     }
 }
 
@@ -461,9 +452,9 @@ cudaError_t launch_gate(const Geometry& g, const float* kv, int nsplit, int64_t 
     if (T == 0) return cudaSuccess;
     if (nsplit < 1 || nsplit > kGateMaxSplits || g.d % 4 != 0 || g.hc > 8)
         return cudaErrorInvalidValue;
-    const int grid = (int)std::min<int64_t>(T, (int64_t)sm_count() * 16);
-    k_gate<<<grid, kGateThreads, 0, s>>>(kv, nsplit, split_stride, windows, T, g.hc, g.d, g.eps,
-                                         hidden, wq, wk, gates);
+    if (T * g.hc > INT32_MAX) return cudaErrorInvalidValue;
+    k_gate_branch<<<(unsigned)(T * g.hc), kGateBranchThreads, 0, s>>>(
+        kv, nsplit, split_stride, windows, g.hc, g.d, g.eps, hidden, wq, wk, gates);
     return cudaGetLastError();
 }
 

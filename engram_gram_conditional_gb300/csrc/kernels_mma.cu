@@ -185,6 +185,29 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
         "l"((uint64_t)map), "r"(bar), "r"(x), "r"(y)
         : "memory");
 }
+// The same two loads with an L2 cache policy (from createpolicy).
+__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                                 int x, int y, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+        "l"((uint64_t)map), "r"(bar), "r"(x), "r"(y), "l"(policy)
+        : "memory");
+}
+__device__ __forceinline__ void tma_load_2d_pair_hint(uint32_t dst, const CUtensorMap* map,
+                                                      uint32_t bar, int x, int y, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+        "l"((uint64_t)map), "r"(bar), "r"(x), "r"(y), "l"(policy)
+        : "memory");
+}
+// A policy that makes the lines it brings into L2 the first to be evicted.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
 __device__ __forceinline__ void fence_proxy_async() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -798,6 +821,11 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
         // TMA producers: warp 12 loads the wkv tiles, warp 14 the A tiles of
         // the TMA-fed variants, each running ahead on its own ring
         const bool do_b = warp == kWarpTma;
+        // with one M unit every wkv byte is read once per launch: its lines
+        // are marked for early eviction, so that they do not push the
+        // launch's outputs (the kv of a small batch) out of L2
+        const bool wkv_once = m_units == 1;
+        const uint64_t policy = l2_evict_first_policy();
         if (lane == 0) {
             int it = 0;
             bool ok = true;
@@ -829,15 +857,25 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
                             // rank) and signals the issuer, who expects both halves
                             const int r = n0 + (int)rank * (kBN / 2);
                             if (issuer) mbar_expect_tx(b_full(sb), 2 * L::kBStageBytes);
-                            tma_load_2d_pair(b_stage(sb), &tmB, map_rank(b_full(sb), 0), b_x(r), b_y(r));
+                            if (wkv_once)
+                                tma_load_2d_pair_hint(b_stage(sb), &tmB, map_rank(b_full(sb), 0),
+                                                      b_x(r), b_y(r), policy);
+                            else
+                                tma_load_2d_pair(b_stage(sb), &tmB, map_rank(b_full(sb), 0), b_x(r),
+                                                 b_y(r));
                         } else {
                             mbar_expect_tx(b_full(sb), L::kBStageBytes);
+                            auto load = [&](uint32_t dst, int x, int y) {
+                                if (wkv_once)
+                                    tma_load_2d_hint(dst, &tmB, b_full(sb), x, y, policy);
+                                else
+                                    tma_load_2d(dst, &tmB, b_full(sb), x, y);
+                            };
                             if (a.b_tiled) {  // two 128-row boxes, the second 16 KB further
-                                tma_load_2d(b_stage(sb), &tmB, b_full(sb), b_x(n0), b_y(n0));
-                                tma_load_2d(b_stage(sb) + kBStageHalf, &tmB, b_full(sb), b_x(n0 + 128),
-                                            b_y(n0 + 128));
+                                load(b_stage(sb), b_x(n0), b_y(n0));
+                                load(b_stage(sb) + kBStageHalf, b_x(n0 + 128), b_y(n0 + 128));
                             } else {
-                                tma_load_2d(b_stage(sb), &tmB, b_full(sb), kb * kBK, n0);
+                                load(b_stage(sb), kb * kBK, n0);
                             }
                         }
                     } else {
@@ -1092,20 +1130,46 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
             if (!holds_sum) {
                 // partial parked for the split that arrives last
             } else if (kMode == kEpiStoreKv) {
+                // A lane holds 32 columns of its own row.  An 8 x 8 transpose of
+                // float4 within each group of 8 lanes (three butterfly rounds of
+                // shuffles) gives lane 8 g + j the float4 j of rows 8 g .. 8 g + 7,
+                // so that each store writes four whole 128-byte row segments
+                // instead of 32 scattered 16-byte pieces.
+                const int g8 = lane & ~7, j8 = lane & 7;
+                float* const kv0 = a.kv + ks * a.kv_split_stride + n0 + j8 * 4;
+                const int64_t row0 = (int64_t)mb * kBM + q * 32 + g8;
 #pragma unroll 1
                 for (int c = 0; c < kBN / 32; ++c) {
                     uint32_t r[32];
                     tmem_ld32(taddr + (uint32_t)(c * 32), r);
                     tmem_wait_ld();
-                    if (t < a.T) {
-                        float4* dst = reinterpret_cast<float4*>(a.kv + ks * a.kv_split_stride +
-                                                                t * a.ldkv + n0 + c * 32);
+                    float v[32];
 #pragma unroll
-                        for (int i = 0; i < 8; ++i)
-                            dst[i] = make_float4(__uint_as_float(r[4 * i]) * a.out_scale,
-                                                 __uint_as_float(r[4 * i + 1]) * a.out_scale,
-                                                 __uint_as_float(r[4 * i + 2]) * a.out_scale,
-                                                 __uint_as_float(r[4 * i + 3]) * a.out_scale);
+                    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]) * a.out_scale;
+#pragma unroll
+                    for (int msk = 1; msk < 8; msk <<= 1) {
+                        const bool upper = (lane & msk) != 0;
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            if ((e & msk) == 0) {
+#pragma unroll
+                                for (int f = 0; f < 4; ++f) {
+                                    const float out = upper ? v[4 * e + f] : v[4 * (e ^ msk) + f];
+                                    const float in = __shfl_xor_sync(0xFFFFFFFFu, out, msk);
+                                    if (upper)
+                                        v[4 * e + f] = in;
+                                    else
+                                        v[4 * (e ^ msk) + f] = in;
+                                }
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int64_t tr = row0 + i;
+                        if (tr < a.T)
+                            *reinterpret_cast<float4*>(kv0 + tr * a.ldkv + c * 32) =
+                                make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
                     }
                 }
             } else if (kMode == kEpiForward && n0 < a.hc * a.d) {
