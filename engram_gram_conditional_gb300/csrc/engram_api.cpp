@@ -811,7 +811,27 @@ engram_status engram_forward(const engram_ctx* ctx, int layer, const uint32_t* d
 // the gate as its own kernel: the fused gate epilogue's loads wait behind the
 // wkv stream in the SM's memory pipeline, which a single wave of tiles cannot
 // hide, while the separate gate kernel has the whole GPU to itself.
-static int staged_splits(const engram_ctx* ctx, int64_t T) { return forward_k_splits(ctx, T, 8); }
+// A batch whose output tiles (128 tokens x 256 outputs) do not fill the GPU
+// twice runs the staged projection with stream K and the gate kernel after it.
+static bool staged_stream_k(const engram_ctx* ctx, int64_t T) {
+    const int64_t tiles = (T + kBM - 1) / kBM * (ctx->N / kBN);
+    return tiles < 2 * (int64_t)device_sm_count();
+}
+
+// Stream-K workspace after e: kv f32[T][N], then one 128 x 256 fp32 slot per
+// CTA, then sixteen ready flags per CTA (one per epilogue warp).
+struct StreamKWs {
+    size_t kv, slots, flags;
+    size_t total() const { return kv + slots + flags; }
+};
+static StreamKWs stream_k_ws(const engram_ctx* ctx, int64_t T) {
+    const size_t ctas = (size_t)device_sm_count();
+    StreamKWs w;
+    w.kv = ((size_t)T * ctx->N * sizeof(float) + 255) & ~(size_t)255;
+    w.slots = ctas * kBM * kBN * sizeof(float);
+    w.flags = (ctas * 16 * sizeof(uint32_t) + 255) & ~(size_t)255;
+    return w;
+}
 
 
 // Bytes of the staged operand matrix e: whole 128-token blocks (the FP16
@@ -824,9 +844,7 @@ static size_t staged_e_bytes(const engram_ctx* ctx, int64_t T) {
 size_t engram_forward_staged_workspace_bytes(const engram_ctx* ctx, int64_t T) {
     if (!ctx || T <= 0) return 0;
     const size_t e = staged_e_bytes(ctx, T);
-    const int splits = staged_splits(ctx, T);
-    if (splits > 1)
-        return e + (((size_t)splits * T * ctx->N * sizeof(float) + 255) & ~(size_t)255);
+    if (staged_stream_k(ctx, T)) return e + stream_k_ws(ctx, T).total();
     return e + forward_workspace_bytes(ctx, T, 8);
 }
 
@@ -873,12 +891,12 @@ engram_status engram_forward_staged_rows(const engram_ctx* ctx, int layer,
     a.n_tiles = ctx->N / kBN;
     cudaStream_t s = (cudaStream_t)stream;
     // the forward GEMM reading e through TMA.  FP16: e is tiled; on CTA pairs
-    // each TMA box holds two k-blocks (the split ranges are even), otherwise
-    // one; BF16: e is row-major [T][K]; pairs from two 128-token blocks on
-    const int splits = staged_splits(ctx, T);
+    // each TMA box holds two k-blocks, otherwise one; BF16: e is row-major
+    // [T][K]; pairs from two 128-token blocks on
+    const bool small = staged_stream_k(ctx, T);
     const int KB = ctx->K / kBK;
     // (a single 128-token block runs on one CTA per tile: half of a pair would idle)
-    const bool two_k = L.f16 && a.m_blocks >= 2 && (KB / splits) % 2 == 0 && KB % splits == 0;
+    const bool two_k = L.f16 && a.m_blocks >= 2 && KB % 2 == 0;
     CUtensorMap tmA;
     cudaError_t e;
     if (L.f16) {
@@ -893,17 +911,23 @@ engram_status engram_forward_staged_rows(const engram_ctx* ctx, int layer,
     const bool pairs = L.f16 ? two_k : a.m_blocks >= 2;
     const CUtensorMap& tmB = L.f16 ? (pairs ? L.tm_wkv_f16_2k : L.tm_wkv_f16)
                                    : (pairs ? L.tm_wkv_half : L.tm_wkv);
-    if (splits > 1) {
-        // small batch: split-K projection into per-split kv buffers, then the gate
-        a.k_splits = splits;
+    if (small) {
+        // small batch: stream-K projection into kv, then the gate
+        const StreamKWs w = stream_k_ws(ctx, T);
+        a.k_splits = 1;
         a.kv = reinterpret_cast<float*>(rest);
         a.ldkv = ctx->N;
-        a.kv_split_stride = T * (int64_t)ctx->N;
+        a.kv_split_stride = 0;
+        a.stream_k = 1;
+        a.sk_slots = reinterpret_cast<float*>(rest + w.kv);
+        a.sk_flags = reinterpret_cast<uint32_t*>(rest + w.kv + w.slots);
+        e = cudaMemsetAsync(a.sk_flags, 0, w.flags, s);
+        if (e != cudaSuccess) return cuda_fail(e, "stream-K flags");
         e = pairs ? launch_project_split_pair(a, L.f16, tmA, tmB, s)
                   : launch_project_split(a, L.f16, tmA, tmB, s);
-        if (e != cudaSuccess) return cuda_fail(e, "split projection launch");
-        e = launch_gate(geometry(ctx), a.kv, splits, a.kv_split_stride, a.windows, T, d_hidden,
-                        L.w.wq, L.w.wk, d_gates, s);
+        if (e != cudaSuccess) return cuda_fail(e, "stream-K projection launch");
+        e = launch_gate(geometry(ctx), a.kv, 1, 0, a.windows, T, d_hidden, L.w.wq, L.w.wk,
+                        d_gates, s);
         if (e != cudaSuccess) return cuda_fail(e, "gate launch");
         return ok();
     }

@@ -89,6 +89,15 @@ struct MmaArgs {
     float* split_partials;
     uint32_t* split_counters;
     float* gates;          // [T][hc] or null
+    // kEpiStoreKv with stream K (k_splits == 1): the (tile, stage) sequence of the
+    // launch is cut into one contiguous range per CTA (or pair); a tile that two
+    // ranges share is finished by the range holding its first stage, which adds
+    // the parked partials of the later ranges in order.  One 128 x 256 fp32 slot
+    // and sixteen ready flags (one per epilogue warp) per CTA, flags zeroed per
+    // call.
+    int stream_k;
+    float* sk_slots;
+    uint32_t* sk_flags;
     HashParams hp;
 };
 

@@ -29,7 +29,8 @@
 //               wkv as an exact FP16 copy scaled by a power of two), else BF16
 //               (decode through fp32)
 //   warps 8..11 epilogue, 168 registers: tcgen05.ld of the accumulator, then store kv
-//               (projection), or per-(token, branch, tile) sums of k^2, h^2
+//               (projection; with a TMA-fed A warps 0..11 share it, three warps
+//               per TMEM quadrant), or per-(token, branch, tile) sums of k^2, h^2
 //               and h w_q w_k k (key tiles), or gates from those sums and
 //               hidden += g v (value tiles) - kv never reaches HBM in the
 //               fused forward.
@@ -57,6 +58,13 @@ constexpr int kLaunchRegs = 128;
 constexpr int kRegsProd = 144, kRegsEpi = 168, kRegsCtl = 56;
 static_assert(kThreads * kLaunchRegs == 128 * (2 * kRegsProd + kRegsEpi + kRegsCtl),
               "setmaxnreg shares must add up to the launch allocation");
+// The TMA-fed kv-store kernels have no A producers: warps 0..11 all run the
+// epilogue, 152 registers each (3 x 152 + 56 = 512 per scheduler, as above).
+constexpr int kRegsWideEpi = 152;
+static_assert(kThreads * kLaunchRegs == 128 * (3 * kRegsWideEpi + kRegsCtl),
+              "setmaxnreg shares must add up to the launch allocation");
+// Ready flags per CTA of a stream-K launch: one per epilogue warp.
+constexpr int kSkFlagsPerCta = 16;
 constexpr int kAStage = kBM * kBK * 2;  // 16 KB
 constexpr int kBStage = kBN * kBK * 2;  // 32 KB
 constexpr int kRowStride = kMaxBuckets + 1;  // row-index table stride (odd: no bank conflicts)
@@ -95,8 +103,8 @@ template <int kASrc, int kKS = 1>
 struct Layout {
     static constexpr bool kPair = kASrc == kASrcTmaPair;
     // ring stages (each kKS k-blocks)
-    static constexpr int kA = kASrc == kASrcGatherBucket ? 8 : kKS == 2 ? 2 : 4;
-    static constexpr int kB = kASrc == kASrcGatherBucket ? 3 : kKS == 2 ? 4 : kPair ? 8 : 4;
+    static constexpr int kA = kASrc == kASrcGatherBucket ? 8 : kKS == 2 ? 3 : 4;
+    static constexpr int kB = kASrc == kASrcGatherBucket ? 3 : kKS == 2 ? 3 : kPair ? 8 : 4;
     static constexpr int kAStageBytes = kAStage * kKS;
     static constexpr int kBStageBytes = (kPair ? kBStageHalf : kBStage) * kKS;
     static constexpr int kOffA = 0;
@@ -735,6 +743,9 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
     constexpr int kA = L::kA, kB = L::kB;
     constexpr bool kPair = L::kPair;
     constexpr bool kFusedA = kASrc != kASrcTma && !kPair;
+    // without A producers, warps 0..7 join the kv-store epilogue
+    constexpr bool kWideEpi = !kFusedA && kMode == kEpiStoreKv;
+    constexpr int kEpiWarps = kWideEpi ? 12 : 4;
     // in a pair, the even CTA issues the MMAs; the odd one only feeds them
     const uint32_t rank = kPair ? cluster_ctarank() : 0u;
     const bool issuer = rank == 0u;
@@ -770,7 +781,7 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
         }
         for (int acc = 0; acc < 2; ++acc) {
             mbar_init(tfull(acc), 1u);
-            mbar_init(tempty(acc), kPair ? 8u : 4u);  // epilogue warps (of both CTAs)
+            mbar_init(tempty(acc), (kPair ? 2u : 1u) * kEpiWarps);  // epilogue warps (of both CTAs)
         }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -809,6 +820,39 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
     // same moment.  Gathered A operands come in order.
     auto k_rotation = [&](int nt, int nkb) { return kFusedA ? 0 : (nt * 13) % nkb; };
 
+    // Work items of this CTA (a pair shares them).  Without stream K: the
+    // (tile, split)s item0, item0 + istep, ...  With stream K: the pieces of
+    // this unit's contiguous range [g0, g1) of the launch's (tile, stage)
+    // sequence, one piece per tile the range touches.
+    const int nst_tile = KB / kKS;
+    const bool sk = kMode == kEpiStoreKv && a.stream_k != 0;
+    const int64_t sk_total = (int64_t)m_units * a.n_tiles * nst_tile;
+    auto sk_start = [&](int u) { return (int64_t)u * sk_total / istep; };
+    const int64_t sk_g0 = sk_start(item0), sk_g1 = sk_start(item0 + 1);
+    const int sk_j0 = (int)(sk_g0 / nst_tile);
+    const int n_items = sk ? (sk_g1 > sk_g0 ? (int)((sk_g1 - 1) / nst_tile) - sk_j0 + 1 : 0)
+                           : (item0 < total ? (total - item0 + istep - 1) / istep : 0);
+    // item i: output tile (mb, nt), split ks, k-blocks [kb_lo, kb_lo + nkb), and
+    // its stage range [st_lo, st_hi) within the tile's nst_tile stages
+    auto get_item = [&](int i, int& mb, int& nt, int& ks, int& kb_lo, int& nkb, int& st_lo,
+                        int& st_hi) {
+        if (sk) {
+            const int j = sk_j0 + i;
+            coords(j, mb, nt, ks);
+            const int64_t base = (int64_t)j * nst_tile;
+            st_lo = (int)(max(sk_g0, base) - base);
+            st_hi = (int)(min(sk_g1, base + nst_tile) - base);
+            kb_lo = st_lo * kKS;
+            nkb = (st_hi - st_lo) * kKS;
+        } else {
+            coords(item0 + i * istep, mb, nt, ks);
+            kb_lo = ks * KB / a.k_splits;
+            nkb = (ks + 1) * KB / a.k_splits - kb_lo;
+            st_lo = 0;
+            st_hi = nkb / kKS;
+        }
+    };
+
     auto fail = [&]() {
         *abort_flag = 1;
         atomicOr(a.err, kErrTimeout);
@@ -829,15 +873,14 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
         if (lane == 0) {
             int it = 0;
             bool ok = true;
-            for (int tile = item0; tile < total && ok; tile += istep) {
-                int mb, nt, ks;
-                coords(tile, mb, nt, ks);
+            for (int i = 0; i < n_items && ok; ++i) {
+                int mb, nt, ks, kb_lo, nkb, st_lo, st_hi;
+                get_item(i, mb, nt, ks, kb_lo, nkb, st_lo, st_hi);
                 const int n0 = (a.n_tile_begin + nt) * kBN;
                 // stages of kKS k-blocks (the host keeps every split's range a
-                // multiple of kKS)
-                const int kb_lo = ks * KB / a.k_splits, nkb = (ks + 1) * KB / a.k_splits - kb_lo;
+                // multiple of kKS); a stream-K piece walks its range in order
                 const int nst = nkb / kKS;
-                const int rot = k_rotation(nt, nst);
+                const int rot = sk ? 0 : k_rotation(nt, nst);
                 for (int j = 0; j < nst && !a.starve_b; ++j, ++it) {
                     const int kb = kb_lo + ((j + rot) % nst) * kKS;  // first k-block of the stage
                     const int sb = it % kB;
@@ -909,7 +952,7 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
         if (lane == 0 && issuer) {
             int it = 0, tc = 0;
             bool ok = true;
-            for (int tile = item0; tile < total && ok; tile += istep, ++tc) {
+            for (; tc < n_items && ok; ++tc) {
                 const int acc = tc & 1;
                 const uint32_t aph = (uint32_t)(tc >> 1) & 1u;
                 if (!wait(tempty(acc), aph ^ 1u)) {
@@ -918,9 +961,8 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * kBN);
-                int mb_, nt_, ks;
-                coords(tile, mb_, nt_, ks);
-                const int kb_lo = ks * KB / a.k_splits, nkb = (ks + 1) * KB / a.k_splits - kb_lo;
+                int mb_, nt_, ks, kb_lo, nkb, st_lo, st_hi;
+                get_item(tc, mb_, nt_, ks, kb_lo, nkb, st_lo, st_hi);
                 const int nst = nkb / kKS;
                 for (int j = 0; j < nst; ++j, ++it) {
                     const int sa = it % kA, sb = it % kB;
@@ -964,7 +1006,7 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
         }
     } else if (warp >= kWarpTma) {
         // warp 15 (and 14 with a gathered A): idle
-    } else if (warp < kWarpEpi) {
+    } else if (warp < kWarpEpi && !kWideEpi) {
         setmaxnreg_inc<kRegsProd>();
         if (kASrc == kASrcGatherBucket) {
             // whole-row gather; rows of this warp: [16 pw, 16 pw + 16); lanes
@@ -1087,8 +1129,16 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
         }
     } else {
         // ---- epilogue ----
-        setmaxnreg_inc<kRegsEpi>();
+        if constexpr (kWideEpi)
+            setmaxnreg_inc<kRegsWideEpi>();
+        else
+            setmaxnreg_inc<kRegsEpi>();
         const int q = warp & 3;  // TMEM lane quadrant this warp may read
+        // kv store: the warp's 32-column chunks (every third one when three
+        // warps share the quadrant) and its ready flag in a stream-K launch
+        const int c_first = kWideEpi ? warp >> 2 : 0;
+        constexpr int kCStep = kWideEpi ? 3 : 1;
+        const int eslot = kWideEpi ? warp : q;
         const int m = q * 32 + lane;
         int tc = 0;
         if (kMode == kEpiForward && item0 < total) {
@@ -1096,9 +1146,10 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
             coords(item0, mb, nt, ks);
             if (mb < a.m_blocks) prefetch_hidden(a, mb, nt, m);
         }
-        for (int tile = item0; tile < total; tile += istep, ++tc) {
-            int mb, nt, ks;
-            coords(tile, mb, nt, ks);
+        for (; tc < n_items; ++tc) {
+            const int tile = item0 + tc * istep;  // (without stream K)
+            int mb, nt, ks, kb_lo, nkb, st_lo, st_hi;
+            get_item(tc, mb, nt, ks, kb_lo, nkb, st_lo, st_hi);
             // the next tile's hidden slices travel to L2 while this one is finished
             if (kMode == kEpiForward && tile + istep < total) {
                 int mb2, nt2, ks2;
@@ -1129,7 +1180,60 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
             }
             if (!holds_sum) {
                 // partial parked for the split that arrives last
+            } else if (kMode == kEpiStoreKv && sk && st_lo > 0) {
+                // stream K, a piece after the tile's first: park the raw
+                // accumulator in this CTA's slot ([quadrant][chunk][float4][lane],
+                // 512 contiguous bytes per warp store) and raise the quadrant's flag
+                const int cta = (int)blockIdx.x;
+                float4* const slot = reinterpret_cast<float4*>(a.sk_slots) +
+                                     (int64_t)cta * (kBM * kBN / 4) + q * (kBN / 4) * 32 + lane;
+#pragma unroll 1
+                for (int c = c_first; c < kBN / 32; c += kCStep) {
+                    uint32_t r[32];
+                    tmem_ld32(taddr + (uint32_t)(c * 32), r);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        __stcg(slot + (c * 8 + i) * 32,
+                               make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
+                                           __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3])));
+                }
+                __threadfence();
+                __syncwarp();
+                if (lane == 0) st_release_u32(a.sk_flags + cta * kSkFlagsPerCta + eslot, 1u);
             } else if (kMode == kEpiStoreKv) {
+                // Stream K, the tile's first piece but not all of it: the later
+                // stages lie in the ranges of the next units (each holds one of
+                // them as its first piece, parked in its slot); wait (bounded) for
+                // those and add them in unit order, which is k order.
+                int u_last = item0;
+                if (sk && st_hi < nst_tile) {
+                    const int64_t g_end = (int64_t)(sk_j0 + tc) * nst_tile + nst_tile - 1;
+                    u_last = (int)(((g_end + 1) * istep - 1) / sk_total);
+                    int ready = 1;
+                    if (lane == 0) {
+                        const uint64_t t0 = globaltimer();
+                        for (int u = item0 + 1; u <= u_last && ready; ++u) {
+                            if (sk_start(u) == sk_start(u + 1)) continue;  // an empty range
+                            const uint32_t* f = a.sk_flags +
+                                                (kPair ? 2 * u + (int)rank : u) * kSkFlagsPerCta + eslot;
+                            uint32_t n = 0;
+                            while (ld_acquire_u32(f) == 0u) {
+                                if ((++n & 63u) == 0u &&
+                                    ((long long)(globaltimer() - t0) > lim || *abort_flag)) {
+                                    ready = 0;
+                                    break;
+                                }
+                            }
+                        }
+                    }
+                    ready = __shfl_sync(0xFFFFFFFFu, ready, 0);
+                    if (!ready) {
+                        if (lane == 0) fail();
+                        break;
+                    }
+                    __threadfence();
+                }
                 // A lane holds 32 columns of its own row.  An 8 x 8 transpose of
                 // float4 within each group of 8 lanes (three butterfly rounds of
                 // shuffles) gives lane 8 g + j the float4 j of rows 8 g .. 8 g + 7,
@@ -1139,13 +1243,30 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
                 float* const kv0 = a.kv + ks * a.kv_split_stride + n0 + j8 * 4;
                 const int64_t row0 = (int64_t)mb * kBM + q * 32 + g8;
 #pragma unroll 1
-                for (int c = 0; c < kBN / 32; ++c) {
+                for (int c = c_first; c < kBN / 32; c += kCStep) {
                     uint32_t r[32];
                     tmem_ld32(taddr + (uint32_t)(c * 32), r);
                     tmem_wait_ld();
                     float v[32];
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]) * a.out_scale;
+                    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+#pragma unroll 1
+                    for (int u = item0 + 1; u <= u_last; ++u) {
+                        if (sk_start(u) == sk_start(u + 1)) continue;
+                        const float4* src = reinterpret_cast<const float4*>(a.sk_slots) +
+                                            (int64_t)(kPair ? 2 * u + (int)rank : u) * (kBM * kBN / 4) +
+                                            q * (kBN / 4) * 32 + c * 8 * 32 + lane;
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const float4 x = __ldcg(src + i * 32);
+                            v[4 * i] += x.x;
+                            v[4 * i + 1] += x.y;
+                            v[4 * i + 2] += x.z;
+                            v[4 * i + 3] += x.w;
+                        }
+                    }
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] *= a.out_scale;
 #pragma unroll
                     for (int msk = 1; msk < 8; msk <<= 1) {
                         const bool upper = (lane & msk) != 0;
@@ -1373,10 +1494,16 @@ cudaError_t launch(const MmaArgs& a, const CUtensorMap& tmA, const CUtensorMap& 
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
+    // work units: the (tile, split)s, or with stream K the (tile, stage)s
+    constexpr int kKS = k_blocks_per_stage<kASrc, kF16>();
+    if (a.stream_k && (kMode != kEpiStoreKv || a.k_splits != 1 || (a.K / kBK) % kKS != 0))
+        return cudaErrorInvalidValue;
+    const int stages = a.stream_k ? (a.K / kBK) / kKS : a.k_splits;
     if (kASrc == kASrcTmaPair) {
         // clusters of two; no more pairs than can be resident at once, since
-        // the forward epilogue's tiles wait on tiles of other CTAs
-        const int units = (a.m_blocks + 1) / 2 * a.n_tiles * a.k_splits;
+        // the forward epilogue's tiles (and stream-K pieces) wait on tiles of
+        // other CTAs
+        const int units = (a.m_blocks + 1) / 2 * a.n_tiles * stages;
         if (units == 0) return cudaSuccess;
         cudaLaunchConfig_t cfg = {};
         cudaLaunchAttribute attr[1];
@@ -1397,7 +1524,7 @@ cudaError_t launch(const MmaArgs& a, const CUtensorMap& tmA, const CUtensorMap& 
         cfg.gridDim = dim3(2 * std::min(units, std::min(resident, device_sm_count() / 2)));
         return cudaLaunchKernelEx(&cfg, kern, tmA, tmB, a);
     }
-    const int total = a.m_blocks * a.n_tiles * a.k_splits;
+    const int total = a.m_blocks * a.n_tiles * stages;
     if (total == 0) return cudaSuccess;
     const int grid = std::min(total, device_sm_count());
     kern<<<grid, kThreads, kSmem, s>>>(tmA, tmB, a);

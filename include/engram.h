@@ -253,8 +253,14 @@ engram_status engram_forward(const engram_ctx* ctx, int layer, const uint32_t* d
  * operand read from e by TMA and the same gate epilogue (kv stays on chip).
  * Unlike engram_forward, the 6,144-vectors pass through device memory (an
  * L2-resident scratch of 12 KB per token for moderate T); in exchange each
- * table row is read once per call instead of once per output tile.  Small
- * batches split K as engram_forward does.
+ * table row is read once per call instead of once per output tile.  A batch
+ * whose output tiles (128 tokens x 256 outputs) do not fill the GPU twice
+ * (decode) runs step 2 as a stream-K projection into an fp32 kv [T][N] in
+ * the workspace, followed by the gate kernel of engram_gate: the launch's
+ * (tile, k-block) sequence is cut into one contiguous range per CTA (or CTA
+ * pair), and a tile that two ranges share is summed, in k order, by the range
+ * that holds its first k-block.  The result is deterministic on a given
+ * device (the ranges depend on its SM count).
  * d_workspace: engram_forward_staged_workspace_bytes(ctx, T) bytes. */
 size_t engram_forward_staged_workspace_bytes(const engram_ctx* ctx, int64_t T);
 engram_status engram_forward_staged(const engram_ctx* ctx, int layer, const uint32_t* d_windows,
