@@ -260,7 +260,8 @@ int forward_k_splits(const engram_ctx* ctx, int64_t T, int max_splits) {
     return 1;
 }
 
-// Workspace of the forward epilogue, in order: the gate sums [T][hc][d/kBN][3];
+// Workspace of the forward epilogue, in order: the gate sums
+// [T][hc][d/kBN][groups][3] (groups: the epilogue warps per TMEM quadrant);
 // the gates [T][hc]; the counters, zeroed by each call (per (M block, TMEM
 // quadrant) finished key tiles and a gates-ready flag, then with split K per
 // (M block, N tile, quadrant) arrivals and partials ready); with split K the
@@ -272,9 +273,9 @@ struct ForwardWs {
     size_t total() const { return part + gbuf + counters + slots; }
 };
 
-ForwardWs forward_ws(const engram_ctx* ctx, int64_t T, int max_splits) {
+ForwardWs forward_ws(const engram_ctx* ctx, int64_t T, int max_splits, int groups) {
     ForwardWs w{};
-    const size_t P = ctx->desc.d / kBN;
+    const size_t P = ctx->desc.d / kBN * (size_t)groups;
     const size_t mb = ((size_t)T + kBM - 1) / kBM, nt = ctx->N / kBN;
     w.splits = forward_k_splits(ctx, T, max_splits);
     w.part = ((size_t)T * ctx->desc.hc * P * 3 * sizeof(float) + 255) & ~(size_t)255;
@@ -285,16 +286,22 @@ ForwardWs forward_ws(const engram_ctx* ctx, int64_t T, int max_splits) {
     return w;
 }
 
-size_t forward_workspace_bytes(const engram_ctx* ctx, int64_t T, int max_splits) {
+size_t forward_workspace_bytes_groups(const engram_ctx* ctx, int64_t T, int max_splits,
+                                      int groups) {
     if (!ctx || T <= 0) return 0;
-    return forward_ws(ctx, T, max_splits).total();
+    return forward_ws(ctx, T, max_splits, groups).total();
+}
+// The fused kernels: one epilogue warp per TMEM quadrant.
+size_t forward_workspace_bytes(const engram_ctx* ctx, int64_t T, int max_splits) {
+    return forward_workspace_bytes_groups(ctx, T, max_splits, 1);
 }
 
 // Points the forward epilogue's fields of `a` into the workspace and zeroes
 // its counters on `s`.
-cudaError_t forward_bind_ws(const engram_ctx* ctx, int64_t T, int max_splits, void* ws,
-                            MmaArgs& a, cudaStream_t s) {
-    const ForwardWs w = forward_ws(ctx, T, max_splits);
+cudaError_t forward_bind_ws(const engram_ctx* ctx, int64_t T, int max_splits, int groups,
+                            void* ws, MmaArgs& a, cudaStream_t s) {
+    const ForwardWs w = forward_ws(ctx, T, max_splits, groups);
+    a.epi_groups = groups;
     char* base = static_cast<char*>(ws);
     a.partials = reinterpret_cast<float*>(base);
     a.gbuf = reinterpret_cast<float*>(base + w.part);
@@ -342,7 +349,7 @@ engram_status forward_fused(const engram_ctx* ctx, int layer, const uint32_t* d_
     a.n_tiles = ctx->N / kBN;
     // one launch: key tiles publish their sums and count in per M block; a
     // value tile's epilogue waits for its block's count before gating
-    cudaError_t e = forward_bind_ws(ctx, T, max_splits, d_workspace, a, (cudaStream_t)stream);
+    cudaError_t e = forward_bind_ws(ctx, T, max_splits, 1, d_workspace, a, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "forward counters");
     e = launch_forward_phase(a, kEpiForward, L.f16, L.bucket_gather, tmB, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "forward launch");
@@ -845,7 +852,8 @@ size_t engram_forward_staged_workspace_bytes(const engram_ctx* ctx, int64_t T) {
     if (!ctx || T <= 0) return 0;
     const size_t e = staged_e_bytes(ctx, T);
     if (staged_stream_k(ctx, T)) return e + stream_k_ws(ctx, T).total();
-    return e + forward_workspace_bytes(ctx, T, 8);
+    // the TMA-fed kernels run two epilogue warps per TMEM quadrant
+    return e + forward_workspace_bytes_groups(ctx, T, 8, 2);
 }
 
 engram_status engram_stage_rows(const engram_ctx* ctx, int layer, const uint32_t* d_windows,
@@ -931,7 +939,7 @@ engram_status engram_forward_staged_rows(const engram_ctx* ctx, int layer,
         if (e != cudaSuccess) return cuda_fail(e, "gate launch");
         return ok();
     }
-    e = forward_bind_ws(ctx, T, 8, rest, a, s);
+    e = forward_bind_ws(ctx, T, 8, 2, rest, a, s);
     if (e != cudaSuccess) return cuda_fail(e, "forward counters");
     e = pairs ? launch_forward_tma_pair(a, L.f16, tmA, tmB, s)
               : launch_forward_tma(a, L.f16, tmA, tmB, s);

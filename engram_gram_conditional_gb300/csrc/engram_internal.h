@@ -78,7 +78,8 @@ struct MmaArgs {
     uint16_t* hidden;      // [T][hc][d]
     const float* wq;       // [hc][d]
     const float* wk;       // [hc][d]
-    float* partials;       // [T][hc][d / kBN][3]
+    float* partials;       // [T][hc][d / kBN][epi_groups][3]
+    int epi_groups;        // kEpiForward: epilogue warps per TMEM quadrant (1, or 2 TMA-fed)
     float* gbuf;           // [T][hc] gates of the call
     // kEpiForward, per (M block, TMEM quadrant): finished key tiles, then a
     // gates-ready flag (zeroed per call)

@@ -29,11 +29,12 @@
 //               wkv as an exact FP16 copy scaled by a power of two), else BF16
 //               (decode through fp32)
 //   warps 8..11 epilogue, 168 registers: tcgen05.ld of the accumulator, then store kv
-//               (projection; with a TMA-fed A warps 0..11 share it, three warps
-//               per TMEM quadrant), or per-(token, branch, tile) sums of k^2, h^2
+//               (projection), or per-(token, branch, tile) sums of k^2, h^2
 //               and h w_q w_k k (key tiles), or gates from those sums and
 //               hidden += g v (value tiles) - kv never reaches HBM in the
-//               fused forward.
+//               fused forward.  With a TMA-fed A (no producers) warps 4..11
+//               run the epilogue, 216 registers, two per TMEM quadrant on
+//               alternate 32-column chunks; warps 0..3 idle.
 // Every mbarrier wait is bounded: on time-out the kernel raises an abort flag,
 // sets the error word and all roles leave their loops and free TMEM.
 #include <cudaTypedefs.h>
@@ -58,10 +59,11 @@ constexpr int kLaunchRegs = 128;
 constexpr int kRegsProd = 144, kRegsEpi = 168, kRegsCtl = 56;
 static_assert(kThreads * kLaunchRegs == 128 * (2 * kRegsProd + kRegsEpi + kRegsCtl),
               "setmaxnreg shares must add up to the launch allocation");
-// The TMA-fed kv-store kernels have no A producers: warps 0..11 all run the
-// epilogue, 152 registers each (3 x 152 + 56 = 512 per scheduler, as above).
-constexpr int kRegsWideEpi = 152;
-static_assert(kThreads * kLaunchRegs == 128 * (3 * kRegsWideEpi + kRegsCtl),
+// The TMA-fed kernels have no A producers: warps 4..11 all run the epilogue
+// with 216 registers each and warps 0..3 idle with 24 (24 + 2 x 216 + 56 =
+// 512 per scheduler, as above).
+constexpr int kRegsWideEpi = 216, kRegsIdle = 24;
+static_assert(kThreads * kLaunchRegs == 128 * (kRegsIdle + 2 * kRegsWideEpi + kRegsCtl),
               "setmaxnreg shares must add up to the launch allocation");
 // Ready flags per CTA of a stream-K launch: one per epilogue warp.
 constexpr int kSkFlagsPerCta = 16;
@@ -96,6 +98,14 @@ constexpr int kBStageHalf = kBStage / 2;  // 16 KB
 template <int kASrc, bool kF16>
 __host__ __device__ constexpr int k_blocks_per_stage() {
     return kASrc == kASrcTmaPair && kF16 ? 2 : 1;
+}
+
+// Epilogue warps per TMEM quadrant: the TMA-fed kernels have no A producers,
+// so warps 4..11 all run the epilogue, two per quadrant, each on every other
+// 32-column chunk of a tile.
+template <int kASrc>
+__host__ __device__ constexpr int epilogue_groups() {
+    return kASrc == kASrcTma || kASrc == kASrcTmaPair ? 2 : 1;
 }
 
 // Shared-memory layout of each variant.
@@ -539,10 +549,10 @@ __device__ __forceinline__ void prefetch_hidden(const MmaArgs& a, int mb, int nt
     }
 }
 
-// Gates of row t (every branch), from the per-(branch, column tile) sums the
-// key tiles published, added in tile order.
-__device__ __forceinline__ void row_gates(const MmaArgs& a, int64_t t, float (&g)[8]) {
-    const int P = a.d / kBN;
+// Gates of row t (every branch), from the per-(branch, column tile, epilogue
+// group) sums the key tiles published, added in (tile, group) order.
+__device__ __forceinline__ void row_gates(const MmaArgs& a, int64_t t, int groups, float (&g)[8]) {
+    const int P = a.d / kBN * groups;
 #pragma unroll
     for (int b = 0; b < 8; ++b) g[b] = 0.f;
     // one branch at a time (its loads all in flight), then the gate into its
@@ -743,9 +753,12 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
     constexpr int kA = L::kA, kB = L::kB;
     constexpr bool kPair = L::kPair;
     constexpr bool kFusedA = kASrc != kASrcTma && !kPair;
-    // without A producers, warps 0..7 join the kv-store epilogue
-    constexpr bool kWideEpi = !kFusedA && kMode == kEpiStoreKv;
-    constexpr int kEpiWarps = kWideEpi ? 12 : 4;
+    // without A producers, warps 0..7 join the epilogue
+    constexpr int kG = epilogue_groups<kASrc>();
+    constexpr bool kWideEpi = kG == 2;
+    static_assert(kWideEpi == !kFusedA, "the TMA-fed variants have the wide epilogue");
+    constexpr int kEpiWarps = 4 * kG;
+    constexpr int kFirstEpi = kWarpEpi - 4 * (kG - 1);  // first epilogue warp
     // in a pair, the even CTA issues the MMAs; the odd one only feeds them
     const uint32_t rank = kPair ? cluster_ctarank() : 0u;
     const bool issuer = rank == 0u;
@@ -1006,6 +1019,8 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
         }
     } else if (warp >= kWarpTma) {
         // warp 15 (and 14 with a gathered A): idle
+    } else if (kWideEpi && warp < kFirstEpi) {
+        setmaxnreg_dec<kRegsIdle>();  // warps 0..3 of a TMA-fed kernel: idle
     } else if (warp < kWarpEpi && !kWideEpi) {
         setmaxnreg_inc<kRegsProd>();
         if (kASrc == kASrcGatherBucket) {
@@ -1134,14 +1149,15 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
         else
             setmaxnreg_inc<kRegsEpi>();
         const int q = warp & 3;  // TMEM lane quadrant this warp may read
-        // kv store: the warp's 32-column chunks (every third one when three
-        // warps share the quadrant) and its ready flag in a stream-K launch
-        const int c_first = kWideEpi ? warp >> 2 : 0;
-        constexpr int kCStep = kWideEpi ? 3 : 1;
+        // the warp's group (of kG sharing the quadrant): its 32-column chunks
+        // are c_first, c_first + kG, ...; its ready flag in a stream-K launch
+        const int grp = (warp - kFirstEpi) >> 2;
+        const int c_first = grp;
+        constexpr int kCStep = kG;
         const int eslot = kWideEpi ? warp : q;
         const int m = q * 32 + lane;
         int tc = 0;
-        if (kMode == kEpiForward && item0 < total) {
+        if (kMode == kEpiForward && item0 < total && grp == 0) {
             int mb, nt, ks;
             coords(item0, mb, nt, ks);
             if (mb < a.m_blocks) prefetch_hidden(a, mb, nt, m);
@@ -1151,7 +1167,7 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
             int mb, nt, ks, kb_lo, nkb, st_lo, st_hi;
             get_item(tc, mb, nt, ks, kb_lo, nkb, st_lo, st_hi);
             // the next tile's hidden slices travel to L2 while this one is finished
-            if (kMode == kEpiForward && tile + istep < total) {
+            if (kMode == kEpiForward && tile + istep < total && grp == 0) {
                 int mb2, nt2, ks2;
                 coords(tile + istep, mb2, nt2, ks2);
                 if (mb2 < a.m_blocks) prefetch_hidden(a, mb2, nt2, m);
@@ -1302,7 +1318,7 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
                 const float* wkr = a.wk + (int64_t)branch * a.d + col0;
                 float skk = 0.f, shh = 0.f, shk = 0.f;
 #pragma unroll 1
-                for (int c = 0; c < kBN / 32; ++c) {
+                for (int c = c_first; c < kBN / 32; c += kCStep) {
                     uint32_t r[32];
                     tmem_ld32(taddr + (uint32_t)(c * 32), r);
                     uint4 hv[4];
@@ -1334,8 +1350,10 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
                     }
                 }
                 if (text) {
+                    // [token][branch][column tile][group][3]
                     const int P = a.d / kBN;
-                    float* pp = a.partials + ((t * a.hc + branch) * P + col0 / kBN) * 3;
+                    float* pp =
+                        a.partials + (((t * a.hc + branch) * P + col0 / kBN) * kG + grp) * 3;
                     pp[0] = skk;
                     pp[1] = shh;
                     pp[2] = shk;
@@ -1350,10 +1368,10 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
                     uint32_t done = 0;
                     if (lane == 0) done = atomicAdd(cnt, 1u) + 1u;
                     done = __shfl_sync(0xFFFFFFFFu, done, 0);
-                    if (done == (uint32_t)(a.hc * a.d / kBN)) {
+                    if (done == (uint32_t)(a.hc * a.d / kBN * kG)) {
                         __threadfence();
                         float g[8];
-                        if (text) row_gates(a, t, g);
+                        if (text) row_gates(a, t, kG, g);
                         if (t < a.T) {
                             for (int b = 0; b < a.hc; ++b) {
                                 const float gb = text ? g[b] : 0.f;
@@ -1406,7 +1424,7 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
                 // issued after it would each wait for memory in turn)
                 uint16_t* const hrow = a.hidden + t * a.hc * (int64_t)a.d + cv;
 #pragma unroll 1
-                for (int c = 0; c < kBN / 32; ++c) {
+                for (int c = c_first; c < kBN / 32; c += kCStep) {
                     uint32_t r[32];
                     tmem_ld32(taddr + (uint32_t)(c * 32), r);
                     tmem_wait_ld();
@@ -1498,6 +1516,7 @@ cudaError_t launch(const MmaArgs& a, const CUtensorMap& tmA, const CUtensorMap& 
     constexpr int kKS = k_blocks_per_stage<kASrc, kF16>();
     if (a.stream_k && (kMode != kEpiStoreKv || a.k_splits != 1 || (a.K / kBK) % kKS != 0))
         return cudaErrorInvalidValue;
+    if (kMode == kEpiForward && a.epi_groups != epilogue_groups<kASrc>()) return cudaErrorInvalidValue;
     const int stages = a.stream_k ? (a.K / kBK) / kKS : a.k_splits;
     if (kASrc == kASrcTmaPair) {
         // clusters of two; no more pairs than can be resident at once, since
