@@ -108,13 +108,19 @@ __host__ __device__ constexpr int epilogue_groups() {
     return kASrc == kASrcTma || kASrc == kASrcTmaPair ? 2 : 1;
 }
 
-// Shared-memory layout of each variant.
-template <int kASrc, int kKS = 1>
+// Shared-memory layout of each variant.  The FP16 pair kernel holds seven or
+// six stages of two k-blocks: with the kv-store epilogue (small batches, whose
+// launch streams wkv from HBM once) four of them wkv; with the forward
+// epilogue (compute-bound batches) three and three.
+template <int kASrc, int kKS = 1, int kMode = 0>
 struct Layout {
     static constexpr bool kPair = kASrc == kASrcTmaPair;
     // ring stages (each kKS k-blocks)
     static constexpr int kA = kASrc == kASrcGatherBucket ? 8 : kKS == 2 ? 3 : 4;
-    static constexpr int kB = kASrc == kASrcGatherBucket ? 3 : kKS == 2 ? 3 : kPair ? 8 : 4;
+    static constexpr int kB = kASrc == kASrcGatherBucket ? 3
+                              : kKS == 2                 ? (kMode == kEpiStoreKv ? 4 : 3)
+                              : kPair                    ? 8
+                                                         : 4;
     static constexpr int kAStageBytes = kAStage * kKS;
     static constexpr int kBStageBytes = (kPair ? kBStageHalf : kBStage) * kKS;
     static constexpr int kOffA = 0;
@@ -749,7 +755,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
       const __grid_constant__ MmaArgs a) {
     constexpr int kKS = k_blocks_per_stage<kASrc, kF16>();
-    using L = Layout<kASrc, kKS>;
+    using L = Layout<kASrc, kKS, kMode>;
     constexpr int kA = L::kA, kB = L::kB;
     constexpr bool kPair = L::kPair;
     constexpr bool kFusedA = kASrc != kASrcTma && !kPair;
@@ -1506,7 +1512,7 @@ cudaError_t launch(const MmaArgs& a, const CUtensorMap& tmA, const CUtensorMap& 
                    cudaStream_t s) {
     static bool attr_set = false;
     auto kern = k_mma<kASrc, kF16, kMode>;
-    constexpr int kSmem = Layout<kASrc, k_blocks_per_stage<kASrc, kF16>()>::kBytes;
+    constexpr int kSmem = Layout<kASrc, k_blocks_per_stage<kASrc, kF16>(), kMode>::kBytes;
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
         if (e != cudaSuccess) return e;
