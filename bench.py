@@ -34,6 +34,11 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 WORKLOAD = "prefill_2048"
+# DRAM bytes (read + write) of one launch of the staged forward GEMM
+# (k_mma, TMA-fed A on CTA pairs, gate epilogue) at 2,048 tokens, from one ncu
+# capture of that kernel (dram__bytes_read.sum 685.9 MB + dram__bytes_write.sum
+# 34.6 MB); the table size does not enter it.  Re-measure when the kernel changes.
+GEMM_DRAM_BYTES = 720.5e6
 FLOP_PER_TOKEN = None  # set from the geometry: 2 N K
 
 
@@ -50,6 +55,9 @@ def parse_args():
                     help="oracle tokens for cpu_baseline (0: skip)")
     ap.add_argument("--small", action="store_true",
                     help="profiling case: same kernels and batch, a 4.8M-row table, 2 batches")
+    ap.add_argument("--decode-small", action="store_true",
+                    help="profiling case of the decode step: 256 sessions, full wkv, a "
+                         "4.8M-row table; prints one line with its ms per step")
     return ap.parse_args()
 
 
@@ -263,6 +271,9 @@ def main():
     if args.impl == "reference":
         reference_arm(args, dist)
         return
+    if args.decode_small:
+        decode_small(args)
+        return
     import torch
 
     import engram_gram_conditional_gb300 as eg
@@ -393,7 +404,8 @@ def main():
         "config": dict(workload_config(w), table_rows=rows, parallelism=f"replicas x{dist.world}",
                        entry="engram_forward_staged"),
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16"],
-                     "unit": "TFLOP/s", "frac": achieved / peaks["bf16"], "traffic": None,
+                     "unit": "TFLOP/s", "frac": achieved / peaks["bf16"],
+                     "traffic": GEMM_DRAM_BYTES,
                      "kernel": "engram_forward_staged: k_gather_stage + k_mma (TMA-fed A, gate "
                                "epilogue); time per call covers both launches",
                      "peak_kind": f"bf16 dense burst, {peaks['src']}",
@@ -434,6 +446,52 @@ def main():
     if dist.rank == 0:
         print(json.dumps(line), flush=True)
     dist.close()
+
+
+def decode_small(args):
+    """The decode step's kernels at full geometry on a small table, for ncu:
+    256 sessions (3-token history), one token each per step, staged entry."""
+    import dataclasses
+
+    import torch
+
+    import engram_gram_conditional_gb300 as eg
+    import synth
+    from engram_gram_conditional_gb300 import build
+    from engram_gram_conditional_gb300.layer import EngramLayerSet
+
+    build.build()
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream()
+    wd = dataclasses.replace(synth.WORKLOADS["decode_256"], bucket_bases=[200_000])
+    tmap = synth.token_map(wd.vocab, wd.vc, wd.seed)
+    wq, wk = synth.wq_wk(wd)
+    dm = EngramLayerSet.from_workload(wd, tmap, device=dev)
+    dm.bind(0, wd.table_seeds[0], synth.wkv_bf16(wd), wq, wk)
+    S = wd.sessions
+    sess = [eg.engram_session_create(dm.ctx) for _ in range(S)]
+    streams = np.stack([synth.session_tokens(wd, i, wd.history + wd.steps) for i in range(S)])
+    for i, s in enumerate(sess):
+        eg.engram_session_append(s, streams[i, :wd.history])
+    wins = [eg.engram_batch_append(sess, streams[:, wd.history + k]) for k in range(wd.steps)]
+    d_wins = torch.from_numpy(np.stack(wins).view(np.int32)).to(dev)
+    d_h = torch.from_numpy(synth.normal_bf16((S, wd.hc, wd.d), 1.0, 0, 77).view(np.int16)).to(dev)
+    d_ws = torch.empty(eg.engram_forward_staged_workspace_bytes(dm.ctx, S), dtype=torch.uint8,
+                       device=dev)
+    sptr = stream.cuda_stream
+
+    def fwd(i):
+        eg.engram_forward_staged(dm.ctx, 0, d_wins[i % wd.steps], S, d_h, d_ws, None, sptr)
+
+    for i in range(args.warmup):
+        fwd(i)
+    ms = timed(fwd, args.steps, stream)
+    eg.engram_sync(dm.ctx, sptr)
+    print(json.dumps({"case": "decode_small", "sessions": S, "table_rows": dm.rows(0),
+                      "steps": args.steps, "ms_per_step": ms}), flush=True)
+    for s in sess:
+        eg.engram_session_destroy(s)
+    dm.close()
 
 
 def timed(fn, steps, stream):
