@@ -74,6 +74,18 @@ __device__ __forceinline__ uint32_t bf16x2_pack_rn(float lo, float hi) {
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 
+// Programmatic dependent launch.  A kernel launched with the
+// programmatic-serialisation attribute may start while the kernel before it in
+// the stream is still running, once every CTA of that kernel has called
+// pdl_launch_dependents (or exited); pdl_wait then blocks until that kernel
+// has finished and its writes are visible.  Every kernel launched this way
+// calls pdl_wait before it touches memory that earlier work in the stream
+// writes.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ float gate_from_sums(float s_kk, float s_hh, float s_hk, int d,
                                                 float eps) {
     // dot = <h rh w_q, k rk w_k> / sqrt(d); gate = sigmoid(copysign(sqrt(max(|dot|, 1e-6)), dot))

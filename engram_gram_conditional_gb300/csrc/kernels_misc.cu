@@ -175,6 +175,9 @@ __global__ void k_gather_stage(const __grid_constant__ HashParams hp, const uint
                                int64_t T, int row_dim, const uint8_t* __restrict__ table,
                                const uint8_t* __restrict__ scales, uint64_t nrows, int exp_shift,
                                int table_bf16, uint16_t* __restrict__ e, uint32_t* err) {
+    // the GEMM that reads e may start its prologue as soon as every CTA of
+    // this grid runs (it waits for this grid's end before reading e)
+    pdl_launch_dependents();
     const int lpr = row_dim / 16;              // lanes per row
     const int rpw = 32 / lpr;                  // rows per warp pass
     const int lane = threadIdx.x & 31;
@@ -276,6 +279,7 @@ k_gate_branch(const float* __restrict__ kv, int nsplit, int64_t split_stride,
               const float* __restrict__ wk, float* __restrict__ gates) {
     __shared__ float red[kGateBranchThreads / 32][3];
     __shared__ float gsh;
+    pdl_wait();  // launched to overlap the end of the projection that writes kv
     const int64_t t = blockIdx.x / hc;
     const int b = (int)(blockIdx.x - t * hc);
     if (windows[t].x == kDead) {
@@ -453,9 +457,19 @@ cudaError_t launch_gate(const Geometry& g, const float* kv, int nsplit, int64_t 
     if (nsplit < 1 || nsplit > kGateMaxSplits || g.d % 4 != 0 || g.hc > 8)
         return cudaErrorInvalidValue;
     if (T * g.hc > INT32_MAX) return cudaErrorInvalidValue;
-    k_gate_branch<<<(unsigned)(T * g.hc), kGateBranchThreads, 0, s>>>(
-        kv, nsplit, split_stride, windows, g.hc, g.d, g.eps, hidden, wq, wk, gates);
-    return cudaGetLastError();
+    // programmatic dependent launch: the CTAs are scheduled while the kernel
+    // before them drains, and wait for it in pdl_wait
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3((unsigned)(T * g.hc));
+    cfg.blockDim = dim3(kGateBranchThreads);
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k_gate_branch, kv, nsplit, split_stride, windows, g.hc, g.d,
+                              g.eps, hidden, wq, wk, gates);
 }
 
 cudaError_t launch_scale_range(const uint8_t* scales, uint64_t n, uint32_t* out, cudaStream_t s) {

@@ -820,6 +820,12 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
     if constexpr (kPair) cluster_sync();  // both CTAs' barriers exist before either signals the other
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // launched as a programmatic dependent: the prologue above may overlap the
+    // end of the kernel before; wait for it before touching memory.  The
+    // kernel after this one (the gate) may then be scheduled as CTAs of this
+    // one exit.
+    pdl_wait();
+    pdl_launch_dependents();
 
     // work items: (M unit, N tile, split); a CTA pair shares one item sequence
     // and its M unit is two M blocks, this CTA's being 2 mu + rank
@@ -1531,7 +1537,7 @@ cudaError_t launch(const MmaArgs& a, const CUtensorMap& tmA, const CUtensorMap& 
         const int units = (a.m_blocks + 1) / 2 * a.n_tiles * stages;
         if (units == 0) return cudaSuccess;
         cudaLaunchConfig_t cfg = {};
-        cudaLaunchAttribute attr[1];
+        cudaLaunchAttribute attr[2];
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = 2;
         attr[0].val.clusterDim.y = 1;
@@ -1547,13 +1553,25 @@ cudaError_t launch(const MmaArgs& a, const CUtensorMap& tmA, const CUtensorMap& 
         if (e != cudaSuccess) return e;
         if (resident < 1) return cudaErrorLaunchOutOfResources;
         cfg.gridDim = dim3(2 * std::min(units, std::min(resident, device_sm_count() / 2)));
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
+        cfg.numAttrs = 2;
         return cudaLaunchKernelEx(&cfg, kern, tmA, tmB, a);
     }
     const int total = a.m_blocks * a.n_tiles * stages;
     if (total == 0) return cudaSuccess;
-    const int grid = std::min(total, device_sm_count());
-    kern<<<grid, kThreads, kSmem, s>>>(tmA, tmB, a);
-    return cudaGetLastError();
+    // programmatic dependent launch (see pdl_wait)
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(std::min(total, device_sm_count()));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmem;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, tmA, tmB, a);
 }
 
 template <int kASrc, bool kF16>
