@@ -875,9 +875,29 @@ engram_status engram_stage_rows(const engram_ctx* ctx, int layer, const uint32_t
     return ok();
 }
 
+// Zeroes the stream-K ready flags of a small batch's workspace on `s`.
+static cudaError_t clear_stream_k_flags(const engram_ctx* ctx, int64_t T, void* d_workspace,
+                                        cudaStream_t s) {
+    const StreamKWs w = stream_k_ws(ctx, T);
+    char* flags = static_cast<char*>(d_workspace) + staged_e_bytes(ctx, T) + w.kv + w.slots;
+    return cudaMemsetAsync(flags, 0, w.flags, s);
+}
+
+// Step 2 of the staged forward; flags_clear: the stream-K flags of the
+// workspace were zeroed earlier on the stream (else this call zeroes them).
+static engram_status staged_rows(const engram_ctx* ctx, int layer, const uint32_t* d_windows,
+                                 int64_t T, uint16_t* d_hidden, void* d_workspace, float* d_gates,
+                                 void* stream, bool flags_clear);
+
 engram_status engram_forward_staged_rows(const engram_ctx* ctx, int layer,
                                          const uint32_t* d_windows, int64_t T, uint16_t* d_hidden,
                                          void* d_workspace, float* d_gates, void* stream) {
+    return staged_rows(ctx, layer, d_windows, T, d_hidden, d_workspace, d_gates, stream, false);
+}
+
+static engram_status staged_rows(const engram_ctx* ctx, int layer, const uint32_t* d_windows,
+                                 int64_t T, uint16_t* d_hidden, void* d_workspace, float* d_gates,
+                                 void* stream, bool flags_clear) {
     engram_status st = check_layer(ctx, layer, true);
     if (st || (st = check_T(T))) return st;
     if (T == 0) return ok();
@@ -929,8 +949,10 @@ engram_status engram_forward_staged_rows(const engram_ctx* ctx, int layer,
         a.stream_k = 1;
         a.sk_slots = reinterpret_cast<float*>(rest + w.kv);
         a.sk_flags = reinterpret_cast<uint32_t*>(rest + w.kv + w.slots);
-        e = cudaMemsetAsync(a.sk_flags, 0, w.flags, s);
-        if (e != cudaSuccess) return cuda_fail(e, "stream-K flags");
+        if (!flags_clear) {
+            e = cudaMemsetAsync(a.sk_flags, 0, w.flags, s);
+            if (e != cudaSuccess) return cuda_fail(e, "stream-K flags");
+        }
         e = pairs ? launch_project_split_pair(a, L.f16, tmA, tmB, s)
                   : launch_project_split(a, L.f16, tmA, tmB, s);
         if (e != cudaSuccess) return cuda_fail(e, "stream-K projection launch");
@@ -956,10 +978,16 @@ engram_status engram_forward_staged(const engram_ctx* ctx, int layer, const uint
     if (!d_windows || !d_hidden || !d_workspace || !aligned16(d_windows) || !aligned16(d_hidden) ||
         !aligned16(d_workspace))
         return fail(ENGRAM_EINVAL, "windows / hidden / workspace (16-byte aligned)");
+    // a small batch's flags are zeroed before the gather, so that nothing
+    // stands between the gather and the GEMM that it hands its rows to
+    const bool small = staged_stream_k(ctx, T);
+    if (small) {
+        cudaError_t e = clear_stream_k_flags(ctx, T, d_workspace, (cudaStream_t)stream);
+        if (e != cudaSuccess) return cuda_fail(e, "stream-K flags");
+    }
     st = engram_stage_rows(ctx, layer, d_windows, T, d_workspace, stream);
     if (st) return st;
-    return engram_forward_staged_rows(ctx, layer, d_windows, T, d_hidden, d_workspace, d_gates,
-                                      stream);
+    return staged_rows(ctx, layer, d_windows, T, d_hidden, d_workspace, d_gates, stream, small);
 }
 
 engram_status engram_project_windows(const engram_ctx* ctx, int layer, const uint32_t* d_windows,
