@@ -264,15 +264,17 @@ __device__ __forceinline__ float4 kv_sum4(const float4* p, int nsplit, int64_t s
 __device__ __forceinline__ float bf16_bits_to_f32(uint32_t b) { return __uint_as_float(b << 16); }
 
 // One CTA per (token, branch b).  Pass 1 reduces sum k^2, sum h^2 and
-// sum h w_q w_k k over the branch's d columns (float4 loads, four per thread
-// in flight per split, then a fixed-order block reduction) into the gate;
+// sum h w_q w_k k over the branch's d columns (float4 loads, then a
+// fixed-order block reduction) into the gate;
 // pass 2 applies h_b += g_b v with one BF16 rounding.  The branches of a token
 // are separate CTAs (each reads v itself), so no pass waits on another branch
 // and a batch of T tokens gives T hc CTAs of two short passes each.  Image
 // rows (c_t == DEAD) are left untouched.
 constexpr int kGateBranchThreads = 256;
 
-__global__ void __launch_bounds__(kGateBranchThreads)
+// Thirty-two registers a thread (eight CTAs per SM): latency is hidden by
+// resident CTAs rather than by loads in flight per thread.
+__global__ void __launch_bounds__(kGateBranchThreads, 8)
 k_gate_branch(const float* __restrict__ kv, int nsplit, int64_t split_stride,
               const uint4* __restrict__ windows, int hc, int d, float eps,
               uint16_t* __restrict__ hidden, const float* __restrict__ wq,
@@ -296,7 +298,7 @@ k_gate_branch(const float* __restrict__ kv, int nsplit, int64_t split_stride,
     const float4* wb = reinterpret_cast<const float4*>(wk + (int64_t)b * d);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     float skk = 0.f, shh = 0.f, shk = 0.f;
-#pragma unroll 4
+#pragma unroll 1
     for (int i = threadIdx.x; i < n4; i += kGateBranchThreads) {
         const float4 k = kv_sum4(kb + i, nsplit, stride4);
         const uint2 h2 = hb[i];
@@ -337,7 +339,7 @@ k_gate_branch(const float* __restrict__ kv, int nsplit, int64_t split_stride,
     }
     __syncthreads();
     const float g = gsh;
-#pragma unroll 4
+#pragma unroll 1
     for (int i = threadIdx.x; i < n4; i += kGateBranchThreads) {
         const float4 vi = kv_sum4(vb + i, nsplit, stride4);
         const uint2 h2 = hb[i];
