@@ -962,6 +962,10 @@ static engram_status staged_rows(const engram_ctx* ctx, int layer, const uint32_
         return ok();
     }
     e = forward_bind_ws(ctx, T, 8, 2, rest, a, s);
+    // the pair kernel finishes the key tiles M unit by M unit: a unit's value
+    // tiles then find their gates ready (2,048 tokens: 0.417 -> 0.399 ms);
+    // the fused kernel keeps the N-major order, which suits it better
+    a.key_tail = 8;
     if (e != cudaSuccess) return cuda_fail(e, "forward counters");
     e = pairs ? launch_forward_tma_pair(a, L.f16, tmA, tmB, s)
               : launch_forward_tma(a, L.f16, tmA, tmB, s);

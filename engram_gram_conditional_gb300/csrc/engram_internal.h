@@ -54,6 +54,8 @@ struct MmaArgs {
     int m_blocks;      // ceil(T / kBM)
     int group_m;       // tile rasterisation: M blocks (pair units) per group
     int key_tiles;     // kEpiForward: N tiles of the keys, ordered before the value tiles (else 0)
+    int key_tail;      // kEpiForward: the last key_tail key tiles and the value tiles of a
+                       // group run M-major (0: all N-major)
     int k_splits;      // split-K factor (>= 1); the tile list holds every (tile, split)
     int b_tiled;       // wkv map over 128 x 64 tiles (the FP16 copy), else row-major [N][K]
     int a_tiled;       // TMA-fed A in 128 x 64 tiles (the staged FP16 operand), else [T][K]

@@ -533,6 +533,19 @@ __device__ __forceinline__ void tile_coords(const MmaArgs& a, int m_units, int t
     const int first_m = g * a.group_m;
     const int gm = min(a.group_m, m_units - first_m);
     const int r = tile - g * per_group;
+    if (a.key_tiles > 0 && a.key_tail > 0) {
+        // the forward: the last key_tail key tiles of a group and all its value
+        // tiles run M-major, so that the M units get their gates one after
+        // the other and each unit's value tiles come after its gates
+        const int head = base_nt == 0 ? max(ntiles - a.key_tail, 0) : 0;  // N-major part
+        if (r >= head * gm) {
+            const int tail = ntiles - head;
+            const int rr = r - head * gm;
+            mb = first_m + rr / tail;
+            nt = base_nt + head + rr % tail;
+            return;
+        }
+    }
     nt = base_nt + r / gm;
     mb = first_m + (r - (r / gm) * gm);
 }
