@@ -494,6 +494,35 @@ def decode_small(args):
     dm.close()
 
 
+def prepass_staged(ctx, T, w, d_win, d_h, peaks, sptr, stream, steps):
+    """engram_prepass (staged: gather once, tcgen05 projection, kv to HBM) with
+    fp32 and with BF16 kv, and the gate on each at the layer entry."""
+    import torch
+
+    import engram_gram_conditional_gb300 as eg
+
+    ws = torch.empty(eg.engram_forward_staged_workspace_bytes(ctx, T), dtype=torch.uint8,
+                     device=d_win.device)
+    res = {"tokens": T}
+    for name, fmt, dt, gate in (("f32", eg.KV_F32, torch.float32, eg.engram_gate),
+                                ("bf16", eg.KV_BF16, torch.int16, eg.engram_gate_bf16kv)):
+        d_kv = torch.empty((T, w.N), dtype=dt, device=d_win.device)
+        for _ in range(3):
+            eg.engram_prepass(ctx, 0, d_win, T, d_kv, fmt, ws, sptr)
+            gate(ctx, 0, d_kv, d_win, T, d_h, None, sptr)
+        ms_p = timed(lambda i: eg.engram_prepass(ctx, 0, d_win, T, d_kv, fmt, ws, sptr), steps,
+                     stream)
+        ms_g = timed(lambda i: gate(ctx, 0, d_kv, d_win, T, d_h, None, sptr), steps, stream)
+        eg.engram_sync(ctx, sptr)
+        kv_bytes = T * w.N * d_kv.element_size()
+        gate_bytes = kv_bytes + T * 2 * w.hc * w.d * 2
+        res[name] = {"prepass_ms": ms_p, "layer_entry_gate_ms": ms_g, "kv_bytes": kv_bytes,
+                     "gate_GB_per_s": gate_bytes / ms_g / 1e6,
+                     "gate_frac": gate_bytes / ms_g / 1e6 / peaks["hbm"]}
+        del d_kv
+    return res
+
+
 def timed(fn, steps, stream):
     import torch
 
@@ -544,6 +573,7 @@ def extras(args, w, W, wq, wk, tmap, win0, d_win0, model, peaks, dev, sptr, stre
                       "kv_bytes": T * w.N * 4,
                       "gate_GB_per_s": gate_bytes / ms_g / 1e6,
                       "gate_frac": gate_bytes / ms_g / 1e6 / peaks["hbm"]}
+    out["prepass_staged"] = prepass_staged(ctx, T, w, d_win0, d_h, peaks, sptr, stream, 50)
     del d_rows, d_emb, d_kv, d_h
 
     # decode: 256 sessions x 1 token per step, 384M-row table resident in HBM
@@ -588,6 +618,8 @@ def extras(args, w, W, wq, wk, tmap, win0, d_win0, model, peaks, dev, sptr, stre
                                            sptr), wd.steps, stream)
     eg.engram_sync(dm.ctx, sptr)
     out["decode_prepass"] = {"sessions": S, "prepass_ms": ms_pwd, "layer_entry_gate_ms": ms_gd}
+    out["decode_prepass_staged"] = prepass_staged(dm.ctx, S, wd, d_wins[0], d_h, peaks, sptr,
+                                                  stream, wd.steps)
     del d_kvd
 
     # gather: unfused engram_gather_dequant over the 384M-row table, 50,032 tokens

@@ -35,7 +35,7 @@ EXPORTS = (
     "engram_workspace_bytes", "engram_hash", "engram_gather_dequant", "engram_project",
     "engram_gate", "engram_forward", "engram_forward_noalloc", "engram_forward_staged",
     "engram_forward_staged_workspace_bytes", "engram_stage_rows", "engram_forward_staged_rows",
-    "engram_project_windows",
+    "engram_project_windows", "engram_prepass", "engram_gate_bf16kv",
     "engram_sync", "engram_ctx_set_wait_limit", "engram_debug_starve_operand",
     "engram_last_error",
 )
@@ -59,6 +59,7 @@ class CtxDesc(C.Structure):
 
 BIND_BF16_OPERANDS = 1
 BIND_TABLE_BF16 = 2
+KV_F32, KV_BF16 = 0, 1  # engram_prepass: kv as fp32, or rounded once to BF16
 
 
 class LayerWeights(C.Structure):
@@ -109,6 +110,8 @@ def lib() -> C.CDLL:
             "engram_gate": [vp, C.c_int, vp, vp, i64, vp, vp, vp],
             "engram_forward": [vp, C.c_int, vp, i64, vp, vp, vp, vp],
             "engram_project_windows": [vp, C.c_int, vp, i64, vp, vp],
+            "engram_prepass": [vp, C.c_int, vp, i64, vp, C.c_int, vp, vp],
+            "engram_gate_bf16kv": [vp, C.c_int, vp, vp, i64, vp, vp, vp],
             "engram_forward_noalloc": [vp, C.c_int, vp, i64, vp, vp, vp],
             "engram_forward_staged": [vp, C.c_int, vp, i64, vp, vp, vp, vp],
             "engram_stage_rows": [vp, C.c_int, vp, i64, vp, vp],
@@ -325,6 +328,16 @@ def engram_forward_noalloc(ctx, layer, d_windows, T, d_hidden, d_gates=None, str
 def engram_project_windows(ctx, layer, d_windows, T, d_kv, stream=None):
     _check(lib().engram_project_windows(ctx, layer, _ptr(d_windows), T, _ptr(d_kv),
                                         _stream(stream)))
+
+
+def engram_prepass(ctx, layer, d_windows, T, d_kv, kv_format, d_workspace, stream=None):
+    _check(lib().engram_prepass(ctx, layer, _ptr(d_windows), T, _ptr(d_kv), int(kv_format),
+                                _ptr(d_workspace), _stream(stream)))
+
+
+def engram_gate_bf16kv(ctx, layer, d_kv, d_windows, T, d_hidden, d_gates=None, stream=None):
+    _check(lib().engram_gate_bf16kv(ctx, layer, _ptr(d_kv), _ptr(d_windows), T, _ptr(d_hidden),
+                                    _ptr(d_gates), _stream(stream)))
 
 
 def engram_ctx_set_wait_limit(ctx, ns: int):

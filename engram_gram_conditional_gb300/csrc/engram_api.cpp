@@ -800,8 +800,9 @@ engram_status engram_gate(const engram_ctx* ctx, int layer, const float* d_kv,
         !aligned16(d_hidden))
         return fail(ENGRAM_EINVAL, "kv / windows / hidden (16-byte aligned)");
     const LayerState& L = ctx->layers[layer];
-    cudaError_t e = launch_gate(geometry(ctx), d_kv, 1, 0, reinterpret_cast<const uint4*>(d_windows), T,
-                                d_hidden, L.w.wq, L.w.wk, d_gates, (cudaStream_t)stream);
+    cudaError_t e = launch_gate(geometry(ctx), d_kv, false, 1, 0,
+                                reinterpret_cast<const uint4*>(d_windows), T, d_hidden, L.w.wq,
+                                L.w.wk, d_gates, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "gate launch");
     return ok();
 }
@@ -875,6 +876,39 @@ engram_status engram_stage_rows(const engram_ctx* ctx, int layer, const uint32_t
     return ok();
 }
 
+// The GEMM of the staged entry reading e through TMA: `a` with the layer's
+// operand scaling, the A tensor map over e and the wkv map.  FP16: e is tiled;
+// on CTA pairs each TMA box holds two k-blocks, otherwise one; BF16: e is
+// row-major [T][K]; pairs from two 128-token blocks on (a single 128-token
+// block runs on one CTA per tile: half of a pair would idle).
+static cudaError_t staged_gemm(const engram_ctx* ctx, int layer, int64_t T, void* d_workspace,
+                               MmaArgs& a, CUtensorMap& tmA, const CUtensorMap*& tmB,
+                               bool& pairs) {
+    const LayerState& L = ctx->layers[layer];
+    uint16_t* e_scratch = static_cast<uint16_t*>(d_workspace);
+    a = mma_args(ctx, layer, T);
+    if (L.f16) {
+        a.a_exp_shift = L.a_exp_shift;
+        a.out_scale = ldexpf(1.0f, -(L.a_exp_shift + L.wkv_exp));
+    }
+    a.n_tile_begin = 0;
+    a.n_tiles = ctx->N / kBN;
+    const int KB = ctx->K / kBK;
+    const bool two_k = L.f16 && a.m_blocks >= 2 && KB % 2 == 0;
+    cudaError_t e;
+    if (L.f16) {
+        a.a_tiled = 1;
+        e = make_tma_16bit(&tmA, e_scratch, (uint64_t)a.m_blocks * KB * kBM, kBK,
+                           two_k ? 2 * kBM : kBM, true);
+    } else {
+        e = make_tma_16bit(&tmA, e_scratch, (uint64_t)T, (uint64_t)ctx->K, kBM, false);
+    }
+    // wkv: FP16 tiled (2-k-block boxes for pairs), or the caller's BF16
+    pairs = L.f16 ? two_k : a.m_blocks >= 2;
+    tmB = L.f16 ? (pairs ? &L.tm_wkv_f16_2k : &L.tm_wkv_f16) : (pairs ? &L.tm_wkv_half : &L.tm_wkv);
+    return e;
+}
+
 // Zeroes the stream-K ready flags of a small batch's workspace on `s`.
 static cudaError_t clear_stream_k_flags(const engram_ctx* ctx, int64_t T, void* d_workspace,
                                         cudaStream_t s) {
@@ -905,40 +939,19 @@ static engram_status staged_rows(const engram_ctx* ctx, int layer, const uint32_
         !aligned16(d_workspace))
         return fail(ENGRAM_EINVAL, "windows / hidden / workspace (16-byte aligned)");
     const LayerState& L = ctx->layers[layer];
-    uint16_t* e_scratch = static_cast<uint16_t*>(d_workspace);
     char* rest = static_cast<char*>(d_workspace) + staged_e_bytes(ctx, T);
-    MmaArgs a = mma_args(ctx, layer, T);
+    MmaArgs a;
+    CUtensorMap tmA;
+    const CUtensorMap* tmBp = nullptr;
+    bool pairs = false;
+    cudaError_t e = staged_gemm(ctx, layer, T, d_workspace, a, tmA, tmBp, pairs);
+    if (e != cudaSuccess) return cuda_fail(e, "e tensor map");
+    const CUtensorMap& tmB = *tmBp;
     a.windows = reinterpret_cast<const uint4*>(d_windows);
     a.hidden = d_hidden;
     a.gates = d_gates;
-    if (L.f16) {
-        a.a_exp_shift = L.a_exp_shift;
-        a.out_scale = ldexpf(1.0f, -(L.a_exp_shift + L.wkv_exp));
-    }
-    a.n_tile_begin = 0;
-    a.n_tiles = ctx->N / kBN;
     cudaStream_t s = (cudaStream_t)stream;
-    // the forward GEMM reading e through TMA.  FP16: e is tiled; on CTA pairs
-    // each TMA box holds two k-blocks, otherwise one; BF16: e is row-major
-    // [T][K]; pairs from two 128-token blocks on
     const bool small = staged_stream_k(ctx, T);
-    const int KB = ctx->K / kBK;
-    // (a single 128-token block runs on one CTA per tile: half of a pair would idle)
-    const bool two_k = L.f16 && a.m_blocks >= 2 && KB % 2 == 0;
-    CUtensorMap tmA;
-    cudaError_t e;
-    if (L.f16) {
-        a.a_tiled = 1;
-        e = make_tma_16bit(&tmA, e_scratch, (uint64_t)a.m_blocks * KB * kBM, kBK,
-                           two_k ? 2 * kBM : kBM, true);
-    } else {
-        e = make_tma_16bit(&tmA, e_scratch, (uint64_t)T, (uint64_t)ctx->K, kBM, false);
-    }
-    if (e != cudaSuccess) return cuda_fail(e, "e tensor map");
-    // wkv: FP16 tiled (2-k-block boxes for pairs), or the caller's BF16
-    const bool pairs = L.f16 ? two_k : a.m_blocks >= 2;
-    const CUtensorMap& tmB = L.f16 ? (pairs ? L.tm_wkv_f16_2k : L.tm_wkv_f16)
-                                   : (pairs ? L.tm_wkv_half : L.tm_wkv);
     if (small) {
         // small batch: stream-K projection into kv, then the gate
         const StreamKWs w = stream_k_ws(ctx, T);
@@ -956,7 +969,7 @@ static engram_status staged_rows(const engram_ctx* ctx, int layer, const uint32_
         e = pairs ? launch_project_split_pair(a, L.f16, tmA, tmB, s)
                   : launch_project_split(a, L.f16, tmA, tmB, s);
         if (e != cudaSuccess) return cuda_fail(e, "stream-K projection launch");
-        e = launch_gate(geometry(ctx), a.kv, 1, 0, a.windows, T, d_hidden, L.w.wq, L.w.wk,
+        e = launch_gate(geometry(ctx), a.kv, false, 1, 0, a.windows, T, d_hidden, L.w.wq, L.w.wk,
                         d_gates, s);
         if (e != cudaSuccess) return cuda_fail(e, "gate launch");
         return ok();
@@ -992,6 +1005,68 @@ engram_status engram_forward_staged(const engram_ctx* ctx, int layer, const uint
     st = engram_stage_rows(ctx, layer, d_windows, T, d_workspace, stream);
     if (st) return st;
     return staged_rows(ctx, layer, d_windows, T, d_hidden, d_workspace, d_gates, stream, small);
+}
+
+engram_status engram_prepass(const engram_ctx* ctx, int layer, const uint32_t* d_windows, int64_t T,
+                             void* d_kv, int kv_format, void* d_workspace, void* stream) {
+    engram_status st = check_layer(ctx, layer, true);
+    if (st || (st = check_T(T))) return st;
+    if (kv_format != ENGRAM_KV_F32 && kv_format != ENGRAM_KV_BF16)
+        return fail(ENGRAM_EINVAL, "kv_format must be ENGRAM_KV_F32 or ENGRAM_KV_BF16");
+    if (T == 0) return ok();
+    if (!d_windows || !d_kv || !d_workspace || !aligned16(d_windows) || !aligned16(d_kv) ||
+        !aligned16(d_workspace))
+        return fail(ENGRAM_EINVAL, "windows / kv / workspace (16-byte aligned)");
+    cudaStream_t s = (cudaStream_t)stream;
+    const bool small = staged_stream_k(ctx, T);
+    cudaError_t e;
+    if (small) {  // zeroed before the gather, as in engram_forward_staged
+        e = clear_stream_k_flags(ctx, T, d_workspace, s);
+        if (e != cudaSuccess) return cuda_fail(e, "stream-K flags");
+    }
+    st = engram_stage_rows(ctx, layer, d_windows, T, d_workspace, stream);
+    if (st) return st;
+    const LayerState& L = ctx->layers[layer];
+    MmaArgs a;
+    CUtensorMap tmA;
+    const CUtensorMap* tmB = nullptr;
+    bool pairs = false;
+    e = staged_gemm(ctx, layer, T, d_workspace, a, tmA, tmB, pairs);
+    if (e != cudaSuccess) return cuda_fail(e, "e tensor map");
+    a.windows = reinterpret_cast<const uint4*>(d_windows);
+    a.kv = static_cast<float*>(d_kv);
+    a.ldkv = ctx->N;
+    a.kv_bf16 = kv_format == ENGRAM_KV_BF16 ? 1 : 0;
+    a.k_splits = 1;
+    a.kv_split_stride = 0;
+    if (small) {
+        const StreamKWs w = stream_k_ws(ctx, T);
+        char* rest = static_cast<char*>(d_workspace) + staged_e_bytes(ctx, T);
+        a.stream_k = 1;
+        a.sk_slots = reinterpret_cast<float*>(rest + w.kv);
+        a.sk_flags = reinterpret_cast<uint32_t*>(rest + w.kv + w.slots);
+    }
+    e = pairs ? launch_project_split_pair(a, L.f16, tmA, *tmB, s)
+              : launch_project_split(a, L.f16, tmA, *tmB, s);
+    if (e != cudaSuccess) return cuda_fail(e, "pre-pass projection launch");
+    return ok();
+}
+
+engram_status engram_gate_bf16kv(const engram_ctx* ctx, int layer, const uint16_t* d_kv,
+                                 const uint32_t* d_windows, int64_t T, uint16_t* d_hidden,
+                                 float* d_gates, void* stream) {
+    engram_status st = check_layer(ctx, layer, true);
+    if (st || (st = check_T(T))) return st;
+    if (T == 0) return ok();
+    if (!d_kv || !d_windows || !d_hidden || !aligned16(d_kv) || !aligned16(d_windows) ||
+        !aligned16(d_hidden))
+        return fail(ENGRAM_EINVAL, "kv / windows / hidden (16-byte aligned)");
+    const LayerState& L = ctx->layers[layer];
+    cudaError_t e = launch_gate(geometry(ctx), d_kv, true, 1, 0,
+                                reinterpret_cast<const uint4*>(d_windows), T, d_hidden, L.w.wq,
+                                L.w.wk, d_gates, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "gate launch");
+    return ok();
 }
 
 engram_status engram_project_windows(const engram_ctx* ctx, int layer, const uint32_t* d_windows,

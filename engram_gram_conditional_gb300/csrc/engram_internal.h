@@ -54,8 +54,8 @@ struct MmaArgs {
     int m_blocks;      // ceil(T / kBM)
     int group_m;       // tile rasterisation: M blocks (pair units) per group
     int key_tiles;     // kEpiForward: N tiles of the keys, ordered before the value tiles (else 0)
-    int key_tail;      // kEpiForward: the last key_tail key tiles and the value tiles of a
-                       // group run M-major (0: all N-major)
+    int key_tail;      // kEpiForward, one group of M units: the last key_tail key tiles and
+                       // the value tiles run M-major (0: all N-major)
     int k_splits;      // split-K factor (>= 1); the tile list holds every (tile, split)
     int b_tiled;       // wkv map over 128 x 64 tiles (the FP16 copy), else row-major [N][K]
     int a_tiled;       // TMA-fed A in 128 x 64 tiles (the staged FP16 operand), else [T][K]
@@ -75,7 +75,8 @@ struct MmaArgs {
     int a_exp_shift;       // FP16 operands: decoded value x 2^(scale - 127 + a_exp_shift)
     float out_scale;       // accumulator x out_scale = kv (undoes the operand scaling)
     // epilogue
-    float* kv;             // kEpiStoreKv: [T][ldkv]
+    float* kv;             // kEpiStoreKv: [T][ldkv] fp32, or BF16 when kv_bf16
+    int kv_bf16;           // kEpiStoreKv: store kv rounded once to BF16 (no split buffers)
     int64_t ldkv;
     uint16_t* hidden;      // [T][hc][d]
     const float* wq;       // [hc][d]
@@ -116,11 +117,12 @@ cudaError_t launch_hash(const HashParams& hp, const uint4* windows, int64_t T, u
 cudaError_t launch_gather(const Geometry& g, const uint32_t* rows, int64_t T,
                           const uint8_t* table, const uint8_t* scales, uint64_t nrows,
                           bool table_bf16, uint16_t* emb, uint32_t* err, cudaStream_t s);
-// kv may be the sum of nsplit (<= 8) partial buffers, split_stride floats
-// apart, added in split order.  kv, hidden, wq and wk 16-byte aligned.
-cudaError_t launch_gate(const Geometry& g, const float* kv, int nsplit, int64_t split_stride,
-                        const uint4* windows, int64_t T, uint16_t* hidden, const float* wq,
-                        const float* wk, float* gates, cudaStream_t s);
+// kv: fp32 [T][N], possibly the sum of nsplit (<= 8) partial buffers
+// split_stride floats apart, added in split order; or BF16 [T][N] (kv_bf16,
+// nsplit 1).  kv, hidden, wq and wk 16-byte aligned.
+cudaError_t launch_gate(const Geometry& g, const void* kv, bool kv_bf16, int nsplit,
+                        int64_t split_stride, const uint4* windows, int64_t T, uint16_t* hidden,
+                        const float* wq, const float* wk, float* gates, cudaStream_t s);
 // Bind-time scans: out[0] = min, out[1] = max of n E8M0 bytes (out preset by
 // the caller to 255 / 0); out[2] = largest |x| of n BF16 values as its bit
 // pattern without the sign (out[2] preset to 0).

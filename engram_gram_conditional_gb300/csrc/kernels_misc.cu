@@ -263,6 +263,19 @@ __device__ __forceinline__ float4 kv_sum4(const float4* p, int nsplit, int64_t s
 
 __device__ __forceinline__ float bf16_bits_to_f32(uint32_t b) { return __uint_as_float(b << 16); }
 
+// Four kv values at float4 index i of a row: fp32 (the sum of nsplit split
+// buffers, stride4 float4 apart), or BF16 (a single buffer).
+template <bool kBf16>
+__device__ __forceinline__ float4 kv_load4(const void* row, int64_t i, int nsplit, int64_t stride4) {
+    if constexpr (kBf16) {
+        const uint2 u = __ldcg(reinterpret_cast<const uint2*>(row) + i);
+        return make_float4(bf16_bits_to_f32(u.x & 0xFFFFu), bf16_bits_to_f32(u.x >> 16),
+                           bf16_bits_to_f32(u.y & 0xFFFFu), bf16_bits_to_f32(u.y >> 16));
+    } else {
+        return kv_sum4(reinterpret_cast<const float4*>(row) + i, nsplit, stride4);
+    }
+}
+
 // One CTA per (token, branch b).  Pass 1 reduces sum k^2, sum h^2 and
 // sum h w_q w_k k over the branch's d columns (float4 loads, then a
 // fixed-order block reduction) into the gate;
@@ -273,9 +286,11 @@ __device__ __forceinline__ float bf16_bits_to_f32(uint32_t b) { return __uint_as
 constexpr int kGateBranchThreads = 256;
 
 // Thirty-two registers a thread (eight CTAs per SM): latency is hidden by
-// resident CTAs rather than by loads in flight per thread.
+// resident CTAs rather than by loads in flight per thread.  kv is fp32, or
+// BF16 (kBf16Kv: the pre-pass's rounded kv).
+template <bool kBf16Kv>
 __global__ void __launch_bounds__(kGateBranchThreads, 8)
-k_gate_branch(const float* __restrict__ kv, int nsplit, int64_t split_stride,
+k_gate_branch(const void* __restrict__ kv, int nsplit, int64_t split_stride,
               const uint4* __restrict__ windows, int hc, int d, float eps,
               uint16_t* __restrict__ hidden, const float* __restrict__ wq,
               const float* __restrict__ wk, float* __restrict__ gates) {
@@ -290,9 +305,10 @@ k_gate_branch(const float* __restrict__ kv, int nsplit, int64_t split_stride,
     }
     const int n4 = d / 4;
     const int64_t stride4 = split_stride / 4;
-    const float4* kvt = reinterpret_cast<const float4*>(kv + t * (int64_t)(hc + 1) * d);
-    const float4* kb = kvt + (int64_t)b * n4;
-    const float4* vb = kvt + (int64_t)hc * n4;
+    const size_t kv_elem = kBf16Kv ? 2 : 4;
+    const char* kvt = static_cast<const char*>(kv) + t * (int64_t)(hc + 1) * d * kv_elem;
+    const char* kb = kvt + (int64_t)b * d * kv_elem;
+    const char* vb = kvt + (int64_t)hc * d * kv_elem;
     uint2* hb = reinterpret_cast<uint2*>(hidden + (t * hc + b) * (int64_t)d);
     const float4* qb = reinterpret_cast<const float4*>(wq + (int64_t)b * d);
     const float4* wb = reinterpret_cast<const float4*>(wk + (int64_t)b * d);
@@ -300,7 +316,7 @@ k_gate_branch(const float* __restrict__ kv, int nsplit, int64_t split_stride,
     float skk = 0.f, shh = 0.f, shk = 0.f;
 #pragma unroll 1
     for (int i = threadIdx.x; i < n4; i += kGateBranchThreads) {
-        const float4 k = kv_sum4(kb + i, nsplit, stride4);
+        const float4 k = kv_load4<kBf16Kv>(kb, i, nsplit, stride4);
         const uint2 h2 = hb[i];
         const float4 q = __ldg(qb + i), w = __ldg(wb + i);
         const float h[4] = {bf16_bits_to_f32(h2.x & 0xFFFFu), bf16_bits_to_f32(h2.x >> 16),
@@ -341,7 +357,7 @@ k_gate_branch(const float* __restrict__ kv, int nsplit, int64_t split_stride,
     const float g = gsh;
 #pragma unroll 1
     for (int i = threadIdx.x; i < n4; i += kGateBranchThreads) {
-        const float4 vi = kv_sum4(vb + i, nsplit, stride4);
+        const float4 vi = kv_load4<kBf16Kv>(vb, i, nsplit, stride4);
         const uint2 h2 = hb[i];
         const float o0 = fmaf(g, vi.x, bf16_bits_to_f32(h2.x & 0xFFFFu));
         const float o1 = fmaf(g, vi.y, bf16_bits_to_f32(h2.x >> 16));
@@ -452,11 +468,11 @@ cudaError_t launch_gather(const Geometry& g, const uint32_t* rows, int64_t T,
     return cudaGetLastError();
 }
 
-cudaError_t launch_gate(const Geometry& g, const float* kv, int nsplit, int64_t split_stride,
-                        const uint4* windows, int64_t T, uint16_t* hidden, const float* wq,
-                        const float* wk, float* gates, cudaStream_t s) {
+cudaError_t launch_gate(const Geometry& g, const void* kv, bool kv_bf16, int nsplit,
+                        int64_t split_stride, const uint4* windows, int64_t T, uint16_t* hidden,
+                        const float* wq, const float* wk, float* gates, cudaStream_t s) {
     if (T == 0) return cudaSuccess;
-    if (nsplit < 1 || nsplit > kGateMaxSplits || g.d % 4 != 0 || g.hc > 8)
+    if (nsplit < 1 || nsplit > kGateMaxSplits || g.d % 4 != 0 || g.hc > 8 || (kv_bf16 && nsplit != 1))
         return cudaErrorInvalidValue;
     if (T * g.hc > INT32_MAX) return cudaErrorInvalidValue;
     // programmatic dependent launch: the CTAs are scheduled while the kernel
@@ -470,8 +486,11 @@ cudaError_t launch_gate(const Geometry& g, const float* kv, int nsplit, int64_t 
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, k_gate_branch, kv, nsplit, split_stride, windows, g.hc, g.d,
-                              g.eps, hidden, wq, wk, gates);
+    if (kv_bf16)
+        return cudaLaunchKernelEx(&cfg, k_gate_branch<true>, kv, nsplit, split_stride, windows,
+                                  g.hc, g.d, g.eps, hidden, wq, wk, gates);
+    return cudaLaunchKernelEx(&cfg, k_gate_branch<false>, kv, nsplit, split_stride, windows, g.hc,
+                              g.d, g.eps, hidden, wq, wk, gates);
 }
 
 cudaError_t launch_scale_range(const uint8_t* scales, uint64_t n, uint32_t* out, cudaStream_t s) {

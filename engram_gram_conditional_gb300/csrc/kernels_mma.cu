@@ -533,10 +533,13 @@ __device__ __forceinline__ void tile_coords(const MmaArgs& a, int m_units, int t
     const int first_m = g * a.group_m;
     const int gm = min(a.group_m, m_units - first_m);
     const int r = tile - g * per_group;
-    if (a.key_tiles > 0 && a.key_tail > 0) {
-        // the forward: the last key_tail key tiles of a group and all its value
+    if (a.key_tiles > 0 && a.key_tail > 0 && m_units <= a.group_m) {
+        // the forward in one group: the last key_tail key tiles and all value
         // tiles run M-major, so that the M units get their gates one after
-        // the other and each unit's value tiles come after its gates
+        // the other and each unit's value tiles come after its gates.  (With
+        // several groups the first value tiles are those of group 0, whose
+        // gates are long done, and M-major value tiles would spread each wkv
+        // value tile over a whole group's worth of time.)
         const int head = base_nt == 0 ? max(ntiles - a.key_tail, 0) : 0;  // N-major part
         if (r >= head * gm) {
             const int tail = ntiles - head;
@@ -1308,6 +1311,45 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
                     }
 #pragma unroll
                     for (int i = 0; i < 32; ++i) v[i] *= a.out_scale;
+                    if (a.kv_bf16) {
+                        // kv rounded once to BF16: the lane's 64 bytes are four
+                        // 16-byte pieces; a 4 x 4 transpose within each group of 4
+                        // lanes gives lane 4 g + j piece j of rows 4 g .. 4 g + 3,
+                        // so that each store writes eight whole 64-byte segments
+                        uint32_t o[4][4];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+#pragma unroll
+                            for (int e2 = 0; e2 < 4; ++e2)
+                                o[i][e2] = bf16x2_pack_rn(v[8 * i + 2 * e2], v[8 * i + 2 * e2 + 1]);
+#pragma unroll
+                        for (int msk = 1; msk < 4; msk <<= 1) {
+                            const bool upper = (lane & msk) != 0;
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                if ((e & msk) == 0) {
+#pragma unroll
+                                    for (int f = 0; f < 4; ++f) {
+                                        const uint32_t out = upper ? o[e][f] : o[e ^ msk][f];
+                                        const uint32_t in = __shfl_xor_sync(0xFFFFFFFFu, out, msk);
+                                        if (upper)
+                                            o[e][f] = in;
+                                        else
+                                            o[e ^ msk][f] = in;
+                                    }
+                                }
+                            }
+                        }
+                        const int64_t row4 = (int64_t)mb * kBM + q * 32 + (lane & ~3);
+                        uint16_t* const kvb = reinterpret_cast<uint16_t*>(a.kv) + n0 + c * 32 +
+                                              (lane & 3) * 8;
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            if (row4 + i < a.T)
+                                *reinterpret_cast<uint4*>(kvb + (row4 + i) * a.ldkv) =
+                                    make_uint4(o[i][0], o[i][1], o[i][2], o[i][3]);
+                        continue;
+                    }
 #pragma unroll
                     for (int msk = 1; msk < 8; msk <<= 1) {
                         const bool upper = (lane & msk) != 0;

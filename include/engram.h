@@ -310,6 +310,29 @@ engram_status engram_forward_noalloc(const engram_ctx* ctx, int layer, const uin
 engram_status engram_project_windows(const engram_ctx* ctx, int layer, const uint32_t* d_windows,
                                      int64_t T, float* d_kv, void* stream);
 
+/* The same pre-pass through the staged path ("DeepSeek V4.1 Flash 的 Engram",
+ * section "提前投影"): every (token, bucket) row is gathered and dequantised
+ * once into the operand matrix e at the start of d_workspace, then the
+ * tcgen05 projection (CTA pairs; stream K for a batch whose output tiles do
+ * not fill the GPU twice, as in engram_forward_staged) stores kv [T][N] in
+ * d_kv, either as fp32 (ENGRAM_KV_F32, the same values as engram_project
+ * up to accumulation order) or rounded once to BF16 (ENGRAM_KV_BF16, half
+ * the bytes to keep until the layer entry; every kv value then carries a
+ * relative error of at most 2^-9, which is not the plain reading of the
+ * step, so the BF16 form is an explicit choice of the caller).
+ * d_workspace: engram_forward_staged_workspace_bytes(ctx, T) bytes, 16-byte
+ * aligned; d_kv 16-byte aligned.  Works for every bound layer, BF16 tables
+ * included.  engram_gate (fp32) or engram_gate_bf16kv then finishes the step. */
+#define ENGRAM_KV_F32 0
+#define ENGRAM_KV_BF16 1
+engram_status engram_prepass(const engram_ctx* ctx, int layer, const uint32_t* d_windows, int64_t T,
+                             void* d_kv, int kv_format, void* d_workspace, void* stream);
+/* a5 on a BF16 kv [T][N] (engram_prepass with ENGRAM_KV_BF16); otherwise as
+ * engram_gate. */
+engram_status engram_gate_bf16kv(const engram_ctx* ctx, int layer, const uint16_t* d_kv,
+                                 const uint32_t* d_windows, int64_t T, uint16_t* d_hidden,
+                                 float* d_gates, void* stream);
+
 /* Synchronise `stream`, then read and clear the context's device error word:
  * ENGRAM_EBOUNDS / ENGRAM_ETIMEOUT if a kernel reported one, ENGRAM_ECUDA on
  * an asynchronous CUDA error. */

@@ -215,6 +215,8 @@ def test_device_calls_validate_before_launch():
         (eg.engram_forward_staged, (0, 16, 4, 16, 16)),
         (eg.engram_stage_rows, (0, 16, 4, 16)),
         (eg.engram_forward_staged_rows, (0, 16, 4, 16, 16)),
+        (eg.engram_prepass, (0, 16, 4, 16, eg.KV_BF16, 16)),
+        (eg.engram_gate_bf16kv, (0, 16, 16, 4, 16)),
     ]:
         with pytest.raises(eg.EngramError) as e:
             fn(ctx, *args)
