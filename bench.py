@@ -8,7 +8,9 @@ inputs resident in HBM) tokens/s per layer of the forward step through the
 faster of the two forward entries (engram_forward_staged; the single fused
 kernel engram_forward is reported beside it under "fused"); `e2e` is the
 same metric through the C ABI with host buffers: append on the host, pinned
-H2D of windows and hidden, the forward, D2H of the updated hidden.
+H2D of windows and hidden, the forward, D2H of the updated hidden, every step,
+with consecutive steps pipelined over an upload, a compute and a download
+stream.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
@@ -365,27 +367,52 @@ def main():
     fused_tf = flops_call / (ms_fused / 1000.0) / 1e12
 
     # ---- e2e through the C ABI with host buffers ----
-    h_win = torch.empty((T, 4), dtype=torch.int32, pin_memory=True)
+    # Every step appends its tokens on the host, copies its windows and hidden
+    # from pinned host memory, runs the forward and copies the updated hidden
+    # back.  Three streams and two buffer sets pipeline the steps: step i's
+    # upload and step i-1's download (opposite directions of the host link)
+    # overlap step i-1's and i's compute.
+    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    h_win = [torch.empty((T, 4), dtype=torch.int32, pin_memory=True) for _ in range(2)]
     h_hid_in = [torch.from_numpy(x.view(np.int16)).pin_memory() for x in hid_h[:2]]
-    h_hid_out = torch.empty((T, w.hc, w.d), dtype=torch.int16, pin_memory=True)
-    e_win = torch.empty((T, 4), dtype=torch.int32, device=dev)
-    e_hid = torch.empty((T, w.hc, w.d), dtype=torch.int16, device=dev)
+    h_hid_out = [torch.empty((T, w.hc, w.d), dtype=torch.int16, pin_memory=True)
+                 for _ in range(2)]
+    e_win = [torch.empty((T, 4), dtype=torch.int32, device=dev) for _ in range(2)]
+    e_hid = [torch.empty((T, w.hc, w.d), dtype=torch.int16, device=dev) for _ in range(2)]
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_comp = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+    for j in range(2):  # recorded once so that the first waits return at once
+        ev_in[j].record(s_in)
+        ev_comp[j].record(stream)
+        ev_out[j].record(s_out)
     tok_h = [synth.session_tokens(w, 100 + base_session + i, T) for i in range(2)]
-    h_win_np = h_win.numpy().view(np.uint32)
+    h_win_np = [x.numpy().view(np.uint32) for x in h_win]
 
     def e2e_step(i):
+        j = i % 2
+        ev_in[j].synchronize()  # step i - 2's upload has read h_win[j]
         s = eg.engram_session_create(ctx)
-        eg.engram_session_append(s, tok_h[i % 2], None, h_win_np)
+        eg.engram_session_append(s, tok_h[i % 2], None, h_win_np[j])
         eg.engram_session_destroy(s)
-        e_win.copy_(h_win, non_blocking=True)
-        e_hid.copy_(h_hid_in[i % 2], non_blocking=True)
-        eg.engram_forward_staged(ctx, 0, e_win, T, e_hid, d_ws, None, sptr)
-        h_hid_out.copy_(e_hid, non_blocking=True)
-        stream.synchronize()
+        s_in.wait_event(ev_comp[j])  # step i - 2's forward is done with e_win/e_hid[j]
+        s_in.wait_event(ev_out[j])   # ... and its download has read e_hid[j]
+        with torch.cuda.stream(s_in):
+            e_win[j].copy_(h_win[j], non_blocking=True)
+            e_hid[j].copy_(h_hid_in[i % 2], non_blocking=True)
+            ev_in[j].record(s_in)
+        stream.wait_event(ev_in[j])
+        eg.engram_forward_staged(ctx, 0, e_win[j], T, e_hid[j], d_ws, None, sptr)
+        ev_comp[j].record(stream)
+        s_out.wait_event(ev_comp[j])
+        with torch.cuda.stream(s_out):
+            h_hid_out[j].copy_(e_hid[j], non_blocking=True)
+            ev_out[j].record(s_out)
 
     e2e_steps = max(1, min(args.steps, 500))
     for i in range(min(args.warmup, 5)):
         e2e_step(i)
+    torch.cuda.synchronize()
     dist.barrier()
     torch.cuda.synchronize()
     t_e0 = time.perf_counter()
