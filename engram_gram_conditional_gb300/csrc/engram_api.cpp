@@ -814,13 +814,11 @@ engram_status engram_forward(const engram_ctx* ctx, int layer, const uint32_t* d
     return forward_fused(ctx, layer, d_windows, T, d_hidden, d_workspace, d_gates, stream, 8);
 }
 
-// The staged forward of a batch too small to fill the GPU (K split) runs the
-// projection with a plain kv-store epilogue into per-split fp32 buffers and
-// the gate as its own kernel: the fused gate epilogue's loads wait behind the
-// wkv stream in the SM's memory pipeline, which a single wave of tiles cannot
-// hide, while the separate gate kernel has the whole GPU to itself.
 // A batch whose output tiles (128 tokens x 256 outputs) do not fill the GPU
-// twice runs the staged projection with stream K and the gate kernel after it.
+// twice runs the staged projection with stream K and a kv-store epilogue, and
+// the gate as its own kernel after it: the fused gate epilogue's loads would
+// wait behind the wkv stream in the SM's memory pipeline, which a single wave
+// of tiles cannot hide, while the separate gate kernel has the whole GPU.
 static bool staged_stream_k(const engram_ctx* ctx, int64_t T) {
     const int64_t tiles = (T + kBM - 1) / kBM * (ctx->N / kBN);
     return tiles < 2 * (int64_t)device_sm_count();
@@ -966,8 +964,8 @@ static engram_status staged_rows(const engram_ctx* ctx, int layer, const uint32_
             e = cudaMemsetAsync(a.sk_flags, 0, w.flags, s);
             if (e != cudaSuccess) return cuda_fail(e, "stream-K flags");
         }
-        e = pairs ? launch_project_split_pair(a, L.f16, tmA, tmB, s)
-                  : launch_project_split(a, L.f16, tmA, tmB, s);
+        e = pairs ? launch_project_tma_pair(a, L.f16, tmA, tmB, s)
+                  : launch_project_tma(a, L.f16, tmA, tmB, s);
         if (e != cudaSuccess) return cuda_fail(e, "stream-K projection launch");
         e = launch_gate(geometry(ctx), a.kv, false, 1, 0, a.windows, T, d_hidden, L.w.wq, L.w.wk,
                         d_gates, s);
@@ -1046,8 +1044,8 @@ engram_status engram_prepass(const engram_ctx* ctx, int layer, const uint32_t* d
         a.sk_slots = reinterpret_cast<float*>(rest + w.kv);
         a.sk_flags = reinterpret_cast<uint32_t*>(rest + w.kv + w.slots);
     }
-    e = pairs ? launch_project_split_pair(a, L.f16, tmA, *tmB, s)
-              : launch_project_split(a, L.f16, tmA, *tmB, s);
+    e = pairs ? launch_project_tma_pair(a, L.f16, tmA, *tmB, s)
+              : launch_project_tma(a, L.f16, tmA, *tmB, s);
     if (e != cudaSuccess) return cuda_fail(e, "pre-pass projection launch");
     return ok();
 }

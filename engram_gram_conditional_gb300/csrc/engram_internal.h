@@ -151,15 +151,17 @@ cudaError_t launch_project(const MmaArgs& a, const CUtensorMap& tmA, const CUten
                            cudaStream_t s);
 cudaError_t launch_forward_phase(const MmaArgs& a, int mode, bool f16, bool bucket,
                                  const CUtensorMap& tmB, cudaStream_t s);
-// Staged forward for small batches: the projection with a TMA-fed A operand,
-// split over K into a.k_splits partial kv buffers (the gate runs after it).
-cudaError_t launch_project_split(const MmaArgs& a, bool f16, const CUtensorMap& tmA,
-                                 const CUtensorMap& tmB, cudaStream_t s);
-// The same two GEMMs on CTA pairs (clusters of two SMs, tcgen05 cta_group::2):
+// The projection with a TMA-fed A operand (the staged operand e) and the
+// kv-store epilogue: kv fp32 or BF16 (a.kv_bf16), whole tiles or, with
+// a.stream_k, stream-K pieces (the staged forward of a small batch, whose gate
+// runs after it, and engram_prepass).
+cudaError_t launch_project_tma(const MmaArgs& a, bool f16, const CUtensorMap& tmA,
+                               const CUtensorMap& tmB, cudaStream_t s);
+// The same GEMMs on CTA pairs (clusters of two SMs, tcgen05 cta_group::2):
 // each pair computes 256-token x 256-output tiles, each CTA holding half of the
 // wkv tile, so tmB_half is a wkv tensor map with 128-row boxes.
-cudaError_t launch_project_split_pair(const MmaArgs& a, bool f16, const CUtensorMap& tmA,
-                                      const CUtensorMap& tmB_half, cudaStream_t s);
+cudaError_t launch_project_tma_pair(const MmaArgs& a, bool f16, const CUtensorMap& tmA,
+                                    const CUtensorMap& tmB_half, cudaStream_t s);
 cudaError_t launch_forward_tma_pair(const MmaArgs& a, bool f16, const CUtensorMap& tmA,
                                    const CUtensorMap& tmB_half, cudaStream_t s);
 // Staged forward, step 2: the whole forward GEMM with a TMA-fed A operand.
