@@ -427,7 +427,10 @@ def main():
         "metric": "Engram tokens/s per layer (prefill, decode); gather HBM GB/s; wkv TC util %",
         "value": value, "unit": "tokens/s", "n_gpus": dist.world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        # the GEMM multiplies FP16 operands that hold the BF16 values exactly
+        # (E4M3 x 2^E8M0 rows, wkv scaled by a power of two) into fp32; the
+        # gate is fp32; hidden is BF16 in and out
+        "scaling": "weak", "vs_baseline": None, "dtype": "f16*f16->f32", "data": "synthetic",
         "config": dict(workload_config(w), table_rows=rows, parallelism=f"replicas x{dist.world}",
                        entry="engram_forward_staged"),
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16"],

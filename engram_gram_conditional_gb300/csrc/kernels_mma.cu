@@ -1665,13 +1665,13 @@ cudaError_t launch_project(const MmaArgs& a, const CUtensorMap& tmA, const CUten
 
 
 cudaError_t launch_project_tma(const MmaArgs& a, bool f16, const CUtensorMap& tmA,
-                                 const CUtensorMap& tmB, cudaStream_t s) {
+                               const CUtensorMap& tmB, cudaStream_t s) {
     if (f16) return launch<kASrcTma, true, kEpiStoreKv>(a, tmA, tmB, s);
     return launch<kASrcTma, false, kEpiStoreKv>(a, tmA, tmB, s);
 }
 
 cudaError_t launch_project_tma_pair(const MmaArgs& a, bool f16, const CUtensorMap& tmA,
-                                      const CUtensorMap& tmB_half, cudaStream_t s) {
+                                    const CUtensorMap& tmB_half, cudaStream_t s) {
     if (f16) return launch<kASrcTmaPair, true, kEpiStoreKv>(a, tmA, tmB_half, s);
     return launch<kASrcTmaPair, false, kEpiStoreKv>(a, tmA, tmB_half, s);
 }
