@@ -863,13 +863,22 @@ engram_status engram_stage_rows(const engram_ctx* ctx, int layer, const uint32_t
     if (!d_windows || !d_workspace || !aligned16(d_windows) || !aligned16(d_workspace))
         return fail(ENGRAM_EINVAL, "windows / workspace (16-byte aligned)");
     const LayerState& L = ctx->layers[layer];
-    // gather and dequantise every (token, bucket) row once into e
+    // gather and dequantise every (token, bucket) row once into e; for a small
+    // batch the same kernel zeroes the stream-K flags of the GEMM after it
+    uint32_t* clear = nullptr;
+    int n_clear = 0;
+    if (staged_stream_k(ctx, T)) {
+        const StreamKWs w = stream_k_ws(ctx, T);
+        clear = reinterpret_cast<uint32_t*>(static_cast<char*>(d_workspace) +
+                                            staged_e_bytes(ctx, T) + w.kv + w.slots);
+        n_clear = (int)(w.flags / sizeof(uint32_t));
+    }
     cudaError_t e = launch_gather_stage(hash_params(ctx, layer),
                                         reinterpret_cast<const uint4*>(d_windows), T,
                                         (int)ctx->desc.row_dim, L.w.table, L.w.scales, L.rows,
                                         L.table_bf16, L.f16, L.a_exp_shift,
-                                        static_cast<uint16_t*>(d_workspace),
-                                        ctx->d_err, (cudaStream_t)stream);
+                                        static_cast<uint16_t*>(d_workspace), ctx->d_err, clear,
+                                        n_clear, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "staged gather launch");
     return ok();
 }
@@ -907,13 +916,6 @@ static cudaError_t staged_gemm(const engram_ctx* ctx, int layer, int64_t T, void
     return e;
 }
 
-// Zeroes the stream-K ready flags of a small batch's workspace on `s`.
-static cudaError_t clear_stream_k_flags(const engram_ctx* ctx, int64_t T, void* d_workspace,
-                                        cudaStream_t s) {
-    const StreamKWs w = stream_k_ws(ctx, T);
-    char* flags = static_cast<char*>(d_workspace) + staged_e_bytes(ctx, T) + w.kv + w.slots;
-    return cudaMemsetAsync(flags, 0, w.flags, s);
-}
 
 // Step 2 of the staged forward; flags_clear: the stream-K flags of the
 // workspace were zeroed earlier on the stream (else this call zeroes them).
@@ -993,16 +995,11 @@ engram_status engram_forward_staged(const engram_ctx* ctx, int layer, const uint
     if (!d_windows || !d_hidden || !d_workspace || !aligned16(d_windows) || !aligned16(d_hidden) ||
         !aligned16(d_workspace))
         return fail(ENGRAM_EINVAL, "windows / hidden / workspace (16-byte aligned)");
-    // a small batch's flags are zeroed before the gather, so that nothing
-    // stands between the gather and the GEMM that it hands its rows to
-    const bool small = staged_stream_k(ctx, T);
-    if (small) {
-        cudaError_t e = clear_stream_k_flags(ctx, T, d_workspace, (cudaStream_t)stream);
-        if (e != cudaSuccess) return cuda_fail(e, "stream-K flags");
-    }
+    // the gather zeroes a small batch's stream-K flags, so that nothing stands
+    // between the gather and the GEMM that it hands its rows to
     st = engram_stage_rows(ctx, layer, d_windows, T, d_workspace, stream);
     if (st) return st;
-    return staged_rows(ctx, layer, d_windows, T, d_hidden, d_workspace, d_gates, stream, small);
+    return staged_rows(ctx, layer, d_windows, T, d_hidden, d_workspace, d_gates, stream, true);
 }
 
 engram_status engram_prepass(const engram_ctx* ctx, int layer, const uint32_t* d_windows, int64_t T,
@@ -1018,10 +1015,7 @@ engram_status engram_prepass(const engram_ctx* ctx, int layer, const uint32_t* d
     cudaStream_t s = (cudaStream_t)stream;
     const bool small = staged_stream_k(ctx, T);
     cudaError_t e;
-    if (small) {  // zeroed before the gather, as in engram_forward_staged
-        e = clear_stream_k_flags(ctx, T, d_workspace, s);
-        if (e != cudaSuccess) return cuda_fail(e, "stream-K flags");
-    }
+    // (the gather zeroes the stream-K flags, as in engram_forward_staged)
     st = engram_stage_rows(ctx, layer, d_windows, T, d_workspace, stream);
     if (st) return st;
     const LayerState& L = ctx->layers[layer];

@@ -131,11 +131,12 @@ cudaError_t launch_absmax_bf16(const uint16_t* x, uint64_t n, uint32_t* out, cud
 // Staged forward, step 1: windows -> operand rows e: FP16 in 128 x 64 tiles
 // (element (t, k) at ((t / 128) (K / 64) + k / 64) 8192 + (t % 128) 64 + k % 64;
 // rows of the last 128-token block past T are not written), or BF16 row-major
-// [T][K].
+// [T][K].  Also zeroes n_clear words at `clear` (may be null with 0), once the
+// kernel before it in the stream has finished.
 cudaError_t launch_gather_stage(const HashParams& hp, const uint4* windows, int64_t T, int row_dim,
                                 const uint8_t* table, const uint8_t* scales, uint64_t nrows,
                                 bool table_bf16, bool f16, int exp_shift, uint16_t* e,
-                                uint32_t* err, cudaStream_t s);
+                                uint32_t* err, uint32_t* clear, int n_clear, cudaStream_t s);
 // FP16 copy of the BF16 wkv [N][K] (N % 128 == 0, K % 64 == 0), values x
 // scale rounded to nearest even, stored as 128 x 64 tiles: element (n, k) at
 // ((n / 128) (K / 64) + k / 64) 8192 + (n % 128) 64 + k % 64.

@@ -170,14 +170,25 @@ __global__ void k_gather(const uint32_t* __restrict__ rows, int64_t T, int nb, i
 // row-major [T][K]).  Each table
 // row is read whole: row_dim / 16 lanes per row, 16 codes and their scale per
 // lane; the first lane of a row hashes its (token, bucket) pair.
+// Launched as a programmatic dependent: the hashing and the row loads (of
+// windows and table, which no kernel of the stream writes) may overlap the
+// kernel before; every thread waits for it (pdl_wait) before its first store,
+// since e may still be read by the GEMM of the previous call.  Block 0 then
+// also zeroes n_clear words at `clear` (the stream-K flags of the GEMM after).
 template <bool kF16>
 __global__ void k_gather_stage(const __grid_constant__ HashParams hp, const uint4* __restrict__ windows,
                                int64_t T, int row_dim, const uint8_t* __restrict__ table,
                                const uint8_t* __restrict__ scales, uint64_t nrows, int exp_shift,
-                               int table_bf16, uint16_t* __restrict__ e, uint32_t* err) {
+                               int table_bf16, uint16_t* __restrict__ e, uint32_t* err,
+                               uint32_t* __restrict__ clear, int n_clear) {
     // the GEMM that reads e may start its prologue as soon as every CTA of
     // this grid runs (it waits for this grid's end before reading e)
     pdl_launch_dependents();
+    if (blockIdx.x == 0 && n_clear > 0) {
+        pdl_wait();
+        for (int i = threadIdx.x; i < n_clear; i += blockDim.x) clear[i] = 0u;
+    }
+    bool waited = false;
     const int lpr = row_dim / 16;              // lanes per row
     const int rpw = 32 / lpr;                  // rows per warp pass
     const int lane = threadIdx.x & 31;
@@ -230,6 +241,10 @@ __global__ void k_gather_stage(const __grid_constant__ HashParams hp, const uint
                 lo = decode8(c.x, c.y, sf);
                 hi = decode8(c.z, c.w, sf);
             }
+        }
+        if (!waited) {
+            pdl_wait();
+            waited = true;
         }
         // column k of row t: row-major, or (kF16) in 128 x 64 tiles, tile
         // (t / 128) (K / 64) + k / 64, so that two k-blocks of a 128-token
@@ -297,6 +312,8 @@ k_gate_branch(const void* __restrict__ kv, int nsplit, int64_t split_stride,
     __shared__ float red[kGateBranchThreads / 32][3];
     __shared__ float gsh;
     pdl_wait();  // launched to overlap the end of the projection that writes kv
+    // the next call's gather may start hashing and loading rows meanwhile
+    pdl_launch_dependents();
     const int64_t t = blockIdx.x / hc;
     const int b = (int)(blockIdx.x - t * hc);
     if (windows[t].x == kDead) {
@@ -516,20 +533,27 @@ cudaError_t launch_wkv_to_f16_tiles(const uint16_t* src, uint16_t* dst, uint64_t
 cudaError_t launch_gather_stage(const HashParams& hp, const uint4* windows, int64_t T, int row_dim,
                                 const uint8_t* table, const uint8_t* scales, uint64_t nrows,
                                 bool table_bf16, bool f16, int exp_shift, uint16_t* e,
-                                uint32_t* err, cudaStream_t s) {
+                                uint32_t* err, uint32_t* clear, int n_clear, cudaStream_t s) {
     if (T == 0) return cudaSuccess;
     if (table_bf16 && f16) return cudaErrorInvalidValue;  // BF16 rows feed BF16 operands
     const int threads = 256;
     const int64_t rows_per_warp = 32 / (row_dim / 16);
     const int64_t warps = (T * hp.nb + rows_per_warp - 1) / rows_per_warp;
-    const int grid = grid_for(warps * 32, threads, 8);
+    // programmatic dependent launch (see the kernel)
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(grid_for(warps * 32, threads, 8));
+    cfg.blockDim = dim3(threads);
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     if (f16)
-        k_gather_stage<true><<<grid, threads, 0, s>>>(hp, windows, T, row_dim, table, scales, nrows,
-                                                      exp_shift, 0, e, err);
-    else
-        k_gather_stage<false><<<grid, threads, 0, s>>>(hp, windows, T, row_dim, table, scales, nrows,
-                                                       exp_shift, table_bf16 ? 1 : 0, e, err);
-    return cudaGetLastError();
+        return cudaLaunchKernelEx(&cfg, k_gather_stage<true>, hp, windows, T, row_dim, table,
+                                  scales, nrows, exp_shift, 0, e, err, clear, n_clear);
+    return cudaLaunchKernelEx(&cfg, k_gather_stage<false>, hp, windows, T, row_dim, table, scales,
+                              nrows, exp_shift, table_bf16 ? 1 : 0, e, err, clear, n_clear);
 }
 
 int device_sm_count() { return sm_count(); }
