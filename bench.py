@@ -57,6 +57,9 @@ def parse_args():
                     help="oracle tokens for cpu_baseline (0: skip)")
     ap.add_argument("--small", action="store_true",
                     help="profiling case: same kernels and batch, a 4.8M-row table, 2 batches")
+    ap.add_argument("--gather-small", action="store_true",
+                    help="profiling case of the unfused gather: 50,032 tokens over a 4.8M-row "
+                         "table; prints one line with its time and GB/s")
     ap.add_argument("--decode-small", action="store_true",
                     help="profiling case of the decode step: 256 sessions, full wkv, a "
                          "4.8M-row table; prints one line with its ms per step")
@@ -276,6 +279,9 @@ def main():
     if args.decode_small:
         decode_small(args)
         return
+    if args.gather_small:
+        gather_small(args)
+        return
     import torch
 
     import engram_gram_conditional_gb300 as eg
@@ -476,6 +482,44 @@ def main():
     if dist.rank == 0:
         print(json.dumps(line), flush=True)
     dist.close()
+
+
+def gather_small(args):
+    """engram_gather_dequant (a3 alone) for 50,032 Zipf tokens over a 4.8M-row
+    table (1.3 GB, ten times L2), for ncu."""
+    import dataclasses
+
+    import torch
+
+    import engram_gram_conditional_gb300 as eg
+    import synth
+    from engram_gram_conditional_gb300 import build
+    from engram_gram_conditional_gb300.layer import EngramLayerSet
+
+    build.build()
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream()
+    w = dataclasses.replace(synth.WORKLOADS["decode_256"], bucket_bases=[200_000])
+    tmap = synth.token_map(w.vocab, w.vc, w.seed)
+    wq, wk = synth.wq_wk(w)
+    m = EngramLayerSet.from_workload(w, tmap, device=dev)
+    m.bind(0, w.table_seeds[0], synth.wkv_bf16(w), wq, wk)
+    T = 50_032
+    s = eg.engram_session_create(m.ctx)
+    win = eg.engram_session_append(s, synth.zipf_tokens(T, w.vocab, seed=5))
+    eg.engram_session_destroy(s)
+    d_w = torch.from_numpy(win.view(np.int32)).to(dev)
+    d_r = torch.empty((T, w.nb), dtype=torch.int32, device=dev)
+    d_e = torch.empty((T, w.K), dtype=torch.int16, device=dev)
+    sptr = stream.cuda_stream
+    eg.engram_hash(m.ctx, 0, d_w, T, d_r, sptr)
+    for _ in range(args.warmup):
+        eg.engram_gather_dequant(m.ctx, 0, d_r, T, d_e, sptr)
+    ms = timed(lambda i: eg.engram_gather_dequant(m.ctx, 0, d_r, T, d_e, sptr), args.steps, stream)
+    eg.engram_sync(m.ctx, sptr)
+    print(json.dumps({"case": "gather_small", "tokens": T, "table_rows": m.rows(0),
+                      "ms": ms, "GB_per_s": T * 18720 / ms / 1e6}), flush=True)
+    m.close()
 
 
 def decode_small(args):
