@@ -152,3 +152,54 @@ def test_prepass_rejects_an_unknown_kv_format(tiny):
     with pytest.raises(eg.EngramError) as e:
         eg.engram_prepass(tiny.model.ctx, 0, to_dev(win), 8, d_kv, 7, ws)
     assert e.value.status == eg.EINVAL
+
+
+def test_back_to_back_calls_on_one_stream_share_a_workspace(prefill):
+    # Kernels of consecutive calls overlap (programmatic dependent launch);
+    # chained on one stream with one workspace and no synchronisation between
+    # them, every call must still give the result it gives alone.
+    ctx = prefill.model.ctx
+    w = prefill.w
+    T1, T2, T3 = 256, 2048, 77
+    win1, _, _ = prefill_windows(prefill, 1, T1, spans=[(10, 3)])
+    win2, _, _ = prefill_windows(prefill, 2, T2 // 2)
+    win3, _, _ = prefill_windows(prefill, 1, T3)
+    h1, h2, h3 = (synth.hidden_bf16(w, T) for T in (T1, T2, T3))
+    ws = torch.empty(max(eg.engram_forward_staged_workspace_bytes(ctx, T) for T in (T1, T2, T3)) +
+                     eg.engram_workspace_bytes(ctx, T2), dtype=torch.uint8, device="cuda")
+
+    def alone(fn):
+        out = fn()
+        eg.engram_sync(ctx)
+        return [x.cpu().numpy() for x in out]
+
+    def staged(win, h):
+        d_h = to_dev(h)
+        eg.engram_forward_staged(ctx, 0, to_dev(win), win.shape[0], d_h, ws, None)
+        return [d_h]
+
+    def prepass_gate(win, h, fmt):
+        T = win.shape[0]
+        d_kv = torch.empty((T, w.N), dtype=torch.float32 if fmt == eg.KV_F32 else torch.int16,
+                           device="cuda")
+        d_w, d_h = to_dev(win), to_dev(h)
+        eg.engram_prepass(ctx, 0, d_w, T, d_kv, fmt, ws)
+        (eg.engram_gate if fmt == eg.KV_F32 else eg.engram_gate_bf16kv)(ctx, 0, d_kv, d_w, T, d_h)
+        return [d_h, d_kv]
+
+    def fused(win, h):
+        d_h = to_dev(h)
+        eg.engram_forward(ctx, 0, to_dev(win), win.shape[0], d_h, ws, None)
+        return [d_h]
+
+    calls = [lambda: prepass_gate(win1, h1, eg.KV_F32), lambda: staged(win2, h2),
+             lambda: prepass_gate(win3, h3, eg.KV_BF16), lambda: staged(win1, h1),
+             lambda: fused(win2, h2), lambda: staged(win3, h3)]
+    ref = [alone(c) for c in calls]
+    outs = [c() for c in calls]  # back to back
+    eg.engram_sync(ctx)
+    for i, (o, r) in enumerate(zip(outs, ref)):
+        for a, b in zip(o, r):
+            assert np.array_equal(a.cpu().numpy(), b), f"call {i}"
+    # the staged forward of a small batch is the stream-K pre-pass plus the gate
+    assert np.array_equal(ref[0][0], ref[3][0])
