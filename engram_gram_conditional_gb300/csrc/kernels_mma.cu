@@ -836,11 +836,13 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
     if constexpr (kPair) cluster_sync();  // both CTAs' barriers exist before either signals the other
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    // launched as a programmatic dependent: the prologue above may overlap the
-    // end of the kernel before; wait for it before touching memory.  The
-    // kernel after this one (the gate) may then be scheduled as CTAs of this
-    // one exit.
-    pdl_wait();
+    // Launched as a programmatic dependent, the kernel may start while the
+    // kernel before it in the stream (the gather that writes the A operand, or
+    // the previous call) still runs.  The roles that touch memory earlier work
+    // writes wait for it (pdl_wait) first: the A producer and the epilogue.
+    // The wkv producer does not: wkv is written only at bind, so the first wkv
+    // stages load while the gather finishes.  The kernel after this one (the
+    // gate) may be scheduled as CTAs of this one exit.
     pdl_launch_dependents();
 
     // work items: (M unit, N tile, split); a CTA pair shares one item sequence
@@ -906,6 +908,7 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
         // TMA producers: warp 12 loads the wkv tiles, warp 14 the A tiles of
         // the TMA-fed variants, each running ahead on its own ring
         const bool do_b = warp == kWarpTma;
+        if (!do_b) pdl_wait();
         // with one M unit every wkv byte is read once per launch: its lines
         // are marked for early eviction, so that they do not push the
         // launch's outputs (the kv of a small batch) out of L2
@@ -1176,6 +1179,7 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
             setmaxnreg_inc<kRegsWideEpi>();
         else
             setmaxnreg_inc<kRegsEpi>();
+        pdl_wait();
         const int q = warp & 3;  // TMEM lane quadrant this warp may read
         // the warp's group (of kG sharing the quadrant): its 32-column chunks
         // are c_first, c_first + kG, ...; its ready flag in a stream-K launch
