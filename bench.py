@@ -41,6 +41,9 @@ WORKLOAD = "prefill_2048"
 # capture of that kernel (dram__bytes_read.sum 858.1 MB + dram__bytes_write.sum
 # 44.5 MB); the table size does not enter it.  Re-measure when the kernel changes.
 GEMM_DRAM_BYTES = 902.6e6
+# The same for the decode step's stream-K GEMM (256 tokens; dram__bytes_read.sum
+# 317.8 MB + dram__bytes_write.sum 10.3 MB, from the --decode-small capture).
+DECODE_GEMM_DRAM_BYTES = 328.1e6
 FLOP_PER_TOKEN = None  # set from the geometry: 2 N K
 
 
@@ -679,7 +682,8 @@ def extras(args, w, W, wq, wk, tmap, win0, d_win0, model, peaks, dev, sptr, stre
             "entry": fwd.__name__, "tokens_per_s": S / (ms_d / 1000.0), "ms_per_step": ms_d,
             "sessions": S, "steps": wd.steps, "table_rows": dm.rows(0),
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm"], "unit": "GB/s",
-                         "frac": gbs / peaks["hbm"], "bytes_per_step": bytes_step}}
+                         "frac": gbs / peaks["hbm"], "bytes_per_step": bytes_step,
+                         "traffic": DECODE_GEMM_DRAM_BYTES if name == "staged" else None}}
     # the decode step as a pre-pass (as soon as the step's tokens are known)
     # plus the gate at the layer entry
     d_kvd = torch.empty((S, w.N), dtype=torch.float32, device=dev)
