@@ -130,6 +130,7 @@ struct LayerState {
     // FP16 operand path of the fused kernels (see engram_layer_info)
     bool f16 = false;
     uint16_t* wkv_f16 = nullptr;   // library-owned copy, wkv x 2^wkv_exp
+    float* wqk = nullptr;          // library-owned w_q * w_k [hc][d], made at bind
     CUtensorMap tm_wkv_f16{};
     CUtensorMap tm_wkv_f16_2k{};   // the tiled FP16 copy with 256-row boxes (2 k-blocks)
     int wkv_exp = 0;
@@ -228,8 +229,7 @@ MmaArgs mma_args(const engram_ctx* ctx, int layer, int64_t T) {
     a.row_dim_log2 = 31 - __builtin_clz(ctx->desc.row_dim);
     a.a_exp_shift = 0;
     a.out_scale = 1.0f;
-    a.wq = L.w.wq;
-    a.wk = L.w.wk;
+    a.wqk = L.wqk;
     a.hp = hash_params(ctx, layer);
     return a;
 }
@@ -436,8 +436,10 @@ engram_status engram_ctx_destroy(engram_ctx* ctx) {
         int cur = -1;
         cudaGetDevice(&cur);
         if (ctx->device >= 0) cudaSetDevice(ctx->device);
-        for (LayerState& L : ctx->layers)
+        for (LayerState& L : ctx->layers) {
             if (L.wkv_f16) cudaFree(L.wkv_f16);
+            if (L.wqk) cudaFree(L.wqk);
+        }
         cudaFree(ctx->d_err);
         if (cur >= 0) cudaSetDevice(cur);
     }
@@ -540,6 +542,19 @@ engram_status engram_layer_bind(engram_ctx* ctx, int layer, const engram_layer_w
     const bool want_f16 = !(w->flags & ENGRAM_BIND_BF16_OPERANDS) && !tbf16;
     const bool scales_fit = smax != 255u && smax >= smin && smax - smin <= 22u;
     const bool w_finite = wabs < 0x7F80u;
+    // the gate's pre-multiplied weights enter only as the product w_q w_k:
+    // kept once per layer (read from the caller's arrays here, at bind)
+    const int64_t nqk = (int64_t)ctx->desc.hc * ctx->desc.d;
+    if (!L.wqk) {
+        e = cudaMalloc(&L.wqk, nqk * sizeof(float));
+        if (e != cudaSuccess) {
+            L.wqk = nullptr;
+            return fail(ENGRAM_ENOMEM, "cudaMalloc of the w_q w_k product");
+        }
+    }
+    e = launch_mul_f32(w->wq, w->wk, L.wqk, nqk, 0);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "w_q w_k product");
     if (L.wkv_f16) {
         cudaFree(L.wkv_f16);
         L.wkv_f16 = nullptr;
@@ -801,8 +816,8 @@ engram_status engram_gate(const engram_ctx* ctx, int layer, const float* d_kv,
         return fail(ENGRAM_EINVAL, "kv / windows / hidden (16-byte aligned)");
     const LayerState& L = ctx->layers[layer];
     cudaError_t e = launch_gate(geometry(ctx), d_kv, false, 1, 0,
-                                reinterpret_cast<const uint4*>(d_windows), T, d_hidden, L.w.wq,
-                                L.w.wk, d_gates, (cudaStream_t)stream);
+                                reinterpret_cast<const uint4*>(d_windows), T, d_hidden, L.wqk,
+                                d_gates, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "gate launch");
     return ok();
 }
@@ -969,8 +984,8 @@ static engram_status staged_rows(const engram_ctx* ctx, int layer, const uint32_
         e = pairs ? launch_project_tma_pair(a, L.f16, tmA, tmB, s)
                   : launch_project_tma(a, L.f16, tmA, tmB, s);
         if (e != cudaSuccess) return cuda_fail(e, "stream-K projection launch");
-        e = launch_gate(geometry(ctx), a.kv, false, 1, 0, a.windows, T, d_hidden, L.w.wq, L.w.wk,
-                        d_gates, s);
+        e = launch_gate(geometry(ctx), a.kv, false, 1, 0, a.windows, T, d_hidden, L.wqk, d_gates,
+                        s);
         if (e != cudaSuccess) return cuda_fail(e, "gate launch");
         return ok();
     }
@@ -1055,8 +1070,8 @@ engram_status engram_gate_bf16kv(const engram_ctx* ctx, int layer, const uint16_
         return fail(ENGRAM_EINVAL, "kv / windows / hidden (16-byte aligned)");
     const LayerState& L = ctx->layers[layer];
     cudaError_t e = launch_gate(geometry(ctx), d_kv, true, 1, 0,
-                                reinterpret_cast<const uint4*>(d_windows), T, d_hidden, L.w.wq,
-                                L.w.wk, d_gates, (cudaStream_t)stream);
+                                reinterpret_cast<const uint4*>(d_windows), T, d_hidden, L.wqk,
+                                d_gates, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "gate launch");
     return ok();
 }

@@ -79,8 +79,7 @@ struct MmaArgs {
     int kv_bf16;           // kEpiStoreKv: store kv rounded once to BF16 (no split buffers)
     int64_t ldkv;
     uint16_t* hidden;      // [T][hc][d]
-    const float* wq;       // [hc][d]
-    const float* wk;       // [hc][d]
+    const float* wqk;      // [hc][d] w_q * w_k (the gate's pre-multiplied weights, product)
     float* partials;       // [T][hc][d / kBN][epi_groups][3]
     int epi_groups;        // kEpiForward: epilogue warps per TMEM quadrant (1, or 2 TMA-fed)
     float* gbuf;           // [T][hc] gates of the call
@@ -119,10 +118,12 @@ cudaError_t launch_gather(const Geometry& g, const uint32_t* rows, int64_t T,
                           bool table_bf16, uint16_t* emb, uint32_t* err, cudaStream_t s);
 // kv: fp32 [T][N], possibly the sum of nsplit (<= 8) partial buffers
 // split_stride floats apart, added in split order; or BF16 [T][N] (kv_bf16,
-// nsplit 1).  kv, hidden, wq and wk 16-byte aligned.
+// nsplit 1).  wqk: [hc][d] w_q * w_k.  kv, hidden and wqk 16-byte aligned.
 cudaError_t launch_gate(const Geometry& g, const void* kv, bool kv_bf16, int nsplit,
                         int64_t split_stride, const uint4* windows, int64_t T, uint16_t* hidden,
-                        const float* wq, const float* wk, float* gates, cudaStream_t s);
+                        const float* wqk, float* gates, cudaStream_t s);
+// out = a * b elementwise (fp32, n values).
+cudaError_t launch_mul_f32(const float* a, const float* b, float* out, int64_t n, cudaStream_t s);
 // Bind-time scans: out[0] = min, out[1] = max of n E8M0 bytes (out preset by
 // the caller to 255 / 0); out[2] = largest |x| of n BF16 values as its bit
 // pattern without the sign (out[2] preset to 0).

@@ -307,8 +307,8 @@ template <bool kBf16Kv>
 __global__ void __launch_bounds__(kGateBranchThreads, 8)
 k_gate_branch(const void* __restrict__ kv, int nsplit, int64_t split_stride,
               const uint4* __restrict__ windows, int hc, int d, float eps,
-              uint16_t* __restrict__ hidden, const float* __restrict__ wq,
-              const float* __restrict__ wk, float* __restrict__ gates) {
+              uint16_t* __restrict__ hidden, const float* __restrict__ wqk,
+              float* __restrict__ gates) {
     __shared__ float red[kGateBranchThreads / 32][3];
     __shared__ float gsh;
     pdl_wait();  // launched to overlap the end of the projection that writes kv
@@ -327,19 +327,18 @@ k_gate_branch(const void* __restrict__ kv, int nsplit, int64_t split_stride,
     const char* kb = kvt + (int64_t)b * d * kv_elem;
     const char* vb = kvt + (int64_t)hc * d * kv_elem;
     uint2* hb = reinterpret_cast<uint2*>(hidden + (t * hc + b) * (int64_t)d);
-    const float4* qb = reinterpret_cast<const float4*>(wq + (int64_t)b * d);
-    const float4* wb = reinterpret_cast<const float4*>(wk + (int64_t)b * d);
+    const float4* qkb = reinterpret_cast<const float4*>(wqk + (int64_t)b * d);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     float skk = 0.f, shh = 0.f, shk = 0.f;
 #pragma unroll 1
     for (int i = threadIdx.x; i < n4; i += kGateBranchThreads) {
         const float4 k = kv_load4<kBf16Kv>(kb, i, nsplit, stride4);
         const uint2 h2 = hb[i];
-        const float4 q = __ldg(qb + i), w = __ldg(wb + i);
+        const float4 qk = __ldg(qkb + i);
         const float h[4] = {bf16_bits_to_f32(h2.x & 0xFFFFu), bf16_bits_to_f32(h2.x >> 16),
                             bf16_bits_to_f32(h2.y & 0xFFFFu), bf16_bits_to_f32(h2.y >> 16)};
         const float kk[4] = {k.x, k.y, k.z, k.w};
-        const float qw[4] = {q.x * w.x, q.y * w.y, q.z * w.z, q.w * w.w};
+        const float qw[4] = {qk.x, qk.y, qk.z, qk.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             skk += kk[e] * kk[e];
@@ -487,7 +486,7 @@ cudaError_t launch_gather(const Geometry& g, const uint32_t* rows, int64_t T,
 
 cudaError_t launch_gate(const Geometry& g, const void* kv, bool kv_bf16, int nsplit,
                         int64_t split_stride, const uint4* windows, int64_t T, uint16_t* hidden,
-                        const float* wq, const float* wk, float* gates, cudaStream_t s) {
+                        const float* wqk, float* gates, cudaStream_t s) {
     if (T == 0) return cudaSuccess;
     if (nsplit < 1 || nsplit > kGateMaxSplits || g.d % 4 != 0 || g.hc > 8 || (kv_bf16 && nsplit != 1))
         return cudaErrorInvalidValue;
@@ -505,9 +504,23 @@ cudaError_t launch_gate(const Geometry& g, const void* kv, bool kv_bf16, int nsp
     cfg.numAttrs = 1;
     if (kv_bf16)
         return cudaLaunchKernelEx(&cfg, k_gate_branch<true>, kv, nsplit, split_stride, windows,
-                                  g.hc, g.d, g.eps, hidden, wq, wk, gates);
+                                  g.hc, g.d, g.eps, hidden, wqk, gates);
     return cudaLaunchKernelEx(&cfg, k_gate_branch<false>, kv, nsplit, split_stride, windows, g.hc,
-                              g.d, g.eps, hidden, wq, wk, gates);
+                              g.d, g.eps, hidden, wqk, gates);
+}
+
+// out = a * b elementwise in fp32 (bind: the gate's w_q w_k product).
+__global__ void k_mul_f32(const float* __restrict__ a, const float* __restrict__ b,
+                          float* __restrict__ out, int64_t n) {
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
+         i += (int64_t)gridDim.x * blockDim.x)
+        out[i] = a[i] * b[i];
+}
+
+cudaError_t launch_mul_f32(const float* a, const float* b, float* out, int64_t n, cudaStream_t s) {
+    if (n == 0) return cudaSuccess;
+    k_mul_f32<<<grid_for(n, 256, 8), 256, 0, s>>>(a, b, out, n);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_scale_range(const uint8_t* scales, uint64_t n, uint32_t* out, cudaStream_t s) {

@@ -1385,8 +1385,7 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
                 const int col0 = n0 - branch * a.d;
                 const bool text = t < a.T && a.windows[t].x != kDead;
                 const uint16_t* hrow = a.hidden + (t * a.hc + branch) * (int64_t)a.d + col0;
-                const float* wqr = a.wq + (int64_t)branch * a.d + col0;
-                const float* wkr = a.wk + (int64_t)branch * a.d + col0;
+                const float* wqkr = a.wqk + (int64_t)branch * a.d + col0;
                 float skk = 0.f, shh = 0.f, shk = 0.f;
 #pragma unroll 1
                 for (int c = c_first; c < kBN / 32; c += kCStep) {
@@ -1402,12 +1401,9 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
                     if (text) {
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
-                            const float4 q0 = __ldg(reinterpret_cast<const float4*>(wqr + c * 32) + 2 * i);
-                            const float4 q1 = __ldg(reinterpret_cast<const float4*>(wqr + c * 32) + 2 * i + 1);
-                            const float4 k0 = __ldg(reinterpret_cast<const float4*>(wkr + c * 32) + 2 * i);
-                            const float4 k1 = __ldg(reinterpret_cast<const float4*>(wkr + c * 32) + 2 * i + 1);
-                            const float wqk[8] = {q0.x * k0.x, q0.y * k0.y, q0.z * k0.z, q0.w * k0.w,
-                                                  q1.x * k1.x, q1.y * k1.y, q1.z * k1.z, q1.w * k1.w};
+                            const float4 p0 = __ldg(reinterpret_cast<const float4*>(wqkr + c * 32) + 2 * i);
+                            const float4 p1 = __ldg(reinterpret_cast<const float4*>(wqkr + c * 32) + 2 * i + 1);
+                            const float wqk[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
                             const uint32_t hw[4] = {hv[i].x, hv[i].y, hv[i].z, hv[i].w};
 #pragma unroll
                             for (int e = 0; e < 8; ++e) {

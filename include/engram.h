@@ -32,9 +32,10 @@
  *    the library never frees them.  The library owns engram_ctx, the sessions,
  *    the per-layer hash parameters, a 16-byte device word per context (error
  *    word and bind-time scan results, allocated at the first
- *    engram_layer_bind) and, per bound layer on the FP16 operand path, an
- *    FP16 copy of wkv (N x K x 2 bytes, allocated by engram_layer_bind and
- *    freed by a rebind or engram_ctx_destroy).
+ *    engram_layer_bind), per bound layer the elementwise product of w_q and
+ *    w_k (hc x d x 4 bytes) and, on the FP16 operand path, an FP16 copy of
+ *    wkv (N x K x 2 bytes), allocated by engram_layer_bind and freed by a
+ *    rebind (the FP16 copy) or engram_ctx_destroy.
  *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
  *    Device calls are asynchronous on that stream.  Faults found by a kernel
  *    (a row index outside the table, a wait that ran out) set the context's
@@ -174,8 +175,9 @@ engram_status engram_layer_set_multipliers(engram_ctx* ctx, int layer, const uin
 /* Bind a layer's weights (pointers are kept, not copied).  Needs a GPU: it
  * allocates the context's device word at first use, scans the table's scale
  * exponents and wkv's magnitude, builds the FP16 copy of wkv when the FP16
- * operand path applies (engram_layer_info) and encodes the TMA descriptors.
- * It synchronises the device. */
+ * operand path applies (engram_layer_info), keeps the product w_q w_k (the
+ * gate uses the two only through it: bind again after changing them) and
+ * encodes the TMA descriptors.  It synchronises the device. */
 engram_status engram_layer_bind(engram_ctx* ctx, int layer, const engram_layer_weights* w);
 
 /* Fill rows [row_begin, row_end) of a table with its deterministic contents:
