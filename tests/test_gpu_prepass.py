@@ -203,3 +203,28 @@ def test_back_to_back_calls_on_one_stream_share_a_workspace(prefill):
             assert np.array_equal(a.cpu().numpy(), b), f"call {i}"
     # the staged forward of a small batch is the stream-K pre-pass plus the gate
     assert np.array_equal(ref[0][0], ref[3][0])
+
+
+@pytest.mark.parametrize("T", [256, 2048])
+def test_gate_bf16kv_full_geometry_sampled(prefill, T):
+    # the BF16-kv gate at full geometry (decode-sized and prefill-sized batches),
+    # against the oracle's gate on the same BF16 kv, with an image span
+    win, _, _ = prefill_windows(prefill, 1, T, spans=[(40, 5)])
+    kv16 = prepass(prefill, win, eg.KV_BF16)
+    hidden = synth.hidden_bf16(prefill.w, T)
+    ctx = prefill.model.ctx
+    d_h = to_dev(hidden)
+    d_g = torch.full((T, prefill.w.hc), float("nan"), device="cuda")
+    eg.engram_gate_bf16kv(ctx, 0, to_dev(kv16), to_dev(win), T, d_h, d_g)
+    eg.engram_sync(ctx)
+    got = from_dev(d_h, np.uint16)
+    gates = d_g.cpu().numpy()
+    g = geom(prefill.w)
+    sample = [0, 39, 40, 44, 45, T // 2, T - 1]
+    kv64 = bf16_f64(kv16[sample])
+    for i, t in enumerate(sample):
+        _, exp_h, exp_g = O.gate(g, kv64[i], int(win[t][0]), hidden[t], prefill.wq[0],
+                                 prefill.wk[0])
+        check_hidden(got[t], exp_h, f"token {t}")
+        assert np.abs(gates[t] - exp_g).max() <= 1e-3
+    assert np.array_equal(got[40:45], hidden[40:45])  # image rows untouched
