@@ -432,6 +432,12 @@ def main():
     e2e_value = dist.sum(float(T * e2e_steps)) / e2e_s
     eg.engram_sync(ctx, sptr)
 
+    # the peak to read the kernel against: the burst figure for a short run, the
+    # sustained one for a run long enough to meet the power cap (seen in the
+    # clock samples of the timed region)
+    capped = "sw_power_cap" in clk.get("reasons", [])
+    peak_tc = peaks["bf16_sus"] if capped else peaks["bf16"]
+    peak_kind = "sustained (the timed run met the power cap)" if capped else "burst"
     line = {
         "metric": "Engram tokens/s per layer (prefill, decode); gather HBM GB/s; wkv TC util %",
         "value": value, "unit": "tokens/s", "n_gpus": dist.world, "steps": args.steps,
@@ -442,12 +448,13 @@ def main():
         "scaling": "weak", "vs_baseline": None, "dtype": "f16*f16->f32", "data": "synthetic",
         "config": dict(workload_config(w), table_rows=rows, parallelism=f"replicas x{dist.world}",
                        entry="engram_forward_staged"),
-        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16"],
-                     "unit": "TFLOP/s", "frac": achieved / peaks["bf16"],
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_tc,
+                     "unit": "TFLOP/s", "frac": achieved / peak_tc,
                      "traffic": GEMM_DRAM_BYTES,
                      "kernel": "engram_forward_staged: k_gather_stage + k_mma (TMA-fed A, gate "
                                "epilogue); time per call covers both launches",
-                     "peak_kind": f"bf16 dense burst, {peaks['src']}",
+                     "peak_kind": f"bf16 dense {peak_kind}, {peaks['src']}",
+                     "frac_of_burst": achieved / peaks["bf16"],
                      "frac_of_sustained": achieved / peaks["bf16_sus"],
                      "flop_per_call": flops_call},
         "fused": {"entry": "engram_forward (one kernel: hash, gather and decode into the "
