@@ -26,21 +26,26 @@
  *       range; one key per hyper-connection branch and one shared value;
  *       sigmoid gate on the normalised dot; masked positions pass through.
  *
- * Readings taken where the pages are silent (each is listed in the design doc):
- *  - primes: strictly increasing primes > bucket_base, bucket order
- *    b = (n - min_n) * heads + head, layers in order, no prime reused by a
- *    later layer; offsets are prefix sums of the primes.
- *  - multipliers: a build convention (Philox4x32-10 keyed by the layer seed,
- *    one odd multiplier per n-gram position shared by all buckets of the
- *    layer, bounded so that no product with a compressed id wraps).
- *    PARITY UNPINNED against the real model: the pages print no multiplier.
- *  - table contents: a build convention, a Philox4x32-10 function of
- *    (seed, row, column).  PARITY UNPINNED against the real model (no row is
- *    printed); pinned to the published Philox known-answer vectors.
- *  - history before the first token holds pad_cid (engram_pad_id = 0).
+ * Readings taken where the pages are silent, each with the passage it rests on:
+ *  - primes [P4 "동작 방식", P2 row counts]: strictly increasing primes >
+ *    bucket_base, bucket order b = (n - min_n) * heads + head, layers in
+ *    order, no prime reused by a later layer; offsets are prefix sums of the
+ *    primes.  With bucket_base 16,000,000 this gives the row counts P2 prints.
+ *  - multipliers [P4 "동작 방식", P1 "第一步"]: a build convention
+ *    (Philox4x32-10 keyed by the layer seed, one odd multiplier per n-gram
+ *    position shared by all buckets of the layer, bounded so that no product
+ *    with a compressed id wraps).  PARITY UNPINNED against the real model:
+ *    the pages print no multiplier.  orc_hash itself takes a general table
+ *    and is pinned to hand-worked values (tests/golden/hash_worked.txt).
+ *  - table contents [P1 "第二步"]: a build convention, a Philox4x32-10
+ *    function of (seed, row, column).  PARITY UNPINNED against the real model
+ *    (no row is printed); pinned to the published Philox known-answer vectors.
+ *  - history before the first token holds pad_cid [P3: engram_pad_id = 0].
  *  - an n-gram containing DEAD yields a masked (all-zero) row for each of its
- *    heads; a row whose own token is DEAD (an image row) is not gated.
- *  - RMS-norm epsilon = 1e-6, inside the square root.
+ *    heads; a row whose own token is DEAD (an image row) is not gated
+ *    [P1 "第四步", P4 "동작 방식"].
+ *  - RMS-norm epsilon = 1e-6, inside the square root [P1 "第三步" prints no
+ *    epsilon; 1e-6 is the gate's own floor constant].
  */
 #ifndef ENGRAM_ORACLE_H
 #define ENGRAM_ORACLE_H

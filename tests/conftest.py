@@ -7,17 +7,11 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-GOLDEN = os.path.join(ROOT, "tests", "golden")
+from golden_io import read_golden  # noqa: E402
 
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built library")
-
-
-def read_golden(name: str):
-    """Non-comment lines of a golden fixture, split on whitespace."""
-    with open(os.path.join(GOLDEN, name)) as f:
-        return [ln.split() for ln in f if ln.strip() and not ln.startswith("#")]
 
 
 @pytest.fixture(scope="session")

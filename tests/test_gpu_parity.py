@@ -13,6 +13,7 @@ import torch
 import engram_gram_conditional_gb300 as eg
 import oracle as O
 import synth
+from golden_io import load_hash_worked
 from helpers import (bf16_f64, check_hidden, check_kv, from_dev, geom, prefill_windows,
                      setup_workload, to_dev)
 
@@ -131,6 +132,30 @@ def test_hash_full_geometry_bit_exact(prefill):
     rng = np.random.default_rng(1)
     for t in [0, 1, 2, 3, 2047] + rng.integers(0, 2048, 59).tolist():
         assert np.array_equal(emb[t], O.gather(g, prefill.w.table_seeds[0], rows[t])), t
+
+
+def test_hash_hand_worked_values_on_gpu():
+    # the hand-worked fixture (two general multiplier tables over primes
+    # 1009..1033) through engram_hash: products above 2^32, products that wrap
+    # 2^64 and a DEAD slot, against values worked out by hand
+    primes, offsets, tables, cases = load_hash_worked()
+    tmap = np.arange(4096, dtype=np.uint32) % 1000
+    ctx = eg.engram_ctx_create(4096, 1000, tmap, [1], [1000], heads=2, row_dim=32, hc=1, d=256)
+    try:
+        _, prime, offset, _ = eg.engram_layer_params(ctx, 0, 6)
+        assert np.array_equal(prime, primes) and np.array_equal(offset, offsets)
+        for name in sorted(tables):
+            eg.engram_layer_set_multipliers(ctx, 0, tables[name])
+            mine = [(w, r) for t, w, r in cases if t == name]
+            # a ragged batch: the worked windows repeated 37 times
+            win = np.array([w for w, _ in mine] * 37, np.uint32)
+            want = np.array([r for _, r in mine] * 37, np.uint32)
+            d_rows = torch.empty((len(win), 6), dtype=torch.int32, device="cuda")
+            eg.engram_hash(ctx, 0, to_dev(win), len(win), d_rows)
+            torch.cuda.synchronize()
+            assert np.array_equal(from_dev(d_rows, np.uint32), want), name
+    finally:
+        eg.engram_ctx_destroy(ctx)
 
 
 # ---- a4: projection ---------------------------------------------------------------------

@@ -13,6 +13,7 @@ import pytest
 import torch
 
 import oracle as O
+from golden_io import load_hash_worked
 
 TINY = O.Geom(vocab=4096, vc=1000, heads=2, row_dim=32, hc=2, d=256)
 FULL = O.Geom(vocab=129_280, vc=100_000)
@@ -294,6 +295,21 @@ def test_hash_general_multiplier_table():
     assert not np.array_equal(r1, r2)
     for b in range(G7.nb):
         assert int(p.offset[b]) <= r2[b] < int(p.offset[b] + p.prime[b])
+
+
+G_WORKED = O.Geom(vocab=4096, vc=1000, heads=2, row_dim=32, hc=1, d=32)
+
+
+def test_hash_hand_worked_values():
+    # x = XOR of the products c_{t-j} m[b][j] (wrapping 64-bit), row = offset +
+    # x mod prime: every value worked by hand in the fixture, including products
+    # above 2^32, products that wrap 2^64 and an n-gram holding DEAD
+    primes, offsets, tables, cases = load_hash_worked()
+    assert len(cases) == 5 and G_WORKED.nb == len(primes)
+    for name, win, want in cases:
+        p = O.LayerParams(tables[name], primes, offsets, int(offsets[-1] + primes[-1]))
+        got = O.hash_rows(G_WORKED, p, np.array(win, np.uint32))
+        assert got.tolist() == want, (name, win)
 
 
 # --------------------------------------------------------------------------
