@@ -51,15 +51,28 @@ class EngramLayerSet:
         return self.params[layer][3]
 
     def bind(self, layer: int, table_seed: int, wkv, wq, wk, host_table: bool = False,
-             stream=None, flags: int = 0):
+             stream=None, flags: int = 0, table=None):
         """Allocate and fill the layer's table, upload wkv / w_q / w_k, bind.
 
         The table is MXFP8 (codes and E8M0 scales), or with flags containing
-        BIND_TABLE_BF16 the same rows stored as BF16 values without scales."""
+        BIND_TABLE_BF16 the same rows stored as BF16 values without scales.
+        ``table``: instead of the generated contents, a host MXFP8 table
+        (codes uint8 [R][row_dim], scales uint8 [R][row_dim / 32]) with R at
+        least the layer's row count, copied as it is (rows past the layer's
+        count stay allocated but outside the bound table)."""
         rows = self.rows(layer)
         rd = self.geom["row_dim"]
         where = dict(pin_memory=True) if host_table else dict(device=self.device)
-        if flags & BIND_TABLE_BF16:
+        if table is not None:
+            codes = np.ascontiguousarray(table[0], np.uint8).reshape(-1)
+            scl = np.ascontiguousarray(table[1], np.uint8).reshape(-1)
+            assert codes.size >= rows * rd and scl.size * 32 == codes.size and not flags & BIND_TABLE_BF16
+            table_t = torch.zeros(_round16(codes.size), dtype=torch.uint8, **where)
+            scales = torch.zeros(_round16(scl.size), dtype=torch.uint8, **where)
+            table_t[:codes.size].copy_(torch.from_numpy(codes))
+            scales[:scl.size].copy_(torch.from_numpy(scl))
+            table = table_t
+        elif flags & BIND_TABLE_BF16:
             table = torch.empty(_round16(rows * rd * 2), dtype=torch.uint8, **where)
             scales = None
             engram_table_fill_bf16(self.ctx, table_seed, table, 0, rows, stream)

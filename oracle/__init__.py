@@ -108,11 +108,15 @@ def lib():
             "orc_windows": (C.c_int, [gp, u32p, i32p, u8p, C.c_int64, u32p]),
             "orc_hash": (None, [gp, u64p, u64p, u64p, u32p, u32p]),
             "orc_gather": (None, [gp, C.c_uint64, u32p, u16p]),
+            "orc_gather_table": (C.c_int, [gp, u8p, u8p, C.c_uint64, u32p, u16p]),
             "orc_project": (None, [gp, u16p, u16p, f64p]),
             "orc_gate": (None, [gp, f64p, C.c_uint32, u16p, f32p, f32p, f64p, u16p, f64p]),
             "orc_forward": (C.c_int, [gp, C.c_uint64, u64p, u64p, u64p, u16p, f32p, f32p, u32p,
                                       u16p, i64p, C.c_int64, C.c_int, u32p, u16p, f64p, f64p,
                                       f64p, u16p]),
+            "orc_forward_table": (C.c_int, [gp, u8p, u8p, C.c_uint64, u64p, u64p, u64p, u16p,
+                                            f32p, f32p, u32p, u16p, i64p, C.c_int64, C.c_int,
+                                            u32p, u16p, f64p, f64p, f64p, u16p]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(_lib, name)
@@ -239,6 +243,22 @@ def gather(g: Geom, seed: int, rows) -> np.ndarray:
     return e
 
 
+def gather_table(g: Geom, codes, scales, rows) -> np.ndarray:
+    """Dequantised vector of one token's rows read from a table held in memory:
+    codes uint8 [R][row_dim], scales uint8 [R][row_dim / 32]."""
+    c = _c(codes, np.uint8)
+    sc = _c(scales, np.uint8)
+    nrows = c.size // g.row_dim
+    assert c.size == nrows * g.row_dim and sc.size >= nrows * (g.row_dim // 32)
+    r = _c(rows, np.uint32)
+    e = np.zeros(g.K, np.uint16)
+    gc = g.c()
+    if lib().orc_gather_table(C.byref(gc), _p(c, C.c_uint8), _p(sc, C.c_uint8), nrows,
+                              _p(r, C.c_uint32), _p(e, C.c_uint16)) != 0:
+        raise ValueError("row index outside the table")
+    return e
+
+
 def project(g: Geom, w_bf16: np.ndarray, e_bf16) -> np.ndarray:
     w = _c(w_bf16, np.uint16)
     e = _c(e_bf16, np.uint16)
@@ -266,8 +286,11 @@ def gate(g: Geom, kv, c_t: int, h_bf16, wq, wk):
 
 def forward(g: Geom, seed: int, p: LayerParams, w_bf16, wq, wk, windows_, hidden_bf16, idx,
             nthreads: int = 1, want_e: bool = False, want_kv: bool = False,
-            want_h64: bool = True) -> dict:
-    """The whole step on the positions ``idx`` (threads over positions)."""
+            want_h64: bool = True, table=None) -> dict:
+    """The whole step on the positions ``idx`` (threads over positions).
+
+    ``table``: None (rows from the generated contents of ``seed``) or a pair
+    (codes uint8 [R][row_dim], scales uint8 [R][row_dim / 32]) held in memory."""
     w = _c(w_bf16, np.uint16)
     q = _c(wq, np.float32)
     k = _c(wk, np.float32)
@@ -288,13 +311,19 @@ def forward(g: Geom, seed: int, p: LayerParams, w_bf16, wq, wk, windows_, hidden
         "h_bf16": np.zeros((n, g.hc, g.d), np.uint16),
     }
     gc = g.c()
-    rc = lib().orc_forward(C.byref(gc), seed, _p(p.mult, C.c_uint64), _p(p.prime, C.c_uint64),
-                           _p(p.offset, C.c_uint64), _p(w, C.c_uint16), _p(q, C.c_float),
-                           _p(k, C.c_float), _p(win, C.c_uint32), _p(hid, C.c_uint16),
-                           _p(ix, C.c_int64), n, nthreads, _p(out["rows"], C.c_uint32),
-                           _p(out["e"], C.c_uint16), _p(out["kv"], C.c_double),
-                           _p(out["gates"], C.c_double), _p(out["h"], C.c_double),
-                           _p(out["h_bf16"], C.c_uint16))
+    tail = (_p(p.mult, C.c_uint64), _p(p.prime, C.c_uint64), _p(p.offset, C.c_uint64),
+            _p(w, C.c_uint16), _p(q, C.c_float), _p(k, C.c_float), _p(win, C.c_uint32),
+            _p(hid, C.c_uint16), _p(ix, C.c_int64), n, nthreads, _p(out["rows"], C.c_uint32),
+            _p(out["e"], C.c_uint16), _p(out["kv"], C.c_double), _p(out["gates"], C.c_double),
+            _p(out["h"], C.c_double), _p(out["h_bf16"], C.c_uint16))
+    if table is None:
+        rc = lib().orc_forward(C.byref(gc), seed, *tail)
+    else:
+        codes, scales = _c(table[0], np.uint8), _c(table[1], np.uint8)
+        nrows = codes.size // g.row_dim
+        assert scales.size >= nrows * (g.row_dim // 32)
+        rc = lib().orc_forward_table(C.byref(gc), _p(codes, C.c_uint8), _p(scales, C.c_uint8),
+                                     nrows, *tail)
     if rc != 0:
         raise RuntimeError("orc_forward failed")
     return out

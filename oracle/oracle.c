@@ -289,6 +289,31 @@ void orc_gather(const orc_geom* g, uint64_t seed, const uint32_t* rows, uint16_t
     }
 }
 
+/* The same gather from a table held in memory (codes [nrows][row_dim],
+ * scales [nrows][row_dim/32]) rather than the generated contents.  Returns -1,
+ * leaving e unspecified, if an unmasked row index is >= nrows (the pages define
+ * no row outside the table). */
+int orc_gather_table(const orc_geom* g, const uint8_t* codes, const uint8_t* scales,
+                     uint64_t nrows, const uint32_t* rows, uint16_t* e)
+{
+    uint32_t nb = (g->max_n - g->min_n + 1) * g->heads;
+    uint32_t groups = g->row_dim / 32u;
+    for (uint32_t b = 0; b < nb; ++b) {
+        if (rows[b] != ORC_MASKED && rows[b] >= nrows) return -1;
+        for (uint32_t i = 0; i < g->row_dim; ++i) {
+            uint16_t out = 0;
+            if (rows[b] != ORC_MASKED) {
+                uint64_t r = rows[b];
+                double v = orc_e4m3_value(codes[r * g->row_dim + i]) *
+                           orc_e8m0_value(scales[r * groups + i / 32u]);
+                out = orc_bf16_from_double(v);
+            }
+            e[b * g->row_dim + i] = out;
+        }
+    }
+    return 0;
+}
+
 /* ------------------------------------------------------------------------ */
 /* wkv projection (P1 "第二步"): kv = W e with W of shape [(hc+1) d][K].     */
 /* ------------------------------------------------------------------------ */
@@ -365,6 +390,8 @@ typedef struct fwd_job {
     const uint32_t* windows;
     const uint16_t* hidden;
     const int64_t* idx;
+    const uint8_t *codes, *scales; /* explicit table, or NULL: generated contents */
+    uint64_t nrows;
     int64_t begin, end;
     uint32_t* rows_out;
     uint16_t* e_out;
@@ -396,7 +423,14 @@ static void* fwd_worker(void* arg)
         const uint32_t* win = j->windows + t * 4;
         uint32_t* rows = j->rows_out + (uint64_t)s * nb;
         orc_hash(g, j->mult, j->prime, j->offset, win, rows);
-        orc_gather(g, j->seed, rows, e);
+        if (!j->codes)
+            orc_gather(g, j->seed, rows, e);
+        else if (orc_gather_table(g, j->codes, j->scales, j->nrows, rows, e) != 0) {
+            free(e);
+            free(kv);
+            j->status = -1;
+            return NULL;
+        }
         orc_project(g, j->w, e, kv);
         orc_gate(g, kv, win[0], j->hidden + (uint64_t)t * HD, j->wq, j->wk,
                  j->h_out ? j->h_out + (uint64_t)s * HD : NULL, j->h_bf16_out + (uint64_t)s * HD,
@@ -410,11 +444,13 @@ static void* fwd_worker(void* arg)
     return NULL;
 }
 
-int orc_forward(const orc_geom* g, uint64_t seed, const uint64_t* mult, const uint64_t* prime,
-                const uint64_t* offset, const uint16_t* w, const float* wq, const float* wk,
-                const uint32_t* windows, const uint16_t* hidden, const int64_t* idx, int64_t nidx,
-                int nthreads, uint32_t* rows_out, uint16_t* e_out, double* kv_out,
-                double* gates_out, double* h_out, uint16_t* h_bf16_out)
+static int forward_impl(const orc_geom* g, uint64_t seed, const uint8_t* codes,
+                        const uint8_t* scales, uint64_t nrows, const uint64_t* mult,
+                        const uint64_t* prime, const uint64_t* offset, const uint16_t* w,
+                        const float* wq, const float* wk, const uint32_t* windows,
+                        const uint16_t* hidden, const int64_t* idx, int64_t nidx, int nthreads,
+                        uint32_t* rows_out, uint16_t* e_out, double* kv_out, double* gates_out,
+                        double* h_out, uint16_t* h_bf16_out)
 {
     if (nthreads < 1) nthreads = 1;
     if (nthreads > nidx) nthreads = nidx > 0 ? (int)nidx : 1;
@@ -430,6 +466,7 @@ int orc_forward(const orc_geom* g, uint64_t seed, const uint64_t* mult, const ui
         j->g = g; j->seed = seed; j->mult = mult; j->prime = prime; j->offset = offset;
         j->w = w; j->wq = wq; j->wk = wk; j->windows = windows; j->hidden = hidden;
         j->idx = idx;
+        j->codes = codes; j->scales = scales; j->nrows = nrows;
         j->begin = nidx * i / nthreads;
         j->end = nidx * (i + 1) / nthreads;
         j->rows_out = rows_out; j->e_out = e_out; j->kv_out = kv_out;
@@ -458,4 +495,27 @@ int orc_forward(const orc_geom* g, uint64_t seed, const uint64_t* mult, const ui
     free(jobs);
     free(th);
     return rc;
+}
+
+int orc_forward(const orc_geom* g, uint64_t seed, const uint64_t* mult, const uint64_t* prime,
+                const uint64_t* offset, const uint16_t* w, const float* wq, const float* wk,
+                const uint32_t* windows, const uint16_t* hidden, const int64_t* idx, int64_t nidx,
+                int nthreads, uint32_t* rows_out, uint16_t* e_out, double* kv_out,
+                double* gates_out, double* h_out, uint16_t* h_bf16_out)
+{
+    return forward_impl(g, seed, NULL, NULL, 0, mult, prime, offset, w, wq, wk, windows, hidden,
+                        idx, nidx, nthreads, rows_out, e_out, kv_out, gates_out, h_out,
+                        h_bf16_out);
+}
+
+int orc_forward_table(const orc_geom* g, const uint8_t* codes, const uint8_t* scales,
+                      uint64_t nrows, const uint64_t* mult, const uint64_t* prime,
+                      const uint64_t* offset, const uint16_t* w, const float* wq, const float* wk,
+                      const uint32_t* windows, const uint16_t* hidden, const int64_t* idx,
+                      int64_t nidx, int nthreads, uint32_t* rows_out, uint16_t* e_out,
+                      double* kv_out, double* gates_out, double* h_out, uint16_t* h_bf16_out)
+{
+    return forward_impl(g, 0, codes, scales, nrows, mult, prime, offset, w, wq, wk, windows,
+                        hidden, idx, nidx, nthreads, rows_out, e_out, kv_out, gates_out, h_out,
+                        h_bf16_out);
 }

@@ -113,6 +113,12 @@ void orc_hash(const orc_geom* g, const uint64_t* mult, const uint64_t* prime,
 void orc_gather(const orc_geom* g, uint64_t seed, const uint32_t* rows /*[nb]*/,
                 uint16_t* e /*[K]*/);
 
+/* The same from a table held in memory: codes [nrows][row_dim] (E4M3),
+ * scales [nrows][row_dim/32] (E8M0).  Returns -1 if an unmasked index is
+ * >= nrows, else 0. */
+int orc_gather_table(const orc_geom* g, const uint8_t* codes, const uint8_t* scales,
+                     uint64_t nrows, const uint32_t* rows /*[nb]*/, uint16_t* e /*[K]*/);
+
 /* kv[o] = sum_i W[o][i] * e[i] in fp64.  W is BF16 [N][K]. */
 void orc_project(const orc_geom* g, const uint16_t* w /*[N][K]*/, const uint16_t* e /*[K]*/,
                  double* kv /*[N]*/);
@@ -133,6 +139,17 @@ int orc_forward(const orc_geom* g, uint64_t seed, const uint64_t* mult,
                 const uint16_t* hidden, const int64_t* idx, int64_t nidx, int nthreads,
                 uint32_t* rows_out, uint16_t* e_out, double* kv_out, double* gates_out,
                 double* h_out, uint16_t* h_bf16_out);
+
+/* orc_forward with the rows read from a table held in memory (as
+ * orc_gather_table) instead of the generated contents.  Returns -1 if a row
+ * index falls outside the table. */
+int orc_forward_table(const orc_geom* g, const uint8_t* codes, const uint8_t* scales,
+                      uint64_t nrows, const uint64_t* mult, const uint64_t* prime,
+                      const uint64_t* offset, const uint16_t* w, const float* wq,
+                      const float* wk, const uint32_t* windows, const uint16_t* hidden,
+                      const int64_t* idx, int64_t nidx, int nthreads, uint32_t* rows_out,
+                      uint16_t* e_out, double* kv_out, double* gates_out, double* h_out,
+                      uint16_t* h_bf16_out);
 
 #ifdef __cplusplus
 }

@@ -76,6 +76,18 @@ def norm_weights(hc: int, d: int, seed: int, stream: int) -> np.ndarray:
     return (1.0 + 0.1 * g.standard_normal((hc, d))).astype(np.float32)
 
 
+def mxfp8_table(rows: int, row_dim: int, seed: int, scale_lo: int, scale_hi: int,
+                stream: int = 50):
+    """A host MXFP8 table: codes uint8 [rows][row_dim] uniform over the 254
+    finite E4M3 codes (0x7F and 0xFF excluded) and E8M0 exponents uint8
+    [rows][row_dim / 32] uniform over [scale_lo, scale_hi]."""
+    g = _rng(seed, stream)
+    idx = g.integers(0, 254, (rows, row_dim), dtype=np.uint16)
+    codes = (idx + (idx >= 127)).astype(np.uint8)
+    scales = g.integers(scale_lo, scale_hi + 1, (rows, row_dim // 32), dtype=np.uint16)
+    return codes, scales.astype(np.uint8)
+
+
 @dataclass
 class Workload:
     """One benchmark / parity configuration (sizes as the pages' workloads)."""

@@ -66,26 +66,43 @@ class Setup:
     wq: list
     wk: list
     oparams: list
+    tables: list = None  # per layer: None (generated contents) or host (codes, scales)
+
+    def table(self, layer=0):
+        return None if self.tables is None else self.tables[layer]
+
+    def oracle_forward(self, layer, win, hidden, idx, **kw):
+        """The oracle's step on positions idx, over this layer's table."""
+        return O.forward(geom(self.w), self.w.table_seeds[layer], self.oparams[layer],
+                         self.W[layer], self.wq[layer], self.wk[layer], win, hidden,
+                         np.asarray(idx), table=self.table(layer), **kw)
 
     def close(self):
         self.model.close()
         torch.cuda.empty_cache()
 
 
-def setup_workload(name: str, layers=None, host_table=False, flags=0, **overrides) -> Setup:
+def setup_workload(name: str, layers=None, host_table=False, flags=0, tables=None, wkv=None,
+                   **overrides) -> Setup:
+    """Bind the workload's layers.  tables / wkv: optional {layer: host MXFP8
+    table (codes, scales)} / {layer: BF16 wkv bits} in place of the generated
+    table contents / the synthetic wkv."""
     import dataclasses
 
     w = dataclasses.replace(synth.WORKLOADS[name], **overrides) if overrides else \
         synth.WORKLOADS[name]
+    tables = tables or {}
+    wkv = wkv or {}
     tmap = synth.token_map(w.vocab, w.vc, w.seed)
     model = EngramLayerSet.from_workload(w, tmap, device="cuda")
     layers = range(len(w.hash_seeds)) if layers is None else layers
     W, WQ, WK = [], [], []
     for l in range(len(w.hash_seeds)):
         if l in layers:
-            Wl = synth.wkv_bf16(w, l)
+            Wl = wkv[l] if l in wkv else synth.wkv_bf16(w, l)
             q, k = synth.wq_wk(w, l)
-            model.bind(l, w.table_seeds[l], Wl, q, k, host_table=host_table, flags=flags)
+            model.bind(l, w.table_seeds[l], Wl, q, k, host_table=host_table, flags=flags,
+                       table=tables.get(l))
         else:
             Wl = q = k = None
         W.append(Wl)
@@ -94,7 +111,8 @@ def setup_workload(name: str, layers=None, host_table=False, flags=0, **override
     g = geom(w)
     op = [O.layer_params(g, w.hash_seeds, w.bucket_bases, l) for l in range(len(w.hash_seeds))]
     torch.cuda.synchronize()
-    return Setup(w, tmap, model, W, WQ, WK, op)
+    tl = [tables.get(l) for l in range(len(w.hash_seeds))] if tables else None
+    return Setup(w, tmap, model, W, WQ, WK, op, tl)
 
 
 def to_dev(a: np.ndarray) -> torch.Tensor:

@@ -1,7 +1,10 @@
 """Parity at the full sizes of the decode, long-prefill and host-table workloads.
 
-Indices and table rows are checked bit-exact on every position the oracle
-can afford; hidden states and gates on sampled positions.  The same windows
+Row indices are checked bit-exact on every position, dequantised rows on every
+position of a decode step and on a random sample of at least 4,096 positions
+of the long prefill; hidden states and gates against the oracle on at least
+4,096 token rows per workload (every row of 16 decode steps, a random sample
+of the prefills; the sample seeds are fixed and printed).  The same windows
 feed every layer of the two-layer workload: tokens enter the history once.
 """
 import dataclasses
@@ -40,12 +43,27 @@ def forward(s, win, hidden, layer, staged):
     return from_dev(d_h, np.uint16), d_g.cpu().numpy()
 
 
-def check_sample(s, layer, win, hidden, h, gates, sample, what):
-    ref = O.forward(geom(s.w), s.w.table_seeds[layer], s.oparams[layer], s.W[layer], s.wq[layer],
-                    s.wk[layer], win, hidden, np.asarray(sample), nthreads=16)
+def check_sample(s, layer, win, hidden, h, gates, sample, what, ref=None):
+    if ref is None:
+        ref = s.oracle_forward(layer, win, hidden, sample, nthreads=16, want_h64=False)
     check_hidden(h[sample], ref["h_bf16"], what)
     assert np.abs(gates[sample] - ref["gates"]).max() <= 1e-3, what
     return ref
+
+
+def all_rows_oracle(s, layer, win):
+    g = geom(s.w)
+    return np.stack([O.hash_rows(g, s.oparams[layer], w_) for w_ in win])
+
+
+def random_sample(T, n, seed, must=()):
+    rng = np.random.default_rng(seed)
+    pick = rng.choice(T, size=n, replace=False)
+    print(f"oracle sample: {n} of {T} positions, numpy default_rng({seed})")
+    return np.unique(np.concatenate([pick, np.asarray(must, np.int64)]))
+
+
+DECODE_STEPS = 16  # x 256 sessions = 4,096 token rows against the oracle
 
 
 def test_decode_256_sessions_on_the_384m_row_table():
@@ -54,28 +72,34 @@ def test_decode_256_sessions_on_the_384m_row_table():
         w = s.w
         assert s.model.rows(0) == 384_006_168
         S = w.sessions
-        streams = np.stack([synth.session_tokens(w, i, w.history + 3) for i in range(S)])
+        streams = np.stack([synth.session_tokens(w, i, w.history + DECODE_STEPS)
+                            for i in range(S)])
         sess = [eg.engram_session_create(s.model.ctx) for _ in range(S)]
         for i, ss in enumerate(sess):
             eg.engram_session_append(ss, streams[i, :w.history])
         hidden = synth.hidden_bf16(w, S)
         g = geom(w)
-        for step in range(3):
+        for step in range(DECODE_STEPS):
             win = eg.engram_batch_append(sess, streams[:, w.history + step])
             # every session's window equals the oracle's window of its whole stream
-            for i in range(0, S, 17):
+            for i in range(S):
                 ref_w = O.windows(g, s.tmap, streams[i, :w.history + step + 1])[-1]
-                assert np.array_equal(win[i], ref_w)
-            # every row index of the step, bit-exact
+                assert np.array_equal(win[i], ref_w), (step, i)
+            ref = s.oracle_forward(0, win, hidden, np.arange(S), nthreads=16, want_e=True,
+                                   want_h64=False)
+            # every row index and every dequantised row of the step, bit-exact
             d_rows = torch.empty((S, w.nb), dtype=torch.int32, device="cuda")
             eg.engram_hash(s.model.ctx, 0, to_dev(win), S, d_rows)
-            rows = from_dev(d_rows, np.uint32)
-            for i in range(S):
-                assert np.array_equal(rows[i], O.hash_rows(g, s.oparams[0], win[i])), (step, i)
+            d_emb = torch.empty((S, w.K), dtype=torch.int16, device="cuda")
+            eg.engram_gather_dequant(s.model.ctx, 0, d_rows, S, d_emb)
+            eg.engram_sync(s.model.ctx)
+            assert np.array_equal(from_dev(d_rows, np.uint32), ref["rows"]), step
+            assert np.array_equal(from_dev(d_emb, np.uint16), ref["e"]), step
+            # hidden and gates of every session
             for staged in (False, True):
                 h, gates = forward(s, win, hidden, 0, staged)
-                check_sample(s, 0, win, hidden, h, gates, [0, 1, 100, 255, 128 + step],
-                             f"decode step {step} staged={staged}")
+                check_sample(s, 0, win, hidden, h, gates, np.arange(S),
+                             f"decode step {step} staged={staged}", ref=ref)
             hidden = h
         for ss in sess:
             eg.engram_session_destroy(ss)
@@ -97,42 +121,62 @@ def test_long_prefill_two_layers_one_history():
         assert np.array_equal(win, O.windows(g, s.tmap, toks, im))
         hidden = synth.hidden_bf16(w, T)
         spans = [st for st, _ in w.image_spans]
-        sample = sorted({0, 1, 2, 3, T - 1} | {p + d for p in spans for d in (-1, 0, 1023, 1024, 1025, 1026)}
-                        | set(np.random.default_rng(3).integers(0, T, 6).tolist()))
+        edges = [0, 1, 2, 3, T - 1] + [p + d for p in spans for d in (-1, 0, 1023, 1024, 1025, 1026)]
+        sample = random_sample(T, 4096, 50_032, edges)
+        image = win[:, 0] == eg.DEAD
+        assert image.sum() == 3 * 1024
         for layer in range(2):
-            p = s.oparams[layer]
-            # both layers hash the same windows with their own parameters
+            # both layers hash the same windows with their own parameters: every index
             d_rows = torch.empty((T, w.nb), dtype=torch.int32, device="cuda")
             eg.engram_hash(s.model.ctx, layer, to_dev(win), T, d_rows)
+            d_emb = torch.empty((T, w.K), dtype=torch.int16, device="cuda")
+            eg.engram_gather_dequant(s.model.ctx, layer, d_rows, T, d_emb)
             eg.engram_sync(s.model.ctx)
             rows = from_dev(d_rows, np.uint32)
-            for t in sample:
-                assert np.array_equal(rows[t], O.hash_rows(g, p, win[t])), (layer, t)
+            assert np.array_equal(rows, all_rows_oracle(s, layer, win)), layer
+            ref = s.oracle_forward(layer, win, hidden, sample, nthreads=16, want_e=True,
+                                   want_h64=False)
+            # the sampled positions' dequantised rows, bit-exact
+            emb = from_dev(d_emb[torch.from_numpy(sample).cuda()], np.uint16)
+            assert np.array_equal(emb, ref["e"]), layer
+            del d_emb
             for staged in (True, False):
                 h, gates = forward(s, win, hidden, layer, staged)
-                ref = check_sample(s, layer, win, hidden, h, gates, sample,
-                                   f"layer {layer} staged={staged}")
-                image = win[:, 0] == eg.DEAD
-                assert image.sum() == 3 * 1024
+                check_sample(s, layer, win, hidden, h, gates, sample,
+                             f"layer {layer} staged={staged}", ref=ref)
                 assert np.array_equal(h[image], hidden[image])
         assert not np.array_equal(s.oparams[0].prime, s.oparams[1].prime)
     finally:
         s.close()
 
 
-def test_host_table_read_through_uva():
-    # the 384M-row table would pin 101 GB of host memory; pinned memory cannot
-    # be paged out, so the test keeps well inside the host's RAM: 64M rows
+HOST_ROWS_FULL = 384_006_168   # the stated table: 101.4 GB of codes and scales, pinned
+
+
+def host_table_bases():
+    """The stated 384M-row table when the host can pin it with room to spare,
+    else a 64M-row table (bucket base 2,666,666)."""
     with open("/proc/meminfo") as f:
         info = {ln.split(":")[0]: int(ln.split()[1]) * 1024 for ln in f if ":" in ln}
     avail = info.get("MemAvailable", 0)
-    if avail < 48 * 2**30:
-        pytest.skip(f"only {avail / 2**30:.0f} GB of host memory available")
-    s = setup_workload("host_table_8x1024", host_table=True, bucket_bases=[2_666_666])
+    need_full = HOST_ROWS_FULL * 264
+    if avail >= need_full + 48 * 2**30:
+        return [16_000_000], avail
+    if avail >= 48 * 2**30:
+        return [2_666_666], avail
+    pytest.skip(f"only {avail / 2**30:.0f} GB of host memory available")
+
+
+def test_host_table_read_through_uva():
+    bases, avail = host_table_bases()
+    print(f"host memory available {avail / 2**30:.0f} GB; bucket base {bases[0]}")
+    s = setup_workload("host_table_8x1024", host_table=True, bucket_bases=bases)
     try:
         w = s.w
         t = s.model.tensors[0]
         assert not t["table"].is_cuda and t["table"].is_pinned()
+        if bases[0] == 16_000_000:
+            assert s.model.rows(0) == HOST_ROWS_FULL
         T = w.sessions * w.tokens_per_session
         wins = []
         for i in range(w.sessions):
@@ -146,19 +190,20 @@ def test_host_table_read_through_uva():
             c, sc = O.table_row(w.table_seeds[0], r, 256)
             assert np.array_equal(t["table"][r * 256:(r + 1) * 256].numpy(), c)
             assert np.array_equal(t["scales"][r * 8:(r + 1) * 8].numpy(), sc)
-        # the unfused gather through UVA, bit-exact
-        g = geom(w)
+        # the unfused gather through UVA: every index, and the sampled rows, bit-exact
         d_rows = torch.empty((T, w.nb), dtype=torch.int32, device="cuda")
         eg.engram_hash(s.model.ctx, 0, to_dev(win), T, d_rows)
         d_emb = torch.empty((T, w.K), dtype=torch.int16, device="cuda")
         eg.engram_gather_dequant(s.model.ctx, 0, d_rows, T, d_emb)
         eg.engram_sync(s.model.ctx)
         rows, emb = from_dev(d_rows, np.uint32), from_dev(d_emb, np.uint16)
-        for tt in [0, 1023, 1024, 8191, 4000]:
-            assert np.array_equal(emb[tt], O.gather(g, w.table_seeds[0], rows[tt]))
+        assert np.array_equal(rows, all_rows_oracle(s, 0, win))
+        sample = random_sample(T, 4096, 8192, [0, 1023, 1024, 8191])
+        ref = s.oracle_forward(0, win, hidden, sample, nthreads=16, want_e=True, want_h64=False)
+        assert np.array_equal(emb[sample], ref["e"])
         for staged in (True, False):
             h, gates = forward(s, win, hidden, 0, staged)
-            check_sample(s, 0, win, hidden, h, gates, [0, 1023, 1024, 5000, 8191],
-                         f"host table staged={staged}")
+            check_sample(s, 0, win, hidden, h, gates, sample, f"host table staged={staged}",
+                         ref=ref)
     finally:
         s.close()

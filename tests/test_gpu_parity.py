@@ -262,24 +262,48 @@ def test_forward_tiny_all_tokens(tiny, tiny_bf16, path, entry, sessions, per, sp
     assert np.array_equal(h[allmasked], hidden[allmasked])
 
 
-@pytest.mark.parametrize("entry", ["fused", "staged"])
-def test_forward_full_geometry_sampled(prefill, entry):
+@pytest.fixture(scope="module")
+def prefill_ref(prefill):
+    """The oracle's step on every token of the 2,048-token prefill (16 threads)."""
     win, _, _ = prefill_windows(prefill, 1, 2048)
-    T = 2048
-    hidden = synth.hidden_bf16(prefill.w, T)
-    h, gates = run_forward(prefill, win, hidden, staged=entry == "staged")
-    sample = np.array([0, 1, 126, 127, 128, 129, 1023, 2046, 2047, 700])
+    hidden = synth.hidden_bf16(prefill.w, 2048)
     ref = O.forward(geom(prefill.w), prefill.w.table_seeds[0], prefill.oparams[0], prefill.W[0],
-                    prefill.wq[0], prefill.wk[0], win, hidden, sample, nthreads=8)
-    check_hidden(h[sample], ref["h_bf16"], "forward 2048")
-    assert np.abs(gates[sample] - ref["gates"]).max() <= 1e-3
-    # and the unfused chain on the GPU agrees with the fused kernel
+                    prefill.wq[0], prefill.wk[0], win, hidden, np.arange(2048), nthreads=16,
+                    want_e=True, want_h64=False)
+    return win, hidden, ref
+
+
+def test_gather_full_geometry_every_row(prefill, prefill_ref):
+    # every dequantised row of the 2,048 tokens (24 x 256 values each), bit-exact
+    win, _, ref = prefill_ref
+    rows, d_rows = gpu_rows(prefill, win)
+    assert np.array_equal(rows, ref["rows"])
+    emb = from_dev(gpu_emb(prefill, d_rows, 2048), np.uint16)
+    assert np.array_equal(emb, ref["e"])
+
+
+@pytest.mark.parametrize("entry", ["fused", "staged"])
+def test_forward_full_geometry_every_token(prefill, prefill_ref, entry):
+    # hidden and gates of all 2,048 tokens against the oracle
+    win, hidden, ref = prefill_ref
+    T = 2048
+    h, gates = run_forward(prefill, win, hidden, staged=entry == "staged")
+    check_hidden(h, ref["h_bf16"], f"forward 2048 {entry}")
+    assert np.abs(gates - ref["gates"]).max() <= 1e-3
+
+
+def test_prepass_and_gate_full_geometry_every_token(prefill, prefill_ref):
+    # the hidden-independent projection (a2-a4 fused) then the gate kernel
+    win, hidden, ref = prefill_ref
+    T = 2048
     d_kv = torch.empty((T, prefill.w.N), dtype=torch.float32, device="cuda")
     eg.engram_project_windows(prefill.model.ctx, 0, to_dev(win), T, d_kv)
     d_h = to_dev(hidden)
-    eg.engram_gate(prefill.model.ctx, 0, d_kv, to_dev(win), T, d_h)
+    d_g = torch.empty((T, prefill.w.hc), dtype=torch.float32, device="cuda")
+    eg.engram_gate(prefill.model.ctx, 0, d_kv, to_dev(win), T, d_h, d_g)
     eg.engram_sync(prefill.model.ctx)
-    check_hidden(h, from_dev(d_h, np.uint16), "fused vs chain")
+    check_hidden(from_dev(d_h, np.uint16), ref["h_bf16"], "project_windows + gate")
+    assert np.abs(d_g.cpu().numpy() - ref["gates"]).max() <= 1e-3
 
 
 @pytest.mark.parametrize("entry", ["fused", "staged"])

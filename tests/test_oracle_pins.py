@@ -13,6 +13,7 @@ import pytest
 import torch
 
 import oracle as O
+import synth
 from golden_io import load_hash_worked
 
 TINY = O.Geom(vocab=4096, vc=1000, heads=2, row_dim=32, hc=2, d=256)
@@ -347,6 +348,43 @@ def test_gather_full_rows_use_one_scale_per_32_values():
         fp8 = torch.from_numpy(codes).view(torch.float8_e4m3fn).double().numpy()
         sc = torch.from_numpy(scales).view(torch.float8_e8m0fnu).double().numpy()
         assert np.array_equal(seg, fp8 * np.repeat(sc, 32))
+
+
+@pytest.mark.parametrize("lo,hi", [(119, 127), (105, 127), (104, 127), (1, 254)])
+def test_gather_from_a_table_in_memory_against_torch(lo, hi):
+    # an explicit table with any E8M0 span: each value is torch's OCP E4M3
+    # decode times 2^(e - 127) rounded once to BF16 (exact for spans inside
+    # 2^-27..2^0; the widest span also overflows to inf and rounds subnormals)
+    g = FULL
+    codes, scales = synth.mxfp8_table(50, 256, 3, lo, hi)
+    rows = np.array([(7 * b) % 50 for b in range(g.nb)], np.uint32)
+    rows[[2, 11]] = O.MASKED
+    e = O.gather_table(g, codes, scales, rows)
+    vals = torch.from_numpy(e.view(np.int16)).view(torch.bfloat16).double().numpy()
+    for b, r in enumerate(rows):
+        seg = vals[b * 256:(b + 1) * 256]
+        if r == O.MASKED:
+            assert (e[b * 256:(b + 1) * 256] == 0).all()
+            continue
+        fp8 = torch.from_numpy(codes[r]).view(torch.float8_e4m3fn).double().numpy()
+        ref = fp8 * np.ldexp(1.0, np.repeat(scales[r].astype(np.int64) - 127, 32))
+        # one round-to-nearest-even to BF16 (the fp32 step is exact for these
+        # 4-bit significands); the identity wherever the product fits BF16
+        ref16 = torch.from_numpy(ref).float().to(torch.bfloat16).double().numpy()
+        if hi <= 127:
+            assert np.array_equal(ref16, ref)
+        assert np.array_equal(seg, ref16), (lo, hi, b)
+    with pytest.raises(ValueError):
+        O.gather_table(g, codes, scales, np.full(g.nb, 50, np.uint32))
+
+
+def test_gather_from_memory_matches_the_generated_contents():
+    g = TINY
+    rows = np.array([5, O.MASKED, 6000, 17, 1009, 3], np.uint32)
+    table = [O.table_row(101, r, 32) for r in range(6126)]
+    codes = np.stack([c for c, _ in table])
+    scales = np.stack([s for _, s in table])
+    assert np.array_equal(O.gather_table(g, codes, scales, rows), O.gather(g, 101, rows))
 
 
 # --------------------------------------------------------------------------
