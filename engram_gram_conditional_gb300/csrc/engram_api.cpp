@@ -322,6 +322,13 @@ cudaError_t forward_bind_ws(const engram_ctx* ctx, int64_t T, int max_splits, in
 
 namespace engram {
 
+// The argument checks every fused forward makes before it looks at its buffers.
+engram_status check_forward_call(const engram_ctx* ctx, int layer, int64_t T) {
+    engram_status st = check_layer(ctx, layer, true);
+    if (st || (st = check_T(T))) return st;
+    return ENGRAM_OK;
+}
+
 // engram_forward with the split-K factor capped at max_splits; the workspace
 // is forward_workspace_bytes(ctx, T, max_splits) bytes.
 engram_status forward_fused(const engram_ctx* ctx, int layer, const uint32_t* d_windows,

@@ -33,6 +33,7 @@ engram_status forward_fused(const engram_ctx* ctx, int layer, const uint32_t* d_
                             int64_t T, uint16_t* d_hidden, void* d_workspace, float* d_gates,
                             void* stream, int max_splits);
 size_t forward_workspace_bytes(const engram_ctx* ctx, int64_t T, int max_splits);
+engram_status check_forward_call(const engram_ctx* ctx, int layer, int64_t T);
 }
 
 namespace {
@@ -46,8 +47,10 @@ std::mutex g_scratch_mu;
 
 // Device address of the scratch buffer on the current device.  The address is
 // looked up once per device, with that device current, on the first call made
-// on it; host code must not use the symbol itself (on the host it names a
-// stand-in object, not device memory).
+// on it, and kept until the process exits; host code must not use the symbol
+// itself (on the host it names a stand-in object, not device memory).  A
+// cudaDeviceReset unloads the library's device image, so the kept address (like
+// every context bound on that device) is not valid after one.
 engram_status scratch_address(void** out) {
     int dev = -1;
     cudaError_t e = cudaGetDevice(&dev);
@@ -70,35 +73,43 @@ engram_status scratch_address(void** out) {
     return ENGRAM_OK;
 }
 
+// Largest batch whose scratch fits the buffer: the workspace grows with T,
+// so a binary search over [0, 2^24] on the same layout the forward uses.
+int64_t max_tokens(const engram_ctx* ctx) {
+    int64_t lo = 0, hi = (int64_t)1 << 24;
+    while (lo < hi) {
+        const int64_t mid = (lo + hi + 1) / 2;
+        if (engram::forward_workspace_bytes(ctx, mid, 1) <= kScratchBytes)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    return lo;
+}
+
 }  // namespace
 
 extern "C" engram_status engram_forward_noalloc(const engram_ctx* ctx, int layer,
                                                 const uint32_t* d_windows, int64_t T,
                                                 uint16_t* d_hidden, float* d_gates,
                                                 void* stream) {
-    if (!ctx) {
-        engram::set_last_error("null context");
-        return ENGRAM_EINVAL;
-    }
-    if (T < 0) {
-        engram::set_last_error("T must be >= 0");
-        return ENGRAM_EINVAL;
-    }
+    // the same checks as engram_forward (context, layer bound, T in range)
+    engram_status st = engram::check_forward_call(ctx, layer, T);
+    if (st != ENGRAM_OK) return st;
     if (T == 0) return engram_forward(ctx, layer, d_windows, 0, d_hidden, nullptr, d_gates, stream);
     // K is never split here: split-K partials of a small batch would need far
     // more scratch than the gate sums, so such a batch runs on fewer SMs
     const size_t need = engram::forward_workspace_bytes(ctx, T, 1);
     if (need > kScratchBytes) {
-        const size_t per_token = engram::forward_workspace_bytes(ctx, 1 << 16, 1) >> 16;
         engram::set_last_error(
             "engram_forward_noalloc: " + std::to_string(T) + " tokens need " + std::to_string(need) +
             " bytes of scratch, above the built-in 8 MiB (at most " +
-            std::to_string(per_token ? kScratchBytes / per_token : 0) +
+            std::to_string(max_tokens(ctx)) +
             " tokens for this geometry); split the batch or use engram_forward");
         return ENGRAM_EINVAL;
     }
     void* scratch = nullptr;
-    engram_status st = scratch_address(&scratch);
+    st = scratch_address(&scratch);
     if (st != ENGRAM_OK) return st;
     return engram::forward_fused(ctx, layer, d_windows, T, d_hidden, scratch, d_gates, stream, 1);
 }

@@ -222,23 +222,49 @@ engram_status engram_batch_append(engram_session* const* sessions, const int32_t
  * SM count. */
 size_t engram_workspace_bytes(const engram_ctx* ctx, int64_t T);
 
-/* a2: windows (device [T][4]) -> row indices (device [T][nb]). */
+/* The n-gram hash.  "DeepSeek V4.1 Flash 的 Engram", section "第一步": the
+ * 2-, 3- and 4-gram suffixes of (c_t, c_{t-1}, c_{t-2}, c_{t-3}) each get one
+ * hash per head; vLLM "Engram" wiki, section "동작 방식": per (order, head),
+ * the ids are multiplied by that pair's multipliers, the products XORed
+ * (wrapping 64-bit) and reduced modulo the pair's prime, inside its own bucket
+ * range: row = offset[b] + x mod prime[b].  An n-gram holding DEAD gives
+ * ENGRAM_MASKED for every head of its order.
+ * d_windows: device uint32 [T][4], 16-byte aligned; d_rows: device uint32
+ * [T][nb], written.  The layer need not be bound. */
 engram_status engram_hash(const engram_ctx* ctx, int layer, const uint32_t* d_windows, int64_t T,
                           uint32_t* d_rows, void* stream);
-/* a3: row indices -> dequantised BF16 vectors (device [T][K]); a masked row
- * gives zeros; an index >= rows gives zeros and sets the error word. */
+/* Gather and dequantise.  "DeepSeek V4.1 Flash 的 Engram", section "第二步",
+ * and "3.84 亿行 Embedding 的存法大揭秘": each row holds 256 E4M3 codes and
+ * one E8M0 scale per 32 of them; value = E4M3(code) x 2^(scale - 127), exact
+ * in BF16; the 24 rows of a token are concatenated in bucket order into its
+ * 6,144-vector.  d_rows: device uint32 [T][nb]; d_emb: device bf16 [T][K],
+ * 16-byte aligned, written.  A masked row gives zeros; an index >= rows gives
+ * zeros and sets the error word (ENGRAM_EBOUNDS at the next engram_sync). */
 engram_status engram_gather_dequant(const engram_ctx* ctx, int layer, const uint32_t* d_rows,
                                     int64_t T, uint16_t* d_emb, void* stream);
-/* a4: kv = emb wkv^T in fp32 (device [T][N]); d_emb 16-byte aligned. */
+/* The wkv projection.  "DeepSeek V4.1 Flash 的 Engram", section "第二步": the
+ * 6,144-vector is multiplied by wkv [25,600 x 6,144] (BF16) into one 5,120-wide
+ * key per hyper-connection branch and one shared value (the last 5,120 rows,
+ * "3.84 亿行 Embedding 的存法大揭秘").  kv = emb wkv^T accumulated in fp32.
+ * d_emb: device bf16 [T][K], 16-byte aligned; d_kv: device fp32 [T][N],
+ * written. */
 engram_status engram_project(const engram_ctx* ctx, int layer, const uint16_t* d_emb, int64_t T,
                              float* d_kv, void* stream);
-/* a5: gate and update hidden in place; image rows (window slot 0 == DEAD)
- * pass through.  d_kv, d_windows and d_hidden 16-byte aligned; d_gates may be
- * NULL. */
+/* The gate.  "DeepSeek V4.1 Flash 的 Engram", section "第三步", and vLLM
+ * "Engram" wiki, section "동작 방식": per branch b, hidden and key b are
+ * RMS-normalised, weighted by the pre-multiplied w_q / w_k,
+ * dot = <n(h) w_q, n(k) w_k> / sqrt(d), gate = sigmoid(copysign(sqrt(max(
+ * |dot|, 1e-6)), dot)), hidden_b += gate value, rounded once to BF16.  Image
+ * rows (window slot 0 == DEAD, section "第四步") pass through with gate 0.
+ * d_kv: device fp32 [T][N]; d_windows: device uint32 [T][4]; d_hidden: device
+ * bf16 [T][hc][d], updated in place; all 16-byte aligned; d_gates: device
+ * fp32 [T][hc] or NULL. */
 engram_status engram_gate(const engram_ctx* ctx, int layer, const float* d_kv,
                           const uint32_t* d_windows, int64_t T, uint16_t* d_hidden,
                           float* d_gates, void* stream);
-/* a7: the whole step fused: hash, gather and dequantise into the GEMM's
+/* The whole step of the pages ("DeepSeek V4.1 Flash 的 Engram", sections
+ * "第一步" to "第三步"; vLLM "Engram" wiki, "동작 방식") in one kernel:
+ * hash, gather and dequantise into the GEMM's
  * shared-memory operand tiles, the tcgen05 projection and the gate as the
  * GEMM epilogue.  Neither the 6,144-vector nor the kv reaches HBM (except,
  * for a small batch run with split K, the partial kv tiles that the splits of
@@ -249,7 +275,7 @@ engram_status engram_forward(const engram_ctx* ctx, int layer, const uint32_t* d
                              int64_t T, uint16_t* d_hidden, void* d_workspace,
                              float* d_gates, void* stream);
 
-/* a7, staged: the same result as engram_forward in two kernels.  Step 1
+/* The same step, staged: the same result as engram_forward in two kernels.  Step 1
  * gathers and dequantises every (token, bucket) row once into a scratch
  * matrix e [T][K] in d_workspace; step 2 is the forward GEMM with its A
  * operand read from e by TMA and the same gate epilogue (kv stays on chip).
@@ -298,13 +324,17 @@ engram_status engram_forward_staged_rows(const engram_ctx* ctx, int layer,
  * K is never split here (the partial tiles would not fit), so a small batch
  * runs on fewer SMs than engram_forward would give it.
  * The first call on a device looks up the buffer's device address (once per
- * device, with that device current); make that first call before any stream
- * capture.  All calls share the buffer: calls whose kernels may overlap on the
- * GPU (other streams, other threads) race on it - keep them on one stream. */
+ * device, with that device current) and keeps it until the process exits;
+ * make that first call before any stream capture.  A cudaDeviceReset unloads
+ * the library's device image and invalidates that address, as it does every
+ * context bound on the device: do not call this after a reset.  The size check
+ * comes after the same argument checks as engram_forward.  All calls share the
+ * buffer: calls whose kernels may overlap on the GPU (other streams, other
+ * threads) race on it - keep them on one stream. */
 engram_status engram_forward_noalloc(const engram_ctx* ctx, int layer, const uint32_t* d_windows,
                                      int64_t T, uint16_t* d_hidden, float* d_gates, void* stream);
 
-/* a2 -> a4 fused, the part of the step that does not depend on hidden
+/* Hash, gather and projection fused: the part of the step that does not depend on hidden
  * ("DeepSeek V4.1 Flash 的 Engram", section "提前投影": hashing, gather and
  * projection depend only on the tokens and can run ahead of the layer):
  * windows (device [T][4]) -> kv fp32 (device [T][N]); the 6,144-vector stays
@@ -329,8 +359,8 @@ engram_status engram_project_windows(const engram_ctx* ctx, int layer, const uin
 #define ENGRAM_KV_BF16 1
 engram_status engram_prepass(const engram_ctx* ctx, int layer, const uint32_t* d_windows, int64_t T,
                              void* d_kv, int kv_format, void* d_workspace, void* stream);
-/* a5 on a BF16 kv [T][N] (engram_prepass with ENGRAM_KV_BF16); otherwise as
- * engram_gate. */
+/* The gate (as engram_gate, "第三步") on a BF16 kv [T][N] (engram_prepass
+ * with ENGRAM_KV_BF16); otherwise as engram_gate. */
 engram_status engram_gate_bf16kv(const engram_ctx* ctx, int layer, const uint16_t* d_kv,
                                  const uint32_t* d_windows, int64_t T, uint16_t* d_hidden,
                                  float* d_gates, void* stream);

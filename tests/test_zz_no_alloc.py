@@ -11,6 +11,8 @@ and nothing it leaves behind may leak into the next result).
 This file is named to be collected last, so that a run stopping at the first
 failure has already run every other test; it also passes on its own.
 """
+import re
+
 import numpy as np
 import pytest
 import torch
@@ -68,17 +70,50 @@ def test_noalloc_matches_forward_on_two_calls_in_a_row(name, sessions, per, span
         s.close()
 
 
+def stated_limit(ctx):
+    """The largest batch the call accepts, as its own rejection message states it."""
+    with pytest.raises(eg.EngramError) as e:
+        eg.engram_forward_noalloc(ctx, 0, 16, 1 << 24, 16)  # rejected before any launch
+    assert e.value.status == eg.EINVAL and "8 MiB" in e.value.message
+    return int(re.search(r"at most (\d+) tokens", e.value.message).group(1))
+
+
 def test_noalloc_rejects_batches_above_its_buffer():
     s = setup_workload("tiny")
     try:
         ctx = s.model.ctx
-        per_token = eg.engram_workspace_bytes(ctx, 1 << 16) // (1 << 16)
-        too_many = (8 << 20) // per_token + 1
+        limit = stated_limit(ctx)
         # rejected before any pointer is touched or any kernel launched
         with pytest.raises(eg.EngramError) as e:
-            eg.engram_forward_noalloc(ctx, 0, 16, too_many, 16)
+            eg.engram_forward_noalloc(ctx, 0, 16, limit + 1, 16)
         assert e.value.status == eg.EINVAL
-        assert "8 MiB" in e.value.message
+        # a bad layer is reported as such, whatever the batch size
+        with pytest.raises(eg.EngramError) as e:
+            eg.engram_forward_noalloc(ctx, 7, 16, 1 << 24, 16)
+        assert e.value.status == eg.EINVAL and "layer" in e.value.message
         eg.engram_forward_noalloc(ctx, 0, None, 0, None)  # T = 0: nothing to do
+    finally:
+        s.close()
+
+
+def test_noalloc_at_its_size_limit_full_geometry():
+    # the largest accepted batch (the buffer nearly full, the tile counters at
+    # its end) against engram_forward; one token more is rejected
+    s = setup_workload("prefill_2048")
+    try:
+        ctx = s.model.ctx
+        T = stated_limit(ctx)
+        assert T == 8592  # hc 4, d 5,120
+        per = (T + 3) // 4
+        win, _, _ = prefill_windows(s, 4, per, [(500, 7)])
+        win = win[:T]
+        for call in range(2):
+            hidden = synth.normal_bf16((T, s.w.hc, s.w.d), 1.0, 6, 910 + call)
+            h_ref, g_ref, h_new, g_new = forward_both(s, win, hidden)
+            check_hidden(h_new, h_ref, f"{T} tokens, call {call}")
+            assert np.abs(g_new - g_ref).max() <= 1e-3
+        with pytest.raises(eg.EngramError) as e:
+            eg.engram_forward_noalloc(ctx, 0, to_dev(win[:1]), T + 1, 16)
+        assert e.value.status == eg.EINVAL
     finally:
         s.close()
