@@ -36,6 +36,9 @@ EXPORTS = (
     "engram_gate", "engram_forward", "engram_forward_noalloc", "engram_forward_staged",
     "engram_forward_staged_workspace_bytes", "engram_stage_rows", "engram_forward_staged_rows",
     "engram_project_windows", "engram_prepass", "engram_gate_bf16kv",
+    "engram_layer_bind_shard", "engram_scale_range", "engram_hash_by_bucket",
+    "engram_raw_row_bytes", "engram_host_table_alloc", "engram_host_table_free",
+    "engram_shard_gather_raw", "engram_stage_raw_rows",
     "engram_sync", "engram_ctx_set_wait_limit", "engram_debug_starve_operand",
     "engram_last_error",
 )
@@ -118,6 +121,15 @@ def lib() -> C.CDLL:
             "engram_forward_staged_rows": [vp, C.c_int, vp, i64, vp, vp, vp, vp],
             "engram_sync": [vp, vp],
             "engram_ctx_set_wait_limit": [vp, i64],
+            "engram_layer_bind_shard": [vp, C.c_int, C.POINTER(LayerWeights), C.c_uint64,
+                                        C.c_uint32, C.c_uint32],
+            "engram_scale_range": [vp, vp, C.c_uint64, C.POINTER(C.c_uint32),
+                                   C.POINTER(C.c_uint32)],
+            "engram_host_table_alloc": [C.c_uint64, C.POINTER(vp)],
+            "engram_host_table_free": [vp, C.c_uint64],
+            "engram_hash_by_bucket": [vp, C.c_int, vp, i64, vp, vp],
+            "engram_shard_gather_raw": [vp, C.c_int, vp, i64, vp, vp],
+            "engram_stage_raw_rows": [vp, C.c_int, vp, vp, i64, vp, vp],
             "engram_debug_starve_operand": [vp, C.c_int],
         }
         for name, args in sig.items():
@@ -127,6 +139,8 @@ def lib() -> C.CDLL:
         for name in ("engram_workspace_bytes", "engram_forward_staged_workspace_bytes"):
             getattr(L, name).argtypes = [vp, i64]
             getattr(L, name).restype = C.c_size_t
+        L.engram_raw_row_bytes.argtypes = [vp]
+        L.engram_raw_row_bytes.restype = C.c_size_t
         L.engram_last_error.argtypes = []
         L.engram_last_error.restype = C.c_char_p
         _lib = L
@@ -338,6 +352,49 @@ def engram_prepass(ctx, layer, d_windows, T, d_kv, kv_format, d_workspace, strea
 def engram_gate_bf16kv(ctx, layer, d_kv, d_windows, T, d_hidden, d_gates=None, stream=None):
     _check(lib().engram_gate_bf16kv(ctx, layer, _ptr(d_kv), _ptr(d_windows), T, _ptr(d_hidden),
                                     _ptr(d_gates), _stream(stream)))
+
+
+def engram_layer_bind_shard(ctx, layer: int, table, scales, rows: int, wkv, wq, wk, row_lo: int,
+                            scale_min: int, scale_max: int, flags: int = 0):
+    w = LayerWeights(_ptr(table), _ptr(scales), rows, _ptr(wkv), _ptr(wq), _ptr(wk), flags)
+    _check(lib().engram_layer_bind_shard(ctx, layer, C.byref(w), row_lo, scale_min, scale_max))
+
+
+def engram_scale_range(ctx, scales, n: int):
+    """(min, max) of n E8M0 bytes on the device (255, 0 for n = 0)."""
+    lo, hi = C.c_uint32(), C.c_uint32()
+    _check(lib().engram_scale_range(ctx, _ptr(scales), n, C.byref(lo), C.byref(hi)))
+    return lo.value, hi.value
+
+
+def engram_host_table_alloc(nbytes: int) -> int:
+    """Registered, huge-page-advised host memory for a table read through UVA
+    (see include/engram.h); returns its address (host and device)."""
+    out = C.c_void_p()
+    _check(lib().engram_host_table_alloc(nbytes, C.byref(out)))
+    return out.value
+
+
+def engram_host_table_free(ptr: int, nbytes: int):
+    _check(lib().engram_host_table_free(ptr, nbytes))
+
+
+def engram_hash_by_bucket(ctx, layer, d_windows, T, d_rows_bm, stream=None):
+    _check(lib().engram_hash_by_bucket(ctx, layer, _ptr(d_windows), T, _ptr(d_rows_bm),
+                                       _stream(stream)))
+
+
+def engram_raw_row_bytes(ctx) -> int:
+    return int(lib().engram_raw_row_bytes(ctx))
+
+
+def engram_shard_gather_raw(ctx, layer, d_ids, n, d_raw, stream=None):
+    _check(lib().engram_shard_gather_raw(ctx, layer, _ptr(d_ids), n, _ptr(d_raw), _stream(stream)))
+
+
+def engram_stage_raw_rows(ctx, layer, d_rows_bm, d_raw_bm, T, d_workspace, stream=None):
+    _check(lib().engram_stage_raw_rows(ctx, layer, _ptr(d_rows_bm), _ptr(d_raw_bm), T,
+                                       _ptr(d_workspace), _stream(stream)))
 
 
 def engram_ctx_set_wait_limit(ctx, ns: int):

@@ -6,12 +6,14 @@
 // the path runs in the CUDA kernels of kernels_misc.cu and kernels_mma.cu.
 #include <cuda_runtime.h>
 #include <string.h>
+#include <sys/mman.h>
 
 #include <math.h>
 
 #include <algorithm>
 #include <new>
 #include <string>
+#include <thread>
 #include <vector>
 
 #include "../../include/engram.h"
@@ -138,6 +140,10 @@ struct LayerState {
     uint32_t scale_min = 0, scale_max = 0;
     bool bucket_gather = false;    // whole 256-wide rows gathered once per tile and bucket
     bool table_bf16 = false;       // BF16 rows without scales (ENGRAM_BIND_TABLE_BF16)
+    // bound to a shard of the table (engram_layer_bind_shard): rows
+    // [row_lo, row_lo + shard_rows) of the layer's table
+    bool shard = false;
+    uint64_t row_lo = 0, shard_rows = 0;
 };
 
 struct engram_ctx {
@@ -162,12 +168,21 @@ struct engram_session {
 namespace {
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+bool aligned4(const void* p) { return ((uintptr_t)p & 3u) == 0; }
 
 engram_status check_layer(const engram_ctx* ctx, int layer, bool need_bound) {
     if (!ctx) return fail(ENGRAM_EINVAL, "null context");
     if (layer < 0 || layer >= (int)ctx->layers.size()) return fail(ENGRAM_EINVAL, "layer out of range");
     if (need_bound && !ctx->layers[layer].bound)
         return fail(ENGRAM_ESTATE, "layer weights not bound (engram_layer_bind)");
+    return ENGRAM_OK;
+}
+
+// Calls that index the layer's table with global row numbers need all of it.
+engram_status check_full_table(const engram_ctx* ctx, int layer) {
+    if (ctx->layers[layer].shard)
+        return fail(ENGRAM_ESTATE, "layer bound to a table shard: its rows come through "
+                                   "engram_shard_gather_raw and engram_stage_raw_rows");
     return ENGRAM_OK;
 }
 
@@ -325,7 +340,7 @@ namespace engram {
 // The argument checks every fused forward makes before it looks at its buffers.
 engram_status check_forward_call(const engram_ctx* ctx, int layer, int64_t T) {
     engram_status st = check_layer(ctx, layer, true);
-    if (st || (st = check_T(T))) return st;
+    if (st || (st = check_T(T)) || (st = check_full_table(ctx, layer))) return st;
     return ENGRAM_OK;
 }
 
@@ -335,7 +350,7 @@ engram_status forward_fused(const engram_ctx* ctx, int layer, const uint32_t* d_
                             int64_t T, uint16_t* d_hidden, void* d_workspace, float* d_gates,
                             void* stream, int max_splits) {
     engram_status st = check_layer(ctx, layer, true);
-    if (st || (st = check_T(T))) return st;
+    if (st || (st = check_T(T)) || (st = check_full_table(ctx, layer))) return st;
     if (T == 0) return ok();
     if (!d_windows || !d_hidden || !d_workspace || !aligned16(d_windows) || !aligned16(d_hidden) ||
         !aligned16(d_workspace))
@@ -474,18 +489,102 @@ engram_status engram_layer_set_multipliers(engram_ctx* ctx, int layer, const uin
     return ok();
 }
 
+namespace {
+// The context's device word (error word and scan results), allocated at the
+// first bind or scan on device dev.
+engram_status ensure_device_word(engram_ctx* ctx, int dev) {
+    if (ctx->d_err) return ENGRAM_OK;
+    cudaError_t e = cudaMalloc(&ctx->d_err, 4 * sizeof(uint32_t));
+    if (e != cudaSuccess) {
+        ctx->d_err = nullptr;
+        return fail(ENGRAM_ENOMEM, "cudaMalloc of the error word");
+    }
+    e = cudaMemset(ctx->d_err, 0, 4 * sizeof(uint32_t));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemset");
+    ctx->device = dev;
+    return ENGRAM_OK;
+}
+}  // namespace
+
+engram_status engram_scale_range(engram_ctx* ctx, const uint8_t* scales, uint64_t n,
+                                 uint32_t* scale_min, uint32_t* scale_max) {
+    if (!ctx || !scale_min || !scale_max || (n > 0 && !scales))
+        return fail(ENGRAM_EINVAL, "null argument");
+    *scale_min = 255u;
+    *scale_max = 0u;
+    if (n == 0) return ok();
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (ctx->device >= 0 && ctx->device != dev)
+        return fail(ENGRAM_ESTATE, "context already bound on another device");
+    const uint8_t* p = scales;
+    cudaPointerAttributes attr{};
+    e = cudaPointerGetAttributes(&attr, scales);
+    if (e != cudaSuccess || (attr.type == cudaMemoryTypeHost && !attr.devicePointer) ||
+        attr.type == cudaMemoryTypeUnregistered) {
+        cudaGetLastError();
+        return fail(ENGRAM_EINVAL, "scales must be device or mapped pinned host memory");
+    }
+    if (attr.type == cudaMemoryTypeHost) p = static_cast<const uint8_t*>(attr.devicePointer);
+    engram_status st = ensure_device_word(ctx, dev);
+    if (st) return st;
+    const uint32_t init[2] = {255u, 0u};
+    e = cudaMemcpy(ctx->d_err + 1, init, sizeof init, cudaMemcpyHostToDevice);
+    if (e == cudaSuccess) e = launch_scale_range(p, n, ctx->d_err + 1, 0);
+    uint32_t res[2] = {255u, 0u};
+    if (e == cudaSuccess) e = cudaMemcpy(res, ctx->d_err + 1, sizeof res, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "scale scan");
+    *scale_min = res[0];
+    *scale_max = res[1];
+    return ok();
+}
+
+namespace {
+// A table shard: rows [row_lo, row_lo + w->rows) of the layer's table, and the
+// E8M0 exponent span of the whole table (the shard cannot scan the others).
+struct ShardSpec {
+    uint64_t row_lo;
+    uint32_t scale_min, scale_max;
+};
+
+engram_status bind_impl(engram_ctx* ctx, int layer, const engram_layer_weights* w,
+                        const ShardSpec* sh);
+}  // namespace
+
 engram_status engram_layer_bind(engram_ctx* ctx, int layer, const engram_layer_weights* w) {
+    return bind_impl(ctx, layer, w, nullptr);
+}
+
+engram_status engram_layer_bind_shard(engram_ctx* ctx, int layer, const engram_layer_weights* w,
+                                      uint64_t row_lo, uint32_t scale_min, uint32_t scale_max) {
+    if (w && (w->flags & ENGRAM_BIND_TABLE_BF16))
+        return fail(ENGRAM_EUNSUPPORTED, "a table shard holds MXFP8 rows");
+    if (scale_min > scale_max || scale_max > 254u)
+        return fail(ENGRAM_EINVAL, "scale span: scale_min <= scale_max <= 254");
+    const ShardSpec sh{row_lo, scale_min, scale_max};
+    return bind_impl(ctx, layer, w, &sh);
+}
+
+namespace {
+engram_status bind_impl(engram_ctx* ctx, int layer, const engram_layer_weights* w,
+                        const ShardSpec* sh) {
     engram_status st = check_layer(ctx, layer, false);
     if (st) return st;
     const bool tbf16 = w && (w->flags & ENGRAM_BIND_TABLE_BF16);
-    if (!w || !w->table || (!tbf16 && !w->scales) || !w->wkv || !w->wq || !w->wk)
+    // a shard of no rows (a rank that owns no bucket) needs no table
+    const bool no_rows = sh && w && w->rows == 0;
+    if (!w || (!no_rows && (!w->table || (!tbf16 && !w->scales))) || !w->wkv || !w->wq || !w->wk)
         return fail(ENGRAM_EINVAL, "null weight pointer");
     if (w->flags & ~(ENGRAM_BIND_BF16_OPERANDS | ENGRAM_BIND_TABLE_BF16))
         return fail(ENGRAM_EINVAL, "unknown bind flag");
     LayerState& L = ctx->layers[layer];
-    if (w->rows != L.rows) return fail(ENGRAM_EINVAL, "table rows differ from the layer's row count");
-    if (!aligned16(w->table) || (!tbf16 && !aligned16(w->scales)) || !aligned16(w->wkv) ||
-        !aligned16(w->wq) || !aligned16(w->wk))
+    if (!sh && w->rows != L.rows)
+        return fail(ENGRAM_EINVAL, "table rows differ from the layer's row count");
+    if (sh && (w->rows > L.rows || sh->row_lo > L.rows - w->rows))
+        return fail(ENGRAM_EINVAL, "shard rows outside the layer's table");
+    if ((w->table && !aligned16(w->table)) || (!tbf16 && w->scales && !aligned16(w->scales)) ||
+        !aligned16(w->wkv) || !aligned16(w->wq) || !aligned16(w->wk))
         return fail(ENGRAM_EINVAL, "weights must be 16-byte aligned");
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -513,13 +612,7 @@ engram_status engram_layer_bind(engram_ctx* ctx, int layer, const engram_layer_w
             return fail(ENGRAM_EINVAL, "table pointer must be device or pinned host memory");
         }
     }
-    if (!ctx->d_err) {
-        e = cudaMalloc(&ctx->d_err, 4 * sizeof(uint32_t));
-        if (e != cudaSuccess) return fail(ENGRAM_ENOMEM, "cudaMalloc of the error word");
-        e = cudaMemset(ctx->d_err, 0, 4 * sizeof(uint32_t));
-        if (e != cudaSuccess) return cuda_fail(e, "cudaMemset");
-        ctx->device = dev;
-    }
+    if ((st = ensure_device_word(ctx, dev))) return st;
     CUtensorMap tm, tm_half;
     e = make_tma_16bit(&tm, w->wkv, (uint64_t)ctx->N, (uint64_t)ctx->K, kBN, false);
     if (e == cudaSuccess)
@@ -537,13 +630,15 @@ engram_status engram_layer_bind(engram_ctx* ctx, int layer, const engram_layer_w
     e = cudaMemcpy(ctx->d_err + 1, init, sizeof init, cudaMemcpyHostToDevice);
     if (e != cudaSuccess) return cuda_fail(e, "bind scan init");
     const uint64_t nscale = L.rows * (ctx->desc.row_dim / 32);
-    if (!tbf16) e = launch_scale_range(bw.scales, nscale, ctx->d_err + 1, 0);
+    if (!tbf16 && !sh) e = launch_scale_range(bw.scales, nscale, ctx->d_err + 1, 0);
     if (e == cudaSuccess)
         e = launch_absmax_bf16(w->wkv, (uint64_t)ctx->N * ctx->K, ctx->d_err + 3, 0);
     uint32_t res[3] = {0, 0, 0};
     if (e == cudaSuccess) e = cudaMemcpy(res, ctx->d_err + 1, sizeof res, cudaMemcpyDeviceToHost);
     if (e != cudaSuccess) return cuda_fail(e, "bind scans");
-    const uint32_t smin = res[0], smax = res[1], wabs = res[2];
+    // a shard takes the whole table's exponent span from the caller
+    const uint32_t smin = sh ? sh->scale_min : res[0], smax = sh ? sh->scale_max : res[1];
+    const uint32_t wabs = res[2];
     // BF16 table rows are copied into BF16 operands (the fused kernels, which
     // decode MXFP8 in their producers, do not take them)
     const bool want_f16 = !(w->flags & ENGRAM_BIND_BF16_OPERANDS) && !tbf16;
@@ -616,9 +711,13 @@ engram_status engram_layer_bind(engram_ctx* ctx, int layer, const engram_layer_w
     L.w = bw;
     L.tm_wkv = tm;
     L.tm_wkv_half = tm_half;
+    L.shard = sh != nullptr;
+    L.row_lo = sh ? sh->row_lo : 0;
+    L.shard_rows = sh ? w->rows : L.rows;
     L.bound = true;
     return ok();
 }
+}  // namespace
 
 engram_status engram_layer_info(const engram_ctx* ctx, int layer, engram_layer_info_t* out) {
     engram_status st = check_layer(ctx, layer, false);
@@ -657,6 +756,47 @@ engram_status engram_table_fill_bf16(const engram_ctx* ctx, uint64_t seed, uint1
     cudaError_t e = launch_table_fill_bf16(seed, data, row_begin, row_end,
                                            (int)ctx->desc.row_dim, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "table fill launch");
+    return ok();
+}
+
+// ---- host memory for a table read through UVA ----------------------------------------------
+
+engram_status engram_host_table_alloc(uint64_t bytes, void** out) {
+    if (!out || bytes == 0) return fail(ENGRAM_EINVAL, "bytes > 0 and an output pointer");
+    *out = nullptr;
+    void* p = mmap(nullptr, bytes, PROT_READ | PROT_WRITE, MAP_PRIVATE | MAP_ANONYMOUS, -1, 0);
+    if (p == MAP_FAILED) return fail(ENGRAM_ENOMEM, "mmap of the host table");
+    // a hint: the kernel may back the mapping with transparent huge pages
+    // (ignored where it offers none)
+    (void)madvise(p, bytes, MADV_HUGEPAGE);
+    // touch every page, in parallel, before the registration pins them
+    {
+        const unsigned nt = std::max(1u, std::min(32u, std::thread::hardware_concurrency()));
+        const uint64_t chunk = (bytes + nt - 1) / nt;
+        std::vector<std::thread> th;
+        for (unsigned i = 0; i < nt; ++i) {
+            const uint64_t lo = std::min<uint64_t>(bytes, i * chunk);
+            const uint64_t hi = std::min<uint64_t>(bytes, lo + chunk);
+            if (hi > lo)
+                th.emplace_back([p, lo, hi] { memset(static_cast<char*>(p) + lo, 0, hi - lo); });
+        }
+        for (auto& t : th) t.join();
+    }
+    cudaError_t e = cudaHostRegister(p, bytes, cudaHostRegisterMapped | cudaHostRegisterPortable);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        munmap(p, bytes);
+        return cuda_fail(e, "cudaHostRegister of the host table");
+    }
+    *out = p;
+    return ok();
+}
+
+engram_status engram_host_table_free(void* p, uint64_t bytes) {
+    if (!p) return ok();
+    cudaError_t e = cudaHostUnregister(p);
+    munmap(p, bytes);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaHostUnregister of the host table");
     return ok();
 }
 
@@ -766,24 +906,58 @@ size_t engram_workspace_bytes(const engram_ctx* ctx, int64_t T) {
     return forward_workspace_bytes(ctx, T, 8);
 }
 
-engram_status engram_hash(const engram_ctx* ctx, int layer, const uint32_t* d_windows, int64_t T,
-                          uint32_t* d_rows, void* stream) {
+static engram_status hash_impl(const engram_ctx* ctx, int layer, const uint32_t* d_windows,
+                               int64_t T, uint32_t* d_rows, bool bucket_major, void* stream) {
     engram_status st = check_layer(ctx, layer, false);
     if (st || (st = check_T(T))) return st;
     if (T == 0) return ok();
-    if (!d_windows || !d_rows || !aligned16(d_windows)) return fail(ENGRAM_EINVAL, "windows / rows");
+    if (!d_windows || !d_rows || !aligned16(d_windows) || !aligned4(d_rows))
+        return fail(ENGRAM_EINVAL, "windows (16-byte aligned) / rows (4-byte aligned)");
     cudaError_t e = launch_hash(hash_params(ctx, layer), reinterpret_cast<const uint4*>(d_windows), T,
-                                d_rows, (cudaStream_t)stream);
+                                d_rows, bucket_major, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "hash launch");
+    return ok();
+}
+
+engram_status engram_hash(const engram_ctx* ctx, int layer, const uint32_t* d_windows, int64_t T,
+                          uint32_t* d_rows, void* stream) {
+    return hash_impl(ctx, layer, d_windows, T, d_rows, false, stream);
+}
+
+engram_status engram_hash_by_bucket(const engram_ctx* ctx, int layer, const uint32_t* d_windows,
+                                    int64_t T, uint32_t* d_rows_bm, void* stream) {
+    return hash_impl(ctx, layer, d_windows, T, d_rows_bm, true, stream);
+}
+
+size_t engram_raw_row_bytes(const engram_ctx* ctx) {
+    return ctx ? (size_t)ctx->desc.row_dim + 16 : 0;
+}
+
+engram_status engram_shard_gather_raw(const engram_ctx* ctx, int layer, const uint32_t* d_ids,
+                                      int64_t n, uint8_t* d_raw, void* stream) {
+    engram_status st = check_layer(ctx, layer, true);
+    if (st) return st;
+    if (n < 0 || n > ((int64_t)1 << 31)) return fail(ENGRAM_EINVAL, "n must be in [0, 2^31]");
+    if (n == 0) return ok();
+    if (!d_ids || !d_raw || !aligned4(d_ids) || !aligned16(d_raw))
+        return fail(ENGRAM_EINVAL, "ids (4-byte aligned) / raw (16-byte aligned)");
+    const LayerState& L = ctx->layers[layer];
+    if (L.table_bf16) return fail(ENGRAM_EUNSUPPORTED, "raw rows are MXFP8 rows");
+    if (L.shard_rows > 0 && !L.w.table) return fail(ENGRAM_ESTATE, "no table bound");
+    cudaError_t e = launch_shard_gather_raw(d_ids, n, L.row_lo, L.shard_rows,
+                                            (int)ctx->desc.row_dim, L.w.table, L.w.scales, d_raw,
+                                            ctx->d_err, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "shard gather launch");
     return ok();
 }
 
 engram_status engram_gather_dequant(const engram_ctx* ctx, int layer, const uint32_t* d_rows,
                                     int64_t T, uint16_t* d_emb, void* stream) {
     engram_status st = check_layer(ctx, layer, true);
-    if (st || (st = check_T(T))) return st;
+    if (st || (st = check_T(T)) || (st = check_full_table(ctx, layer))) return st;
     if (T == 0) return ok();
-    if (!d_rows || !d_emb || !aligned16(d_emb)) return fail(ENGRAM_EINVAL, "rows / emb");
+    if (!d_rows || !d_emb || !aligned4(d_rows) || !aligned16(d_emb))
+        return fail(ENGRAM_EINVAL, "rows (4-byte aligned) / emb (16-byte aligned)");
     const LayerState& L = ctx->layers[layer];
     cudaError_t e = launch_gather(geometry(ctx), d_rows, T, L.w.table, L.w.scales, L.rows,
                                   L.table_bf16, d_emb,
@@ -837,25 +1011,33 @@ engram_status engram_forward(const engram_ctx* ctx, int layer, const uint32_t* d
 }
 
 // A batch whose output tiles (128 tokens x 256 outputs) do not fill the GPU
-// twice runs the staged projection with stream K and a kv-store epilogue, and
-// the gate as its own kernel after it: the fused gate epilogue's loads would
-// wait behind the wkv stream in the SM's memory pipeline, which a single wave
-// of tiles cannot hide, while the separate gate kernel has the whole GPU.
+// twice runs the staged GEMM with stream K: the launch's (tile, stage)
+// sequence is cut into one contiguous range per CTA (or pair).  The pieces
+// that finish key tiles publish the gate's sums and those that finish value
+// tiles store v (kEpiForwardSk); a light kernel then makes the gates and
+// updates hidden.  Nothing in the GEMM waits for gates: a value tile that
+// waited for every key tile stalled its range's later MMAs (0.147 ms per
+// decode step against 0.080 ms).
 static bool staged_stream_k(const engram_ctx* ctx, int64_t T) {
     const int64_t tiles = (T + kBM - 1) / kBM * (ctx->N / kBN);
     return tiles < 2 * (int64_t)device_sm_count();
 }
 
-// Stream-K workspace after e: kv f32[T][N], then one 128 x 256 fp32 slot per
-// CTA, then sixteen ready flags per CTA (one per epilogue warp).
+// Stream-K workspace after e: the gate sums f32 [T][hc][d/kBN][2][3]; v f32
+// [T][d]; one 128 x 256 fp32 slot per CTA for the parked pieces; sixteen
+// ready flags per CTA (one per epilogue warp), zeroed before every call.  The
+// pre-pass (kv-store epilogue, kv in the caller's buffer) uses the slots and
+// the flags only.
 struct StreamKWs {
-    size_t kv, slots, flags;
-    size_t total() const { return kv + slots + flags; }
+    size_t part, v, slots, flags;
+    size_t total() const { return part + v + slots + flags; }
 };
 static StreamKWs stream_k_ws(const engram_ctx* ctx, int64_t T) {
     const size_t ctas = (size_t)device_sm_count();
     StreamKWs w;
-    w.kv = ((size_t)T * ctx->N * sizeof(float) + 255) & ~(size_t)255;
+    w.part = ((size_t)T * ctx->desc.hc * (ctx->desc.d / kBN) * 2 * 3 * sizeof(float) + 255) &
+             ~(size_t)255;
+    w.v = ((size_t)T * ctx->desc.d * sizeof(float) + 255) & ~(size_t)255;
     w.slots = ctas * kBM * kBN * sizeof(float);
     w.flags = (ctas * 16 * sizeof(uint32_t) + 255) & ~(size_t)255;
     return w;
@@ -877,24 +1059,54 @@ size_t engram_forward_staged_workspace_bytes(const engram_ctx* ctx, int64_t T) {
     return e + forward_workspace_bytes_groups(ctx, T, 8, 2);
 }
 
+// The stream-K flags a small batch's staging zeroes (null, 0 for a large one).
+static void staged_clear(const engram_ctx* ctx, int64_t T, void* d_workspace, uint32_t*& clear,
+                         int& n_clear) {
+    clear = nullptr;
+    n_clear = 0;
+    if (staged_stream_k(ctx, T)) {
+        const StreamKWs w = stream_k_ws(ctx, T);
+        clear = reinterpret_cast<uint32_t*>(static_cast<char*>(d_workspace) +
+                                            staged_e_bytes(ctx, T) + w.part + w.v + w.slots);
+        n_clear = (int)(w.flags / sizeof(uint32_t));
+    }
+}
+
+engram_status engram_stage_raw_rows(const engram_ctx* ctx, int layer, const uint32_t* d_rows_bm,
+                                    const uint8_t* d_raw_bm, int64_t T, void* d_workspace,
+                                    void* stream) {
+    engram_status st = check_layer(ctx, layer, true);
+    if (st || (st = check_T(T))) return st;
+    if (T == 0) return ok();
+    if (!d_rows_bm || !d_raw_bm || !d_workspace || !aligned4(d_rows_bm) || !aligned16(d_raw_bm) ||
+        !aligned16(d_workspace))
+        return fail(ENGRAM_EINVAL, "rows / raw rows / workspace (16-byte aligned)");
+    const LayerState& L = ctx->layers[layer];
+    if (L.table_bf16) return fail(ENGRAM_EUNSUPPORTED, "raw rows are MXFP8 rows");
+    uint32_t* clear;
+    int n_clear;
+    staged_clear(ctx, T, d_workspace, clear, n_clear);
+    cudaError_t e = launch_stage_raw(hash_params(ctx, layer), d_rows_bm, d_raw_bm, T,
+                                     (int)ctx->desc.row_dim, L.f16, L.a_exp_shift,
+                                     static_cast<uint16_t*>(d_workspace), ctx->d_err, clear,
+                                     n_clear, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "raw staging launch");
+    return ok();
+}
+
 engram_status engram_stage_rows(const engram_ctx* ctx, int layer, const uint32_t* d_windows,
                                 int64_t T, void* d_workspace, void* stream) {
     engram_status st = check_layer(ctx, layer, true);
-    if (st || (st = check_T(T))) return st;
+    if (st || (st = check_T(T)) || (st = check_full_table(ctx, layer))) return st;
     if (T == 0) return ok();
     if (!d_windows || !d_workspace || !aligned16(d_windows) || !aligned16(d_workspace))
         return fail(ENGRAM_EINVAL, "windows / workspace (16-byte aligned)");
     const LayerState& L = ctx->layers[layer];
     // gather and dequantise every (token, bucket) row once into e; for a small
     // batch the same kernel zeroes the stream-K flags of the GEMM after it
-    uint32_t* clear = nullptr;
-    int n_clear = 0;
-    if (staged_stream_k(ctx, T)) {
-        const StreamKWs w = stream_k_ws(ctx, T);
-        clear = reinterpret_cast<uint32_t*>(static_cast<char*>(d_workspace) +
-                                            staged_e_bytes(ctx, T) + w.kv + w.slots);
-        n_clear = (int)(w.flags / sizeof(uint32_t));
-    }
+    uint32_t* clear;
+    int n_clear;
+    staged_clear(ctx, T, d_workspace, clear, n_clear);
     cudaError_t e = launch_gather_stage(hash_params(ctx, layer),
                                         reinterpret_cast<const uint4*>(d_windows), T,
                                         (int)ctx->desc.row_dim, L.w.table, L.w.scales, L.rows,
@@ -975,24 +1187,29 @@ static engram_status staged_rows(const engram_ctx* ctx, int layer, const uint32_
     cudaStream_t s = (cudaStream_t)stream;
     const bool small = staged_stream_k(ctx, T);
     if (small) {
-        // small batch: stream-K projection into kv, then the gate
+        // small batch: stream K; key tiles publish the gate's sums, value tiles
+        // store v; then the gates and hidden += g v
         const StreamKWs w = stream_k_ws(ctx, T);
         a.k_splits = 1;
-        a.kv = reinterpret_cast<float*>(rest);
-        a.ldkv = ctx->N;
-        a.kv_split_stride = 0;
         a.stream_k = 1;
-        a.sk_slots = reinterpret_cast<float*>(rest + w.kv);
-        a.sk_flags = reinterpret_cast<uint32_t*>(rest + w.kv + w.slots);
+        a.epi_groups = 2;
+        a.key_tiles = (int)(ctx->desc.hc * ctx->desc.d / kBN);
+        a.key_tail = 0;
+        a.partials = reinterpret_cast<float*>(rest);
+        a.kv = reinterpret_cast<float*>(rest + w.part);
+        a.ldkv = ctx->desc.d;
+        a.kv_bf16 = 0;
+        a.kv_split_stride = 0;
+        a.sk_slots = reinterpret_cast<float*>(rest + w.part + w.v);
+        a.sk_flags = reinterpret_cast<uint32_t*>(rest + w.part + w.v + w.slots);
         if (!flags_clear) {
             e = cudaMemsetAsync(a.sk_flags, 0, w.flags, s);
             if (e != cudaSuccess) return cuda_fail(e, "stream-K flags");
         }
-        e = pairs ? launch_project_tma_pair(a, L.f16, tmA, tmB, s)
-                  : launch_project_tma(a, L.f16, tmA, tmB, s);
-        if (e != cudaSuccess) return cuda_fail(e, "stream-K projection launch");
-        e = launch_gate(geometry(ctx), a.kv, false, 1, 0, a.windows, T, d_hidden, L.wqk, d_gates,
-                        s);
+        e = launch_forward_sk(a, L.f16, pairs, tmA, tmB, s);
+        if (e != cudaSuccess) return cuda_fail(e, "stream-K forward launch");
+        e = launch_gate_sums(geometry(ctx), a.partials, 2, a.kv, a.windows, T, d_hidden, d_gates,
+                             s);
         if (e != cudaSuccess) return cuda_fail(e, "gate launch");
         return ok();
     }
@@ -1057,8 +1274,8 @@ engram_status engram_prepass(const engram_ctx* ctx, int layer, const uint32_t* d
         const StreamKWs w = stream_k_ws(ctx, T);
         char* rest = static_cast<char*>(d_workspace) + staged_e_bytes(ctx, T);
         a.stream_k = 1;
-        a.sk_slots = reinterpret_cast<float*>(rest + w.kv);
-        a.sk_flags = reinterpret_cast<uint32_t*>(rest + w.kv + w.slots);
+        a.sk_slots = reinterpret_cast<float*>(rest + w.part + w.v);
+        a.sk_flags = reinterpret_cast<uint32_t*>(rest + w.part + w.v + w.slots);
     }
     e = pairs ? launch_project_tma_pair(a, L.f16, tmA, *tmB, s)
               : launch_project_tma(a, L.f16, tmA, *tmB, s);
@@ -1086,7 +1303,7 @@ engram_status engram_gate_bf16kv(const engram_ctx* ctx, int layer, const uint16_
 engram_status engram_project_windows(const engram_ctx* ctx, int layer, const uint32_t* d_windows,
                                      int64_t T, float* d_kv, void* stream) {
     engram_status st = check_layer(ctx, layer, true);
-    if (st || (st = check_T(T))) return st;
+    if (st || (st = check_T(T)) || (st = check_full_table(ctx, layer))) return st;
     if (T == 0) return ok();
     if (!d_windows || !d_kv || !aligned16(d_windows) || !aligned16(d_kv))
         return fail(ENGRAM_EINVAL, "windows / kv (16-byte aligned)");

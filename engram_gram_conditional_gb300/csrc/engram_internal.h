@@ -41,9 +41,15 @@ constexpr int kBK = 64;   // reduction slice per pipeline stage (128-byte rows)
 
 enum EpilogueMode : int {
     kEpiStoreKv = 0,   // write kv fp32
-    kEpiForward = 3    // the gate: key tiles publish per-(token, branch, tile) sums
+    kEpiForward = 3,   // the gate: key tiles publish per-(token, branch, tile) sums
                        // and the last key tile of each M block quadrant turns them
                        // into gates; value tiles wait for those, then hidden += g v
+    kEpiForwardSk = 4  // stream K (a batch too small to fill the GPU), the gate's
+                       // first half: the piece that finishes a key tile (after
+                       // adding the later ranges' parked pieces) publishes its
+                       // sums, one that finishes a value tile stores v [T][d];
+                       // nothing waits for gates, and launch_gate_sums then
+                       // turns the sums into gates and updates hidden
 };
 
 struct MmaArgs {
@@ -92,7 +98,7 @@ struct MmaArgs {
     float* split_partials;
     uint32_t* split_counters;
     float* gates;          // [T][hc] or null
-    // kEpiStoreKv with stream K (k_splits == 1): the (tile, stage) sequence of the
+    // kEpiStoreKv with stream K, and kEpiForwardSk (k_splits == 1): the (tile, stage) sequence of the
     // launch is cut into one contiguous range per CTA (or pair); a tile that two
     // ranges share is finished by the range holding its first stage, which adds
     // the parked partials of the later ranges in order.  One 128 x 256 fp32 slot
@@ -110,8 +116,21 @@ cudaError_t launch_table_fill(uint64_t seed, uint8_t* data, uint8_t* scale, uint
 // The same rows stored as BF16 values (the dequantised MXFP8 values, exact).
 cudaError_t launch_table_fill_bf16(uint64_t seed, uint16_t* data, uint64_t row_begin,
                                    uint64_t row_end, int row_dim, cudaStream_t s);
+// rows [T][nb], or with bucket_major [nb][T]
 cudaError_t launch_hash(const HashParams& hp, const uint4* windows, int64_t T, uint32_t* rows,
-                        cudaStream_t s);
+                        bool bucket_major, cudaStream_t s);
+// A table sharded over ranks by bucket.  Owner side: the raw rows (row_dim
+// codes, row_dim / 32 scale bytes, zeros to row_dim + 16 bytes) of n global
+// row ids from a shard holding rows [row_lo, row_lo + nrows).  Requester side:
+// those rows, bucket-major [nb][T], decoded into the staged operand e as
+// launch_gather_stage writes it (rows_bm [nb][T]: the requester's row indices,
+// for the masked rows; n_clear words at `clear` zeroed as there).
+cudaError_t launch_shard_gather_raw(const uint32_t* ids, int64_t n, uint64_t row_lo, uint64_t nrows,
+                                    int row_dim, const uint8_t* table, const uint8_t* scales,
+                                    uint8_t* raw, uint32_t* err, cudaStream_t s);
+cudaError_t launch_stage_raw(const HashParams& hp, const uint32_t* rows_bm, const uint8_t* raw,
+                             int64_t T, int row_dim, bool f16, int exp_shift, uint16_t* e,
+                             uint32_t* err, uint32_t* clear, int n_clear, cudaStream_t s);
 // table_bf16: BF16 rows [R][row_dim] without scales (scales unused).
 cudaError_t launch_gather(const Geometry& g, const uint32_t* rows, int64_t T,
                           const uint8_t* table, const uint8_t* scales, uint64_t nrows,
@@ -122,6 +141,13 @@ cudaError_t launch_gather(const Geometry& g, const uint32_t* rows, int64_t T,
 cudaError_t launch_gate(const Geometry& g, const void* kv, bool kv_bf16, int nsplit,
                         int64_t split_stride, const uint4* windows, int64_t T, uint16_t* hidden,
                         const float* wqk, float* gates, cudaStream_t s);
+// The gate's second half after a kEpiForwardSk GEMM: per token, the gates from
+// the key tiles' sums partials [T][hc][d / 256][groups][3] (added in (tile,
+// group) order), then hidden_b += g_b v with v [T][d] fp32; image rows pass
+// through with gate 0.  hidden and v 16-byte aligned; gates [T][hc] or null.
+cudaError_t launch_gate_sums(const Geometry& g, const float* partials, int groups, const float* v,
+                             const uint4* windows, int64_t T, uint16_t* hidden, float* gates,
+                             cudaStream_t s);
 // out = a * b elementwise (fp32, n values).
 cudaError_t launch_mul_f32(const float* a, const float* b, float* out, int64_t n, cudaStream_t s);
 // Bind-time scans: out[0] = min, out[1] = max of n E8M0 bytes (out preset by
@@ -169,6 +195,10 @@ cudaError_t launch_forward_tma_pair(const MmaArgs& a, bool f16, const CUtensorMa
 // Staged forward, step 2: the whole forward GEMM with a TMA-fed A operand.
 cudaError_t launch_forward_tma(const MmaArgs& a, bool f16, const CUtensorMap& tmA,
                                const CUtensorMap& tmB, cudaStream_t s);
+// The same forward GEMM of a small batch with stream K (a.stream_k = 1, the
+// gate epilogue on the pieces that finish tiles), on CTA pairs or single CTAs.
+cudaError_t launch_forward_sk(const MmaArgs& a, bool f16, bool pairs, const CUtensorMap& tmA,
+                              const CUtensorMap& tmB, cudaStream_t s);
 int device_sm_count();
 
 }  // namespace engram

@@ -118,13 +118,49 @@ __global__ void k_table_fill_bf16(uint64_t seed, uint16_t* __restrict__ data, ui
 
 // a2: one thread per (token, bucket).
 __global__ void k_hash(const __grid_constant__ HashParams hp, const uint4* __restrict__ windows,
-                       int64_t T, uint32_t* __restrict__ rows) {
+                       int64_t T, uint32_t* __restrict__ rows, int bucket_major) {
     const int64_t items = T * hp.nb;
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < items;
          i += (int64_t)gridDim.x * blockDim.x) {
         const int64_t t = i / hp.nb;
         const int b = (int)(i - t * hp.nb);
-        rows[i] = hash_bucket(hp, windows[t], b);
+        rows[bucket_major ? b * T + t : i] = hash_bucket(hp, windows[t], b);
+    }
+}
+
+// Owner side of a table sharded over ranks by bucket: the raw MXFP8 rows of
+// the n global row ids a rank received.  A raw row is row_dim + 16 bytes: the
+// row_dim E4M3 codes, then its row_dim / 32 E8M0 scale bytes, zero-padded to
+// 16.  One thread per 16-byte chunk.  The shard holds rows [row_lo, row_lo +
+// nrows); a masked id gives a zero row; an id outside the shard gives a zero
+// row and sets the error word.
+__global__ void k_shard_gather_raw(const uint32_t* __restrict__ ids, int64_t n, uint64_t row_lo,
+                                   uint64_t nrows, int row_dim, const uint8_t* __restrict__ table,
+                                   const uint8_t* __restrict__ scales, uint8_t* __restrict__ raw,
+                                   uint32_t* err) {
+    const int cpr = row_dim / 16;  // code chunks; chunk cpr holds the scales
+    const int64_t items = n * (int64_t)(cpr + 1);
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < items;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = i / (cpr + 1);
+        const int j = (int)(i - r * (cpr + 1));
+        const uint32_t id = ids[r];
+        bool ok = id != kMasked;
+        const uint64_t local = (uint64_t)id - row_lo;
+        if (ok && ((uint64_t)id < row_lo || local >= nrows)) {
+            if (j == 0) atomicOr(err, kErrBounds);
+            ok = false;
+        }
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (ok && j < cpr) {
+            v = __ldg(reinterpret_cast<const uint4*>(table + local * row_dim) + j);
+        } else if (ok) {
+            uint32_t w[4] = {0, 0, 0, 0};
+            const uint8_t* s = scales + local * (row_dim / 32);
+            for (int k = 0; k < row_dim / 32; ++k) w[k >> 2] |= (uint32_t)__ldg(s + k) << (8 * (k & 3));
+            v = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        reinterpret_cast<uint4*>(raw + r * (int64_t)(row_dim + 16))[j] = v;
     }
 }
 
@@ -175,12 +211,19 @@ __global__ void k_gather(const uint32_t* __restrict__ rows, int64_t T, int nb, i
 // kernel before; every thread waits for it (pdl_wait) before its first store,
 // since e may still be read by the GEMM of the previous call.  Block 0 then
 // also zeroes n_clear words at `clear` (the stream-K flags of the GEMM after).
-template <bool kF16>
+// kRaw: the rows come not from the table but from raw MXFP8 rows that the
+// ranks owning their buckets returned (k_shard_gather_raw), bucket-major:
+// row (t, b) at raw + (b T + t) (row_dim + 16); rows_bm [nb][T] are the
+// requester's own row indices, which mark the masked rows.  A raw scale that
+// the FP16 operand cannot take (outside the layer's bound exponent span)
+// gives a zero row and sets the error word.
+template <bool kF16, bool kRaw>
 __global__ void k_gather_stage(const __grid_constant__ HashParams hp, const uint4* __restrict__ windows,
                                int64_t T, int row_dim, const uint8_t* __restrict__ table,
                                const uint8_t* __restrict__ scales, uint64_t nrows, int exp_shift,
                                int table_bf16, uint16_t* __restrict__ e, uint32_t* err,
-                               uint32_t* __restrict__ clear, int n_clear) {
+                               uint32_t* __restrict__ clear, int n_clear,
+                               const uint32_t* __restrict__ rows_bm, const uint8_t* __restrict__ raw) {
     // the GEMM that reads e may start its prologue as soon as every CTA of
     // this grid runs (it waits for this grid's end before reading e)
     pdl_launch_dependents();
@@ -204,24 +247,41 @@ __global__ void k_gather_stage(const __grid_constant__ HashParams hp, const uint
         const int b = live_item ? (int)(item - t * hp.nb) : 0;
         uint32_t row = kMasked;
         if (live_item && chunk == 0) {
-            row = hash_bucket(hp, windows[t], b);
-            if (row != kMasked && (uint64_t)row >= nrows) {
-                atomicOr(err, kErrBounds);
-                row = kMasked;
+            if (kRaw) {
+                row = rows_bm[b * T + t];
+            } else {
+                row = hash_bucket(hp, windows[t], b);
+                if (row != kMasked && (uint64_t)row >= nrows) {
+                    atomicOr(err, kErrBounds);
+                    row = kMasked;
+                }
             }
         }
         row = __shfl_sync(0xFFFFFFFFu, row, sub * lpr);
         if (!live_item) continue;
         uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
-        if (row != kMasked && !kF16 && table_bf16) {  // BF16 rows: a copy
+        if (row != kMasked && !kF16 && !kRaw && table_bf16) {  // BF16 rows: a copy
             const uint4* src = reinterpret_cast<const uint4*>(table + (uint64_t)row * row_dim * 2) + chunk * 2;
             lo = __ldg(src);
             hi = __ldg(src + 1);
         } else if (row != kMasked) {
-            const uint4 c = __ldg(reinterpret_cast<const uint4*>(table + (uint64_t)row * row_dim) + chunk);
-            const uint32_t se = __ldg(scales + (uint64_t)row * (row_dim / 32) + chunk / 2);
+            uint4 c;
+            uint32_t se;
+            if (kRaw) {
+                const uint8_t* rr = raw + (b * T + t) * (int64_t)(row_dim + 16);
+                c = __ldg(reinterpret_cast<const uint4*>(rr) + chunk);
+                se = __ldg(rr + row_dim + chunk / 2);
+            } else {
+                c = __ldg(reinterpret_cast<const uint4*>(table + (uint64_t)row * row_dim) + chunk);
+                se = __ldg(scales + (uint64_t)row * (row_dim / 32) + chunk / 2);
+            }
+            int ex = (int)se - 127 + exp_shift;  // in [-24, 15] for a bound table (its scan)
+            if (kF16 && kRaw && (ex < -24 || ex > 15)) {
+                atomicOr(err, kErrBounds);
+                c = make_uint4(0, 0, 0, 0);
+                ex = 0;
+            }
             if (kF16) {
-                const int ex = (int)se - 127 + exp_shift;  // in [-24, 15] (checked at bind)
                 const uint32_t h = ex >= -14 ? (uint32_t)(ex + 15) << 10 : 1u << (ex + 24);
                 const uint32_t sc2 = h | (h << 16);
                 const uint32_t w[4] = {c.x, c.y, c.z, c.w};
@@ -299,6 +359,67 @@ __device__ __forceinline__ float4 kv_load4(const void* row, int64_t i, int nspli
 // and a batch of T tokens gives T hc CTAs of two short passes each.  Image
 // rows (c_t == DEAD) are left untouched.
 constexpr int kGateBranchThreads = 256;
+
+// The gate's second half after the stream-K GEMM whose key tiles published
+// their sums (Σk², Σh², Σh w_q w_k k per (token, branch, column tile, epilogue
+// group)) and whose value tiles stored v [T][d].  CTA (t, part) takes columns
+// [part d / parts, (part + 1) d / parts) of token t for every branch: it
+// turns the branch sums into gates (added in (tile, group) order, as the
+// whole-tile gate epilogue adds them), then hidden_b += g_b v with one BF16
+// rounding, v read once for all branches.  Image rows pass through.
+constexpr int kGateSumsThreads = 256;
+__global__ void __launch_bounds__(kGateSumsThreads)
+k_gate_sums(const float* __restrict__ partials, int groups, const float* __restrict__ v,
+            const uint4* __restrict__ windows, int hc, int d, float eps, int parts,
+            uint16_t* __restrict__ hidden, float* __restrict__ gates) {
+    __shared__ float gsh[8];
+    pdl_wait();  // launched to overlap the end of the GEMM that writes the sums and v
+    pdl_launch_dependents();
+    const int64_t t = blockIdx.x / parts;
+    const int part = (int)(blockIdx.x - t * parts);
+    if (windows[t].x == kDead) {
+        if (gates && part == 0 && (int)threadIdx.x < hc) gates[t * hc + threadIdx.x] = 0.0f;
+        return;
+    }
+    if ((int)threadIdx.x < hc) {
+        const int P = d / 256 * groups;
+        const float* pp = partials + (t * hc + threadIdx.x) * (int64_t)P * 3;
+        float s0 = 0.f, s1 = 0.f, s2 = 0.f;
+        for (int p = 0; p < P; ++p) {
+            s0 += __ldcg(pp + 3 * p);
+            s1 += __ldcg(pp + 3 * p + 1);
+            s2 += __ldcg(pp + 3 * p + 2);
+        }
+        const float g = gate_from_sums(s0, s1, s2, d, eps);
+        gsh[threadIdx.x] = g;
+        if (gates && part == 0) gates[t * hc + threadIdx.x] = g;
+    }
+    __syncthreads();
+    float g[8];
+#pragma unroll
+    for (int b = 0; b < 8; ++b) g[b] = b < hc ? gsh[b] : 0.f;
+    const int n4 = d / 4;
+    const int c0 = part * n4 / parts, c1 = (part + 1) * n4 / parts;
+    const float4* vt = reinterpret_cast<const float4*>(v + t * (int64_t)d);
+    uint2* const ht = reinterpret_cast<uint2*>(hidden + t * hc * (int64_t)d);
+#pragma unroll 1
+    for (int i = c0 + (int)threadIdx.x; i < c1; i += kGateSumsThreads) {
+        const float4 vi = __ldcg(vt + i);
+        uint2 h2[8];
+#pragma unroll
+        for (int b = 0; b < 8; ++b)
+            if (b < hc) h2[b] = ht[(int64_t)b * n4 + i];
+#pragma unroll
+        for (int b = 0; b < 8; ++b)
+            if (b < hc) {
+                const float o0 = fmaf(g[b], vi.x, bf16_bits_to_f32(h2[b].x & 0xFFFFu));
+                const float o1 = fmaf(g[b], vi.y, bf16_bits_to_f32(h2[b].x >> 16));
+                const float o2 = fmaf(g[b], vi.z, bf16_bits_to_f32(h2[b].y & 0xFFFFu));
+                const float o3 = fmaf(g[b], vi.w, bf16_bits_to_f32(h2[b].y >> 16));
+                ht[(int64_t)b * n4 + i] = make_uint2(bf16x2_pack_rn(o0, o1), bf16x2_pack_rn(o2, o3));
+            }
+    }
+}
 
 // Thirty-two registers a thread (eight CTAs per SM): latency is hidden by
 // resident CTAs rather than by loads in flight per thread.  kv is fp32, or
@@ -386,10 +507,19 @@ k_gate_branch(const void* __restrict__ kv, int nsplit, int64_t split_stride,
 // Bind-time scans and the FP16 copy of wkv.
 __global__ void k_scale_range(const uint8_t* __restrict__ s, uint64_t n, uint32_t* out) {
     uint32_t lo = 255u, hi = 0u;
-    const uint64_t nv = n / 16;
-    for (uint64_t i = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; i < nv;
-         i += (uint64_t)gridDim.x * blockDim.x) {
-        const uint4 v = __ldg(reinterpret_cast<const uint4*>(s) + i);
+    const uint64_t tid = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x;
+    const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
+    // bytes up to the first 16-byte boundary one by one, then 16 at a time,
+    // then the tail one by one (s may start anywhere)
+    const uint64_t head = min(n, (uint64_t)((16u - ((uintptr_t)s & 15u)) & 15u));
+    for (uint64_t i = tid; i < head; i += stride) {
+        lo = min(lo, (uint32_t)s[i]);
+        hi = max(hi, (uint32_t)s[i]);
+    }
+    const uint64_t nv = (n - head) / 16;
+    const uint4* sv = reinterpret_cast<const uint4*>(s + head);
+    for (uint64_t i = tid; i < nv; i += stride) {
+        const uint4 v = __ldg(sv + i);
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
@@ -398,8 +528,7 @@ __global__ void k_scale_range(const uint8_t* __restrict__ s, uint64_t n, uint32_
             hi = max(hi, b);
         }
     }
-    for (uint64_t i = nv * 16 + blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; i < n;
-         i += (uint64_t)gridDim.x * blockDim.x) {
+    for (uint64_t i = head + nv * 16 + tid; i < n; i += stride) {
         lo = min(lo, (uint32_t)s[i]);
         hi = max(hi, (uint32_t)s[i]);
     }
@@ -465,10 +594,11 @@ cudaError_t launch_table_fill(uint64_t seed, uint8_t* data, uint8_t* scale, uint
 }
 
 cudaError_t launch_hash(const HashParams& hp, const uint4* windows, int64_t T, uint32_t* rows,
-                        cudaStream_t s) {
+                        bool bucket_major, cudaStream_t s) {
     if (T == 0) return cudaSuccess;
     const int threads = 256;
-    k_hash<<<grid_for(T * hp.nb, threads, 8), threads, 0, s>>>(hp, windows, T, rows);
+    k_hash<<<grid_for(T * hp.nb, threads, 8), threads, 0, s>>>(hp, windows, T, rows,
+                                                               bucket_major ? 1 : 0);
     return cudaGetLastError();
 }
 
@@ -517,6 +647,27 @@ __global__ void k_mul_f32(const float* __restrict__ a, const float* __restrict__
         out[i] = a[i] * b[i];
 }
 
+cudaError_t launch_gate_sums(const Geometry& g, const float* partials, int groups, const float* v,
+                             const uint4* windows, int64_t T, uint16_t* hidden, float* gates,
+                             cudaStream_t s) {
+    if (T == 0) return cudaSuccess;
+    if (g.hc > 8 || g.d % kBN != 0 || groups < 1) return cudaErrorInvalidValue;
+    // about one float4 of v per thread: parts x 256 threads x 4 columns ~ d
+    const int parts = std::max(1, g.d / (4 * kGateSumsThreads));
+    if (T * parts > INT32_MAX) return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3((unsigned)(T * parts));
+    cfg.blockDim = dim3(kGateSumsThreads);
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k_gate_sums, partials, groups, v, windows, g.hc, g.d, g.eps,
+                              parts, hidden, gates);
+}
+
 cudaError_t launch_mul_f32(const float* a, const float* b, float* out, int64_t n, cudaStream_t s) {
     if (n == 0) return cudaSuccess;
     k_mul_f32<<<grid_for(n, 256, 8), 256, 0, s>>>(a, b, out, n);
@@ -562,11 +713,52 @@ cudaError_t launch_gather_stage(const HashParams& hp, const uint4* windows, int6
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    const uint32_t* no_rows = nullptr;
+    const uint8_t* no_raw = nullptr;
     if (f16)
-        return cudaLaunchKernelEx(&cfg, k_gather_stage<true>, hp, windows, T, row_dim, table,
-                                  scales, nrows, exp_shift, 0, e, err, clear, n_clear);
-    return cudaLaunchKernelEx(&cfg, k_gather_stage<false>, hp, windows, T, row_dim, table, scales,
-                              nrows, exp_shift, table_bf16 ? 1 : 0, e, err, clear, n_clear);
+        return cudaLaunchKernelEx(&cfg, k_gather_stage<true, false>, hp, windows, T, row_dim, table,
+                                  scales, nrows, exp_shift, 0, e, err, clear, n_clear, no_rows,
+                                  no_raw);
+    return cudaLaunchKernelEx(&cfg, k_gather_stage<false, false>, hp, windows, T, row_dim, table,
+                              scales, nrows, exp_shift, table_bf16 ? 1 : 0, e, err, clear, n_clear,
+                              no_rows, no_raw);
+}
+
+cudaError_t launch_stage_raw(const HashParams& hp, const uint32_t* rows_bm, const uint8_t* raw,
+                             int64_t T, int row_dim, bool f16, int exp_shift, uint16_t* e,
+                             uint32_t* err, uint32_t* clear, int n_clear, cudaStream_t s) {
+    if (T == 0) return cudaSuccess;
+    const int threads = 256;
+    const int64_t rows_per_warp = 32 / (row_dim / 16);
+    const int64_t warps = (T * hp.nb + rows_per_warp - 1) / rows_per_warp;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(grid_for(warps * 32, threads, 8));
+    cfg.blockDim = dim3(threads);
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const uint4* no_windows = nullptr;
+    const uint8_t* no_table = nullptr;
+    if (f16)
+        return cudaLaunchKernelEx(&cfg, k_gather_stage<true, true>, hp, no_windows, T, row_dim,
+                                  no_table, no_table, (uint64_t)0, exp_shift, 0, e, err, clear,
+                                  n_clear, rows_bm, raw);
+    return cudaLaunchKernelEx(&cfg, k_gather_stage<false, true>, hp, no_windows, T, row_dim,
+                              no_table, no_table, (uint64_t)0, exp_shift, 0, e, err, clear, n_clear,
+                              rows_bm, raw);
+}
+
+cudaError_t launch_shard_gather_raw(const uint32_t* ids, int64_t n, uint64_t row_lo, uint64_t nrows,
+                                    int row_dim, const uint8_t* table, const uint8_t* scales,
+                                    uint8_t* raw, uint32_t* err, cudaStream_t s) {
+    if (n == 0) return cudaSuccess;
+    const int threads = 256;
+    k_shard_gather_raw<<<grid_for(n * (row_dim / 16 + 1), threads, 16), threads, 0, s>>>(
+        ids, n, row_lo, nrows, row_dim, table, scales, raw, err);
+    return cudaGetLastError();
 }
 
 int device_sm_count() { return sm_count(); }

@@ -118,7 +118,7 @@ struct Layout {
     // ring stages (each kKS k-blocks)
     static constexpr int kA = kASrc == kASrcGatherBucket ? 8 : kKS == 2 ? 3 : 4;
     static constexpr int kB = kASrc == kASrcGatherBucket ? 3
-                              : kKS == 2                 ? (kMode == kEpiStoreKv ? 4 : 3)
+                              : kKS == 2 ? (kMode == kEpiStoreKv || kMode == kEpiForwardSk ? 4 : 3)
                               : kPair                    ? 8
                                                          : 4;
     static constexpr int kAStageBytes = kAStage * kKS;
@@ -868,7 +868,9 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
     // this unit's contiguous range [g0, g1) of the launch's (tile, stage)
     // sequence, one piece per tile the range touches.
     const int nst_tile = KB / kKS;
-    const bool sk = kMode == kEpiStoreKv && a.stream_k != 0;
+    const bool sk = (kMode == kEpiStoreKv && a.stream_k != 0) || kMode == kEpiForwardSk;
+    // the gate epilogue, on whole tiles (kEpiForward) or on stream-K pieces
+    constexpr bool kFwd = kMode == kEpiForward || kMode == kEpiForwardSk;
     const int64_t sk_total = (int64_t)m_units * a.n_tiles * nst_tile;
     auto sk_start = [&](int u) { return (int64_t)u * sk_total / istep; };
     const int64_t sk_g0 = sk_start(item0), sk_g1 = sk_start(item0 + 1);
@@ -1189,21 +1191,21 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
         const int eslot = kWideEpi ? warp : q;
         const int m = q * 32 + lane;
         int tc = 0;
-        if (kMode == kEpiForward && item0 < total && grp == 0) {
-            int mb, nt, ks;
-            coords(item0, mb, nt, ks);
-            if (mb < a.m_blocks) prefetch_hidden(a, mb, nt, m);
-        }
+        // the hidden slices an item's gate epilogue reads travel to L2 while the
+        // item before it is finished (a stream-K piece that only parks reads none)
+        auto prefetch_item = [&](int i) {
+            int mb2, nt2, ks2, kb2, nkb2, lo2, hi2;
+            get_item(i, mb2, nt2, ks2, kb2, nkb2, lo2, hi2);
+            // (kEpiForwardSk: a value tile only stores v and reads no hidden)
+            const bool value2 = (a.n_tile_begin + nt2) * kBN >= a.hc * a.d;
+            if (mb2 < a.m_blocks && !(sk && lo2 > 0) && !(kMode == kEpiForwardSk && value2))
+                prefetch_hidden(a, mb2, nt2, m);
+        };
+        if (kFwd && n_items > 0 && grp == 0) prefetch_item(0);
         for (; tc < n_items; ++tc) {
-            const int tile = item0 + tc * istep;  // (without stream K)
             int mb, nt, ks, kb_lo, nkb, st_lo, st_hi;
             get_item(tc, mb, nt, ks, kb_lo, nkb, st_lo, st_hi);
-            // the next tile's hidden slices travel to L2 while this one is finished
-            if (kMode == kEpiForward && tile + istep < total && grp == 0) {
-                int mb2, nt2, ks2;
-                coords(tile + istep, mb2, nt2, ks2);
-                if (mb2 < a.m_blocks) prefetch_hidden(a, mb2, nt2, m);
-            }
+            if (kFwd && tc + 1 < n_items && grp == 0) prefetch_item(tc + 1);
             const int acc = tc & 1;
             const uint32_t aph = (uint32_t)(tc >> 1) & 1u;
             int full_ok = 1;
@@ -1219,7 +1221,7 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
             const int n0 = (a.n_tile_begin + nt) * kBN;
             // an odd pair CTA past the last M block has no rows to write
             int holds_sum = mb < a.m_blocks ? 1 : 0;
-            if (holds_sum && kMode == kEpiForward && a.k_splits > 1) {
+            if (holds_sum && kFwd && a.k_splits > 1) {
                 holds_sum = split_k_quadrant(a, mb, nt, ks, q, lane, taddr, abort_flag, lim);
                 if (holds_sum < 0) {
                     if (lane == 0) fail();
@@ -1228,7 +1230,7 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
             }
             if (!holds_sum) {
                 // partial parked for the split that arrives last
-            } else if (kMode == kEpiStoreKv && sk && st_lo > 0) {
+            } else if (sk && st_lo > 0) {
                 // stream K, a piece after the tile's first: park the raw
                 // accumulator in this CTA's slot ([quadrant][chunk][float4][lane],
                 // 512 contiguous bytes per warp store) and raise the quadrant's flag
@@ -1249,11 +1251,12 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
                 __threadfence();
                 __syncwarp();
                 if (lane == 0) st_release_u32(a.sk_flags + cta * kSkFlagsPerCta + eslot, 1u);
-            } else if (kMode == kEpiStoreKv) {
-                // Stream K, the tile's first piece but not all of it: the later
-                // stages lie in the ranges of the next units (each holds one of
-                // them as its first piece, parked in its slot); wait (bounded) for
-                // those and add them in unit order, which is k order.
+            } else {
+                // The piece that finishes the tile.  With stream K, when it is
+                // the tile's first piece but not all of it, the later stages lie
+                // in the ranges of the next units (each holds one of them as its
+                // first piece, parked in its slot): wait (bounded) for those and
+                // add them in unit order, which is k order.
                 int u_last = item0;
                 if (sk && st_hi < nst_tile) {
                     const int64_t g_end = (int64_t)(sk_j0 + tc) * nst_tile + nst_tile - 1;
@@ -1282,20 +1285,13 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
                     }
                     __threadfence();
                 }
-                // A lane holds 32 columns of its own row.  An 8 x 8 transpose of
-                // float4 within each group of 8 lanes (three butterfly rounds of
-                // shuffles) gives lane 8 g + j the float4 j of rows 8 g .. 8 g + 7,
-                // so that each store writes four whole 128-byte row segments
-                // instead of 32 scattered 16-byte pieces.
-                const int g8 = lane & ~7, j8 = lane & 7;
-                float* const kv0 = a.kv + ks * a.kv_split_stride + n0 + j8 * 4;
-                const int64_t row0 = (int64_t)mb * kBM + q * 32 + g8;
-#pragma unroll 1
-                for (int c = c_first; c < kBN / 32; c += kCStep) {
+                // Columns [32 c, 32 c + 32) of this lane's row of the tile: the
+                // TMEM accumulator plus the later ranges' parked pieces, in range
+                // order, scaled back to kv.
+                auto acc_chunk = [&](int c, float (&v)[32]) {
                     uint32_t r[32];
                     tmem_ld32(taddr + (uint32_t)(c * 32), r);
                     tmem_wait_ld();
-                    float v[32];
 #pragma unroll
                     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 #pragma unroll 1
@@ -1315,6 +1311,23 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
                     }
 #pragma unroll
                     for (int i = 0; i < 32; ++i) v[i] *= a.out_scale;
+                };
+                // kEpiForwardSk: a value tile stores its 256 columns of v into
+                // kv = v [T][d] (its gate runs later, from the key tiles' sums)
+                const int kv_col0 = kMode == kEpiForwardSk ? a.hc * a.d : 0;
+                if (kMode == kEpiStoreKv || (kMode == kEpiForwardSk && n0 >= a.hc * a.d)) {
+                // A lane holds 32 columns of its own row.  An 8 x 8 transpose of
+                // float4 within each group of 8 lanes (three butterfly rounds of
+                // shuffles) gives lane 8 g + j the float4 j of rows 8 g .. 8 g + 7,
+                // so that each store writes four whole 128-byte row segments
+                // instead of 32 scattered 16-byte pieces.
+                const int g8 = lane & ~7, j8 = lane & 7;
+                float* const kv0 = a.kv + ks * a.kv_split_stride + (n0 - kv_col0) + j8 * 4;
+                const int64_t row0 = (int64_t)mb * kBM + q * 32 + g8;
+#pragma unroll 1
+                for (int c = c_first; c < kBN / 32; c += kCStep) {
+                    float v[32];
+                    acc_chunk(c, v);
                     if (a.kv_bf16) {
                         // kv rounded once to BF16: the lane's 64 bytes are four
                         // 16-byte pieces; a 4 x 4 transpose within each group of 4
@@ -1345,7 +1358,7 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
                             }
                         }
                         const int64_t row4 = (int64_t)mb * kBM + q * 32 + (lane & ~3);
-                        uint16_t* const kvb = reinterpret_cast<uint16_t*>(a.kv) + n0 + c * 32 +
+                        uint16_t* const kvb = reinterpret_cast<uint16_t*>(a.kv) + (n0 - kv_col0) + c * 32 +
                                               (lane & 3) * 8;
 #pragma unroll
                         for (int i = 0; i < 4; ++i)
@@ -1380,7 +1393,7 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
                                 make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
                     }
                 }
-            } else if (kMode == kEpiForward && n0 < a.hc * a.d) {
+            } else if (kFwd && n0 < a.hc * a.d) {
                 const int branch = n0 / a.d;
                 const int col0 = n0 - branch * a.d;
                 const bool text = t < a.T && a.windows[t].x != kDead;
@@ -1389,15 +1402,15 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
                 float skk = 0.f, shh = 0.f, shk = 0.f;
 #pragma unroll 1
                 for (int c = c_first; c < kBN / 32; c += kCStep) {
-                    uint32_t r[32];
-                    tmem_ld32(taddr + (uint32_t)(c * 32), r);
+                    // the hidden slice's loads go out before the accumulator is read
                     uint4 hv[4];
                     if (text) {
 #pragma unroll
                         for (int i = 0; i < 4; ++i)
                             hv[i] = __ldg(reinterpret_cast<const uint4*>(hrow + c * 32) + i);
                     }
-                    tmem_wait_ld();
+                    float kv[32];
+                    acc_chunk(c, kv);  // warp-collective: every lane, text row or not
                     if (text) {
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
@@ -1408,7 +1421,7 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
 #pragma unroll
                             for (int e = 0; e < 8; ++e) {
                                 const float h = (e & 1) ? bf16_hi(hw[e >> 1]) : bf16_lo(hw[e >> 1]);
-                                const float k = __uint_as_float(r[8 * i + e]) * a.out_scale;
+                                const float k = kv[8 * i + e];
                                 skk = fmaf(k, k, skk);
                                 shh = fmaf(h, h, shh);
                                 shk = fmaf(h * wqk[e], k, shk);
@@ -1451,7 +1464,7 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
                         if (lane == 0) st_release_u32(cnt + 1, 1u);
                     }
                 }
-            } else {  // value tile
+            } else {  // value tile (kEpiForward)
                 if (kMode == kEpiForward) {
                     // wait (bounded) for the gates of this M block quadrant
                     if (lane == 0) {
@@ -1492,9 +1505,8 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
                 uint16_t* const hrow = a.hidden + t * a.hc * (int64_t)a.d + cv;
 #pragma unroll 1
                 for (int c = c_first; c < kBN / 32; c += kCStep) {
-                    uint32_t r[32];
-                    tmem_ld32(taddr + (uint32_t)(c * 32), r);
-                    tmem_wait_ld();
+                    float vv[32];
+                    acc_chunk(c, vv);
                     if (text) {
 #pragma unroll
                         for (int b0 = 0; b0 < 8; b0 += 2) {
@@ -1521,8 +1533,8 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
                                             uint32_t o[4];
 #pragma unroll
                                             for (int e2 = 0; e2 < 4; ++e2) {
-                                                const float v0 = __uint_as_float(r[8 * i + 2 * e2]) * a.out_scale;
-                                                const float v1 = __uint_as_float(r[8 * i + 2 * e2 + 1]) * a.out_scale;
+                                                const float v0 = vv[8 * i + 2 * e2];
+                                                const float v1 = vv[8 * i + 2 * e2 + 1];
                                                 o[e2] = bf16x2_pack_rn(fmaf(gb, v0, bf16_lo(hw[e2])),
                                                                        fmaf(gb, v1, bf16_hi(hw[e2])));
                                             }
@@ -1534,6 +1546,7 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
                     }
                 }
             }
+            }  // the piece that finishes the tile
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {
@@ -1581,9 +1594,14 @@ cudaError_t launch(const MmaArgs& a, const CUtensorMap& tmA, const CUtensorMap& 
     }
     // work units: the (tile, split)s, or with stream K the (tile, stage)s
     constexpr int kKS = k_blocks_per_stage<kASrc, kF16>();
-    if (a.stream_k && (kMode != kEpiStoreKv || a.k_splits != 1 || (a.K / kBK) % kKS != 0))
+    // stream K: the kv-store epilogue, or the gate epilogue of kEpiForwardSk
+    // (which always runs it), on the TMA-fed operand, one split
+    if ((kMode == kEpiForwardSk) != (a.stream_k && kMode != kEpiStoreKv)) return cudaErrorInvalidValue;
+    if (a.stream_k && (kMode == kEpiForward || a.k_splits != 1 || (a.K / kBK) % kKS != 0 ||
+                       (kMode == kEpiForwardSk && kASrc != kASrcTma && kASrc != kASrcTmaPair)))
         return cudaErrorInvalidValue;
-    if (kMode == kEpiForward && a.epi_groups != epilogue_groups<kASrc>()) return cudaErrorInvalidValue;
+    if ((kMode == kEpiForward || kMode == kEpiForwardSk) && a.epi_groups != epilogue_groups<kASrc>())
+        return cudaErrorInvalidValue;
     const int stages = a.stream_k ? (a.K / kBK) / kKS : a.k_splits;
     if (kASrc == kASrcTmaPair) {
         // clusters of two; no more pairs than can be resident at once, since
@@ -1686,6 +1704,15 @@ cudaError_t launch_forward_tma(const MmaArgs& a, bool f16, const CUtensorMap& tm
                                const CUtensorMap& tmB, cudaStream_t s) {
     if (f16) return launch<kASrcTma, true, kEpiForward>(a, tmA, tmB, s);
     return launch<kASrcTma, false, kEpiForward>(a, tmA, tmB, s);
+}
+
+cudaError_t launch_forward_sk(const MmaArgs& a, bool f16, bool pairs, const CUtensorMap& tmA,
+                              const CUtensorMap& tmB, cudaStream_t s) {
+    if (pairs)
+        return f16 ? launch<kASrcTmaPair, true, kEpiForwardSk>(a, tmA, tmB, s)
+                   : launch<kASrcTmaPair, false, kEpiForwardSk>(a, tmA, tmB, s);
+    return f16 ? launch<kASrcTma, true, kEpiForwardSk>(a, tmA, tmB, s)
+               : launch<kASrcTma, false, kEpiForwardSk>(a, tmA, tmB, s);
 }
 
 // Operand paths of the fused kernels: bucket gather (256-wide rows) or k-block

@@ -1,16 +1,20 @@
 """Device memory plumbing for a set of Engram layers.
 
-PyTorch allocates the buffers (device HBM, or pinned host memory for a table
-read through UVA); the library fills the tables on the device and binds the
-weights.  No forward arithmetic happens here.
+PyTorch allocates the device buffers (HBM); a table read through UVA lives in
+the library's registered, huge-page-advised host memory
+(engram_host_table_alloc).  The library fills the tables on the device and
+binds the weights.  No forward arithmetic happens here.
 """
 from __future__ import annotations
+
+import ctypes
 
 import numpy as np
 import torch
 
-from . import (BIND_TABLE_BF16, engram_ctx_create, engram_ctx_destroy, engram_layer_bind,
-               engram_layer_params, engram_table_fill, engram_table_fill_bf16)
+from . import (BIND_TABLE_BF16, engram_ctx_create, engram_ctx_destroy, engram_host_table_alloc,
+               engram_host_table_free, engram_layer_bind, engram_layer_params, engram_table_fill,
+               engram_table_fill_bf16)
 
 
 def _round16(n: int) -> int:
@@ -40,6 +44,7 @@ class EngramLayerSet:
         self.n_layers = len(layer_seeds)
         self.params = [engram_layer_params(self.ctx, l, self.nb) for l in range(self.n_layers)]
         self.tensors = [dict() for _ in range(self.n_layers)]
+        self._host = []  # (address, bytes) of host tables from engram_host_table_alloc
 
     @classmethod
     def from_workload(cls, w, token_map, device="cuda"):
@@ -62,23 +67,33 @@ class EngramLayerSet:
         count stay allocated but outside the bound table)."""
         rows = self.rows(layer)
         rd = self.geom["row_dim"]
-        where = dict(pin_memory=True) if host_table else dict(device=self.device)
+
+        def buf(nbytes):
+            # host tables: the library's registered, huge-page-advised host
+            # memory (zeroed); device tables: HBM from torch
+            if not host_table:
+                return torch.zeros(nbytes, dtype=torch.uint8, device=self.device)
+            ptr = engram_host_table_alloc(nbytes)
+            self._host.append((ptr, nbytes))
+            arr = np.ctypeslib.as_array((ctypes.c_uint8 * nbytes).from_address(ptr))
+            return torch.from_numpy(arr)
+
         if table is not None:
             codes = np.ascontiguousarray(table[0], np.uint8).reshape(-1)
             scl = np.ascontiguousarray(table[1], np.uint8).reshape(-1)
             assert codes.size >= rows * rd and scl.size * 32 == codes.size and not flags & BIND_TABLE_BF16
-            table_t = torch.zeros(_round16(codes.size), dtype=torch.uint8, **where)
-            scales = torch.zeros(_round16(scl.size), dtype=torch.uint8, **where)
+            table_t = buf(_round16(codes.size))
+            scales = buf(_round16(scl.size))
             table_t[:codes.size].copy_(torch.from_numpy(codes))
             scales[:scl.size].copy_(torch.from_numpy(scl))
             table = table_t
         elif flags & BIND_TABLE_BF16:
-            table = torch.empty(_round16(rows * rd * 2), dtype=torch.uint8, **where)
+            table = buf(_round16(rows * rd * 2))
             scales = None
             engram_table_fill_bf16(self.ctx, table_seed, table, 0, rows, stream)
         else:
-            table = torch.empty(_round16(rows * rd), dtype=torch.uint8, **where)
-            scales = torch.empty(_round16(rows * rd // 32), dtype=torch.uint8, **where)
+            table = buf(_round16(rows * rd))
+            scales = buf(_round16(rows * rd // 32))
             engram_table_fill(self.ctx, table_seed, table, scales, 0, rows, stream)
         d_wkv = _as_device(wkv, torch.int16, self.device).view(self.N, self.K)
         d_wq = _as_device(wq, torch.float32, self.device).view(-1)
@@ -90,6 +105,11 @@ class EngramLayerSet:
 
     def close(self):
         if self.ctx is not None:
+            if self._host:
+                torch.cuda.synchronize(self.device)  # no kernel reads a table freed below
             engram_ctx_destroy(self.ctx)
             self.ctx = None
         self.tensors = []
+        for ptr, nbytes in self._host:
+            engram_host_table_free(ptr, nbytes)
+        self._host = []

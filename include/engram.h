@@ -195,6 +195,20 @@ engram_status engram_table_fill(const engram_ctx* ctx, uint64_t seed, uint8_t* d
 engram_status engram_table_fill_bf16(const engram_ctx* ctx, uint64_t seed, uint16_t* data,
                                      uint64_t row_begin, uint64_t row_end, void* stream);
 
+/* Host memory for a table read through UVA (vLLM "Engram" wiki, "CPU 오프로드":
+ * the table in pinned host memory, read by the GPU).  bytes of an anonymous
+ * mapping, advised to use transparent huge pages where the kernel offers them,
+ * zeroed (every page touched, in parallel) and registered with CUDA, mapped
+ * into the device address space; *out is both its host and its device
+ * address.  Random row reads from a table this large are bound by address
+ * translation, which huge pages reduce: on GB300 (64 KB base pages, 512 MB
+ * huge pages), gathering 8,192 tokens x 24 rows from a 101 GB table took
+ * 12.8 ms from cudaHostAlloc memory and 5.3 ms from this.  The caller owns the
+ * memory and releases it with engram_host_table_free(p, bytes) once no layer
+ * is bound to it. */
+engram_status engram_host_table_alloc(uint64_t bytes, void** out);
+engram_status engram_host_table_free(void* p, uint64_t bytes);
+
 /* Sessions: a hash history (the last three compressed ids and a count).
  * "第四步": every token enters the history exactly once; prefill appends a
  * span, decode appends one token; fork copies the history; reset empties it.
@@ -311,6 +325,70 @@ engram_status engram_stage_rows(const engram_ctx* ctx, int layer, const uint32_t
 engram_status engram_forward_staged_rows(const engram_ctx* ctx, int layer,
                                          const uint32_t* d_windows, int64_t T, uint16_t* d_hidden,
                                          void* d_workspace, float* d_gates, void* stream);
+
+/* A table sharded over data-parallel ranks by bucket (vLLM "Engram" wiki,
+ * section "데이터 병렬 토폴로지": with embedding_across_dp the hash heads are
+ * spread over the co-located replicas; each replica looks up the rows of its
+ * own heads for the ids every replica sends it and returns them, an
+ * all-to-all that replaces an all-reduce, as in the FlagScale plugin's
+ * decoupled parallelism).  Rank r owns a contiguous range of buckets, hence a
+ * contiguous range of the layer's table rows, and holds only those.  Per
+ * step: every rank hashes its own windows bucket-major
+ * (engram_hash_by_bucket), sends each owner the ids of the owner's buckets
+ * (the caller's collective), the owner gathers the raw rows of the ids it
+ * received (engram_shard_gather_raw), the requester receives them back in
+ * bucket order and decodes them into its staged operand
+ * (engram_stage_raw_rows); engram_forward_staged_rows then runs the GEMM and
+ * the gate on its own tokens.  The collectives themselves are the caller's
+ * (the package's sharded.py runs them with torch.distributed). */
+
+/* Bind a layer to a shard of its table: table/scales hold rows
+ * [row_lo, row_lo + w->rows) of the layer's table (w->rows may be 0, with null
+ * table and scales, for a rank that owns no bucket); wkv, wq, wk are whole.
+ * scale_min..scale_max is the E8M0 exponent span of the WHOLE table (the
+ * ranks combine their shards' spans), which picks the operand encoding as
+ * engram_layer_bind's scan does.  MXFP8 tables only (a BF16-table flag is
+ * ENGRAM_EUNSUPPORTED).  A layer bound this way serves
+ * engram_shard_gather_raw, engram_stage_raw_rows, engram_forward_staged_rows,
+ * engram_project and engram_gate; the calls that index the table with global
+ * row numbers (engram_gather_dequant, engram_forward, engram_forward_noalloc,
+ * engram_forward_staged, engram_stage_rows, engram_project_windows,
+ * engram_prepass) return ENGRAM_ESTATE. */
+engram_status engram_layer_bind_shard(engram_ctx* ctx, int layer, const engram_layer_weights* w,
+                                      uint64_t row_lo, uint32_t scale_min, uint32_t scale_max);
+/* The smallest and largest of n E8M0 bytes (device or mapped pinned host
+ * memory): a shard's span, for the ranks to combine before
+ * engram_layer_bind_shard.  n = 0 gives 255 and 0.  Synchronises the device.
+ * To fill a shard that holds rows [row_lo, row_hi) with engram_table_fill,
+ * which writes row r at data + r row_dim and its scales at scale + r row_dim /
+ * 32, pass data - row_lo row_dim and scale - row_lo row_dim / 32 with that
+ * row range: only rows inside the shard are written. */
+engram_status engram_scale_range(engram_ctx* ctx, const uint8_t* scales, uint64_t n,
+                                 uint32_t* scale_min, uint32_t* scale_max);
+/* engram_hash with the row indices bucket-major: d_rows_bm [nb][T], so that
+ * the ids of a range of buckets are one contiguous block per owner. */
+engram_status engram_hash_by_bucket(const engram_ctx* ctx, int layer, const uint32_t* d_windows,
+                                    int64_t T, uint32_t* d_rows_bm, void* stream);
+/* Bytes of one raw row: row_dim E4M3 codes, row_dim / 32 E8M0 scale bytes,
+ * zero padding to row_dim + 16 (272 at row_dim 256). */
+size_t engram_raw_row_bytes(const engram_ctx* ctx);
+/* Owner side: d_raw [n][engram_raw_row_bytes] (device, 16-byte aligned) gets
+ * the raw rows of the n global row ids d_ids (device uint32), read from the
+ * rows this layer is bound to (a shard, or the whole table).  A masked id
+ * gives a zero row; an id outside the bound rows gives a zero row and sets
+ * the error word (ENGRAM_EBOUNDS at the next engram_sync). */
+engram_status engram_shard_gather_raw(const engram_ctx* ctx, int layer, const uint32_t* d_ids,
+                                      int64_t n, uint8_t* d_raw, void* stream);
+/* Requester side: decode raw rows, bucket-major d_raw_bm [nb][T][raw row]
+ * (16-byte aligned), into the staged operand at the start of d_workspace
+ * (engram_forward_staged_workspace_bytes(ctx, T) bytes), as engram_stage_rows
+ * would from the table; d_rows_bm [nb][T] are this rank's own row indices
+ * (engram_hash_by_bucket), which mark the masked rows.  A raw scale outside
+ * the bound exponent span gives zeros and sets the error word.  Then call
+ * engram_forward_staged_rows on the same workspace. */
+engram_status engram_stage_raw_rows(const engram_ctx* ctx, int layer, const uint32_t* d_rows_bm,
+                                    const uint8_t* d_raw_bm, int64_t T, void* d_workspace,
+                                    void* stream);
 
 /* engram_forward for callers that cannot allocate device memory.  The pages
  * have no counterpart: this is a deployment variant.  A serving engine that

@@ -201,8 +201,11 @@ def test_back_to_back_calls_on_one_stream_share_a_workspace(prefill):
     for i, (o, r) in enumerate(zip(outs, ref)):
         for a, b in zip(o, r):
             assert np.array_equal(a.cpu().numpy(), b), f"call {i}"
-    # the staged forward of a small batch is the stream-K pre-pass plus the gate
-    assert np.array_equal(ref[0][0], ref[3][0])
+    # the staged forward of a small batch (the gate as the stream-K GEMM's
+    # epilogue) and the stream-K pre-pass plus the gate kernel compute the same
+    # step; the gate's sums are added in another order, so compare within the
+    # tolerance of the oracle check
+    check_hidden(ref[3][0].view(np.uint16), ref[0][0].view(np.uint16), "staged vs pre-pass + gate")
 
 
 @pytest.mark.parametrize("T", [256, 2048])
