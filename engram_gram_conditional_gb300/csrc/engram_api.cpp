@@ -1055,8 +1055,18 @@ size_t engram_forward_staged_workspace_bytes(const engram_ctx* ctx, int64_t T) {
     if (!ctx || T <= 0) return 0;
     const size_t e = staged_e_bytes(ctx, T);
     if (staged_stream_k(ctx, T)) return e + stream_k_ws(ctx, T).total();
-    // the TMA-fed kernels run two epilogue warps per TMEM quadrant
-    return e + forward_workspace_bytes_groups(ctx, T, 8, 2);
+    // the TMA-fed kernels run two epilogue warps per TMEM quadrant; then one
+    // has-text flag per 128-token block
+    return e + forward_workspace_bytes_groups(ctx, T, 8, 2) +
+           ((((size_t)T + kBM - 1) / kBM * sizeof(uint32_t) + 255) & ~(size_t)255);
+}
+
+// The has-text flags of a large batch's blocks in its staged workspace (null
+// for a small batch, whose stream-K GEMM skips nothing).
+static uint32_t* staged_block_text(const engram_ctx* ctx, int64_t T, void* d_workspace) {
+    if (staged_stream_k(ctx, T)) return nullptr;
+    return reinterpret_cast<uint32_t*>(static_cast<char*>(d_workspace) + staged_e_bytes(ctx, T) +
+                                       forward_workspace_bytes_groups(ctx, T, 8, 2));
 }
 
 // The stream-K flags a small batch's staging zeroes (null, 0 for a large one).
@@ -1089,13 +1099,15 @@ engram_status engram_stage_raw_rows(const engram_ctx* ctx, int layer, const uint
     cudaError_t e = launch_stage_raw(hash_params(ctx, layer), d_rows_bm, d_raw_bm, T,
                                      (int)ctx->desc.row_dim, L.f16, L.a_exp_shift,
                                      static_cast<uint16_t*>(d_workspace), ctx->d_err, clear,
-                                     n_clear, (cudaStream_t)stream);
+                                     n_clear, nullptr, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "raw staging launch");
     return ok();
 }
 
-engram_status engram_stage_rows(const engram_ctx* ctx, int layer, const uint32_t* d_windows,
-                                int64_t T, void* d_workspace, void* stream) {
+// Step 1 of the staged forward; flags: also write which 128-token blocks hold
+// a text row, for a GEMM that compacts its units (the chunks of a long batch).
+static engram_status stage_impl(const engram_ctx* ctx, int layer, const uint32_t* d_windows,
+                                int64_t T, void* d_workspace, void* stream, bool flags) {
     engram_status st = check_layer(ctx, layer, true);
     if (st || (st = check_T(T)) || (st = check_full_table(ctx, layer))) return st;
     if (T == 0) return ok();
@@ -1112,9 +1124,16 @@ engram_status engram_stage_rows(const engram_ctx* ctx, int layer, const uint32_t
                                         (int)ctx->desc.row_dim, L.w.table, L.w.scales, L.rows,
                                         L.table_bf16, L.f16, L.a_exp_shift,
                                         static_cast<uint16_t*>(d_workspace), ctx->d_err, clear,
-                                        n_clear, (cudaStream_t)stream);
+                                        n_clear,
+                                        flags ? staged_block_text(ctx, T, d_workspace) : nullptr,
+                                        (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "staged gather launch");
     return ok();
+}
+
+engram_status engram_stage_rows(const engram_ctx* ctx, int layer, const uint32_t* d_windows,
+                                int64_t T, void* d_workspace, void* stream) {
+    return stage_impl(ctx, layer, d_windows, T, d_workspace, stream, false);
 }
 
 // The GEMM of the staged entry reading e through TMA: `a` with the layer's
@@ -1152,20 +1171,23 @@ static cudaError_t staged_gemm(const engram_ctx* ctx, int layer, int64_t T, void
 
 
 // Step 2 of the staged forward; flags_clear: the stream-K flags of the
-// workspace were zeroed earlier on the stream (else this call zeroes them).
+// workspace were zeroed earlier on the stream (else this call zeroes them);
+// compact: the staging wrote the block flags, and the GEMM of a large batch
+// runs only the M units that hold text.
 static engram_status staged_rows(const engram_ctx* ctx, int layer, const uint32_t* d_windows,
                                  int64_t T, uint16_t* d_hidden, void* d_workspace, float* d_gates,
-                                 void* stream, bool flags_clear);
+                                 void* stream, bool flags_clear, bool compact);
 
 engram_status engram_forward_staged_rows(const engram_ctx* ctx, int layer,
                                          const uint32_t* d_windows, int64_t T, uint16_t* d_hidden,
                                          void* d_workspace, float* d_gates, void* stream) {
-    return staged_rows(ctx, layer, d_windows, T, d_hidden, d_workspace, d_gates, stream, false);
+    return staged_rows(ctx, layer, d_windows, T, d_hidden, d_workspace, d_gates, stream, false,
+                       false);
 }
 
 static engram_status staged_rows(const engram_ctx* ctx, int layer, const uint32_t* d_windows,
                                  int64_t T, uint16_t* d_hidden, void* d_workspace, float* d_gates,
-                                 void* stream, bool flags_clear) {
+                                 void* stream, bool flags_clear, bool compact) {
     engram_status st = check_layer(ctx, layer, true);
     if (st || (st = check_T(T))) return st;
     if (T == 0) return ok();
@@ -1214,6 +1236,9 @@ static engram_status staged_rows(const engram_ctx* ctx, int layer, const uint32_
         return ok();
     }
     e = forward_bind_ws(ctx, T, 8, 2, rest, a, s);
+    // the staging wrote which blocks hold text: the GEMM runs only the units
+    // that hold some (a unit of image rows only passes through)
+    a.block_text = compact ? staged_block_text(ctx, T, d_workspace) : nullptr;
     // the pair kernel finishes the key tiles M unit by M unit: a unit's value
     // tiles then find their gates ready (2,048 tokens: 0.417 -> 0.399 ms);
     // the fused kernel keeps the N-major order, which suits it better
@@ -1225,6 +1250,28 @@ static engram_status staged_rows(const engram_ctx* ctx, int layer, const uint32_
     return ok();
 }
 
+// Chunk of a long staged batch: a multiple of 256 tokens (a CTA-pair unit)
+// from 3,072 to 6,144 (e of 36 to 72 MB, inside the 126 MB L2 beside the wkv
+// stream), the one whose output tiles (units x N / 256) leave the least of a
+// last wave idle on this device's CTA pairs; the smallest such on a tie.  On
+// 152 SMs: 4,864 tokens, 19 units x 100 tiles = 25 waves of 76 pairs exactly
+// (4,096 tokens gave 21 waves and 4 tiles).
+static int64_t staged_chunk_tokens(const engram_ctx* ctx) {
+    const int64_t pairs = std::max(1, device_sm_count() / 2);
+    const int64_t nt = ctx->N / kBN;
+    int64_t best = 4096, best_idle = -1;
+    for (int64_t units = 12; units <= 24; ++units) {
+        const int64_t tiles = units * nt;
+        const int64_t idle = (pairs - tiles % pairs) % pairs;  // empty slots of the last wave
+        // per tile of work, so that larger chunks are not favoured by size alone
+        if (best_idle < 0 || idle * best / 256 < best_idle * units) {
+            best = units * 256;
+            best_idle = idle;
+        }
+    }
+    return best;
+}
+
 engram_status engram_forward_staged(const engram_ctx* ctx, int layer, const uint32_t* d_windows,
                                     int64_t T, uint16_t* d_hidden, void* d_workspace,
                                     float* d_gates, void* stream) {
@@ -1234,11 +1281,31 @@ engram_status engram_forward_staged(const engram_ctx* ctx, int layer, const uint
     if (!d_windows || !d_hidden || !d_workspace || !aligned16(d_windows) || !aligned16(d_hidden) ||
         !aligned16(d_workspace))
         return fail(ENGRAM_EINVAL, "windows / hidden / workspace (16-byte aligned)");
-    // the gather zeroes a small batch's stream-K flags, so that nothing stands
-    // between the gather and the GEMM that it hands its rows to
-    st = engram_stage_rows(ctx, layer, d_windows, T, d_workspace, stream);
-    if (st) return st;
-    return staged_rows(ctx, layer, d_windows, T, d_hidden, d_workspace, d_gates, stream, true);
+    // A long batch runs in chunks on the same workspace, so that each chunk's
+    // operand matrix e (12 KB a token) stays in L2 between the gather that
+    // writes it and the GEMM that reads it, instead of going through HBM; a
+    // chunk's gather waits for the GEMM before it (as two calls in a row do)
+    // before it overwrites e.
+    // The chunks of a long batch also run only their M units that hold text
+    // (units of image rows only pass through): their GEMMs wait for the
+    // staging before loading wkv, which costs a few microseconds a chunk
+    // against the whole units a long image span saves.  A batch of one chunk
+    // (the 2,048-token prefill) keeps the early wkv loads.
+    const int64_t chunk = staged_chunk_tokens(ctx);
+    const bool compact = T > chunk;
+    for (int64_t t0 = 0; t0 < T; t0 += chunk) {
+        const int64_t n = std::min(chunk, T - t0);
+        const uint32_t* w = d_windows + t0 * 4;
+        uint16_t* h = d_hidden + t0 * (int64_t)ctx->desc.hc * ctx->desc.d;
+        float* g = d_gates ? d_gates + t0 * (int64_t)ctx->desc.hc : nullptr;
+        // the gather zeroes a small batch's stream-K flags, so that nothing stands
+        // between the gather and the GEMM that it hands its rows to
+        st = stage_impl(ctx, layer, w, n, d_workspace, stream, compact);
+        if (st) return st;
+        st = staged_rows(ctx, layer, w, n, h, d_workspace, g, stream, true, compact);
+        if (st) return st;
+    }
+    return ok();
 }
 
 engram_status engram_prepass(const engram_ctx* ctx, int layer, const uint32_t* d_windows, int64_t T,

@@ -44,12 +44,15 @@ enum EpilogueMode : int {
     kEpiForward = 3,   // the gate: key tiles publish per-(token, branch, tile) sums
                        // and the last key tile of each M block quadrant turns them
                        // into gates; value tiles wait for those, then hidden += g v
-    kEpiForwardSk = 4  // stream K (a batch too small to fill the GPU), the gate's
-                       // first half: the piece that finishes a key tile (after
-                       // adding the later ranges' parked pieces) publishes its
-                       // sums, one that finishes a value tile stores v [T][d];
-                       // nothing waits for gates, and launch_gate_sums then
-                       // turns the sums into gates and updates hidden
+    kEpiForwardSk = 4,  // stream K (a batch too small to fill the GPU), the gate's
+                        // first half: the piece that finishes a key tile (after
+                        // adding the later ranges' parked pieces) publishes its
+                        // sums, one that finishes a value tile stores v [T][d];
+                        // nothing waits for gates, and launch_gate_sums then
+                        // turns the sums into gates and updates hidden
+    kEpiForwardCompact = 5  // kEpiForward over the M units that hold a text row
+                            // only (MmaArgs::block_text); a separate instantiation,
+                            // so that kEpiForward's code is untouched by it
 };
 
 struct MmaArgs {
@@ -107,6 +110,12 @@ struct MmaArgs {
     int stream_k;
     float* sk_slots;
     uint32_t* sk_flags;
+    // kEpiForward on a TMA-fed operand without splits: per 128-token block,
+    // nonzero when it holds a text row (written by the staging kernel); the
+    // items of an M unit whose blocks hold only image rows are skipped by every
+    // role (those rows pass through; their gates are written as 0).  Null: no
+    // skipping.
+    const uint32_t* block_text;
     HashParams hp;
 };
 
@@ -128,9 +137,12 @@ cudaError_t launch_hash(const HashParams& hp, const uint4* windows, int64_t T, u
 cudaError_t launch_shard_gather_raw(const uint32_t* ids, int64_t n, uint64_t row_lo, uint64_t nrows,
                                     int row_dim, const uint8_t* table, const uint8_t* scales,
                                     uint8_t* raw, uint32_t* err, cudaStream_t s);
+// (block_text, may be null: set to 1 for every block - raw rows carry no
+// image marks, so nothing is skipped)
 cudaError_t launch_stage_raw(const HashParams& hp, const uint32_t* rows_bm, const uint8_t* raw,
                              int64_t T, int row_dim, bool f16, int exp_shift, uint16_t* e,
-                             uint32_t* err, uint32_t* clear, int n_clear, cudaStream_t s);
+                             uint32_t* err, uint32_t* clear, int n_clear, uint32_t* block_text,
+                             cudaStream_t s);
 // table_bf16: BF16 rows [R][row_dim] without scales (scales unused).
 cudaError_t launch_gather(const Geometry& g, const uint32_t* rows, int64_t T,
                           const uint8_t* table, const uint8_t* scales, uint64_t nrows,
@@ -160,10 +172,13 @@ cudaError_t launch_absmax_bf16(const uint16_t* x, uint64_t n, uint32_t* out, cud
 // rows of the last 128-token block past T are not written), or BF16 row-major
 // [T][K].  Also zeroes n_clear words at `clear` (may be null with 0), once the
 // kernel before it in the stream has finished.
+// block_text (may be null): per 128-token block, 1 when it holds a text row,
+// else 0 (written after the kernel before it has finished).
 cudaError_t launch_gather_stage(const HashParams& hp, const uint4* windows, int64_t T, int row_dim,
                                 const uint8_t* table, const uint8_t* scales, uint64_t nrows,
                                 bool table_bf16, bool f16, int exp_shift, uint16_t* e,
-                                uint32_t* err, uint32_t* clear, int n_clear, cudaStream_t s);
+                                uint32_t* err, uint32_t* clear, int n_clear, uint32_t* block_text,
+                                cudaStream_t s);
 // FP16 copy of the BF16 wkv [N][K] (N % 128 == 0, K % 64 == 0), values x
 // scale rounded to nearest even, stored as 128 x 64 tiles: element (n, k) at
 // ((n / 128) (K / 64) + k / 64) 8192 + (n % 128) 64 + k % 64.

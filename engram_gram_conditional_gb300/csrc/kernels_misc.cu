@@ -223,7 +223,8 @@ __global__ void k_gather_stage(const __grid_constant__ HashParams hp, const uint
                                const uint8_t* __restrict__ scales, uint64_t nrows, int exp_shift,
                                int table_bf16, uint16_t* __restrict__ e, uint32_t* err,
                                uint32_t* __restrict__ clear, int n_clear,
-                               const uint32_t* __restrict__ rows_bm, const uint8_t* __restrict__ raw) {
+                               const uint32_t* __restrict__ rows_bm, const uint8_t* __restrict__ raw,
+                               uint32_t* __restrict__ block_text) {
     // the GEMM that reads e may start its prologue as soon as every CTA of
     // this grid runs (it waits for this grid's end before reading e)
     pdl_launch_dependents();
@@ -316,6 +317,24 @@ __global__ void k_gather_stage(const __grid_constant__ HashParams hp, const uint
         dst[0] = lo;
         dst[1] = hi;
     }
+    // Per 128-token block: does it hold a text row?  The GEMM after this skips
+    // the units whose blocks hold only image rows.  Raw rows carry no image
+    // marks: every block counts as text.  (Written after the wait: the GEMM
+    // before may still read the flags.)
+    if (block_text) {
+        if (!waited) pdl_wait();
+        const int64_t nblk = (T + 127) / 128;
+        for (int64_t mb = warp0; mb < nblk; mb += nwarps) {
+            bool text = kRaw;
+            if (!kRaw)
+                for (int r = lane; r < 128; r += 32) {
+                    const int64_t t = mb * 128 + r;
+                    if (t < T && windows[t].x != kDead) text = true;
+                }
+            text = __any_sync(0xFFFFFFFFu, text);
+            if (lane == 0) block_text[mb] = text ? 1u : 0u;
+        }
+    }
 }
 
 // a5 standalone.  kv may be the sum of nsplit partial buffers split_stride
@@ -366,12 +385,18 @@ constexpr int kGateBranchThreads = 256;
 // [part d / parts, (part + 1) d / parts) of token t for every branch: it
 // turns the branch sums into gates (added in (tile, group) order, as the
 // whole-tile gate epilogue adds them), then hidden_b += g_b v with one BF16
-// rounding, v read once for all branches.  Image rows pass through.
+// rounding, v read once for all branches.  Image rows pass through.  Each
+// thread owns at most one float4 of columns (parts = ceil(d / 4 / threads)),
+// and every load is issued at once: the thread's v and hidden, and all of
+// the token's sums (hc x d / 256 x groups x 3 floats, staged in shared
+// memory by the whole CTA) before the gates are added up, so the kernel
+// waits for memory about once.
 constexpr int kGateSumsThreads = 256;
 __global__ void __launch_bounds__(kGateSumsThreads)
 k_gate_sums(const float* __restrict__ partials, int groups, const float* __restrict__ v,
             const uint4* __restrict__ windows, int hc, int d, float eps, int parts,
             uint16_t* __restrict__ hidden, float* __restrict__ gates) {
+    extern __shared__ float sums[];  // [hc][P][3] of this token
     __shared__ float gsh[8];
     pdl_wait();  // launched to overlap the end of the GEMM that writes the sums and v
     pdl_launch_dependents();
@@ -381,44 +406,47 @@ k_gate_sums(const float* __restrict__ partials, int groups, const float* __restr
         if (gates && part == 0 && (int)threadIdx.x < hc) gates[t * hc + threadIdx.x] = 0.0f;
         return;
     }
-    if ((int)threadIdx.x < hc) {
-        const int P = d / 256 * groups;
-        const float* pp = partials + (t * hc + threadIdx.x) * (int64_t)P * 3;
+    const int n4 = d / 4;
+    const int i = part * kGateSumsThreads + (int)threadIdx.x;  // this thread's float4 column
+    const bool live = i < n4;
+    uint2* const ht = reinterpret_cast<uint2*>(hidden + t * hc * (int64_t)d);
+    float4 vi = make_float4(0.f, 0.f, 0.f, 0.f);
+    uint2 h2[8];
+    if (live) {
+        vi = __ldcg(reinterpret_cast<const float4*>(v + t * (int64_t)d) + i);
+#pragma unroll
+        for (int b = 0; b < 8; ++b)
+            if (b < hc) h2[b] = ht[(int64_t)b * n4 + i];
+    }
+    const int P = d / 256 * groups;
+    const int nsum = hc * P * 3;
+    const float* pt = partials + t * (int64_t)nsum;
+    for (int k = threadIdx.x; k < nsum; k += kGateSumsThreads) sums[k] = __ldcg(pt + k);
+    __syncthreads();
+    if ((int)threadIdx.x < hc) {  // (column tile, group) order, as the whole-tile epilogue adds them
+        const float* pp = sums + threadIdx.x * P * 3;
         float s0 = 0.f, s1 = 0.f, s2 = 0.f;
         for (int p = 0; p < P; ++p) {
-            s0 += __ldcg(pp + 3 * p);
-            s1 += __ldcg(pp + 3 * p + 1);
-            s2 += __ldcg(pp + 3 * p + 2);
+            s0 += pp[3 * p];
+            s1 += pp[3 * p + 1];
+            s2 += pp[3 * p + 2];
         }
         const float g = gate_from_sums(s0, s1, s2, d, eps);
         gsh[threadIdx.x] = g;
         if (gates && part == 0) gates[t * hc + threadIdx.x] = g;
     }
     __syncthreads();
-    float g[8];
+    if (!live) return;
 #pragma unroll
-    for (int b = 0; b < 8; ++b) g[b] = b < hc ? gsh[b] : 0.f;
-    const int n4 = d / 4;
-    const int c0 = part * n4 / parts, c1 = (part + 1) * n4 / parts;
-    const float4* vt = reinterpret_cast<const float4*>(v + t * (int64_t)d);
-    uint2* const ht = reinterpret_cast<uint2*>(hidden + t * hc * (int64_t)d);
-#pragma unroll 1
-    for (int i = c0 + (int)threadIdx.x; i < c1; i += kGateSumsThreads) {
-        const float4 vi = __ldcg(vt + i);
-        uint2 h2[8];
-#pragma unroll
-        for (int b = 0; b < 8; ++b)
-            if (b < hc) h2[b] = ht[(int64_t)b * n4 + i];
-#pragma unroll
-        for (int b = 0; b < 8; ++b)
-            if (b < hc) {
-                const float o0 = fmaf(g[b], vi.x, bf16_bits_to_f32(h2[b].x & 0xFFFFu));
-                const float o1 = fmaf(g[b], vi.y, bf16_bits_to_f32(h2[b].x >> 16));
-                const float o2 = fmaf(g[b], vi.z, bf16_bits_to_f32(h2[b].y & 0xFFFFu));
-                const float o3 = fmaf(g[b], vi.w, bf16_bits_to_f32(h2[b].y >> 16));
-                ht[(int64_t)b * n4 + i] = make_uint2(bf16x2_pack_rn(o0, o1), bf16x2_pack_rn(o2, o3));
-            }
-    }
+    for (int b = 0; b < 8; ++b)
+        if (b < hc) {
+            const float g = gsh[b];
+            const float o0 = fmaf(g, vi.x, bf16_bits_to_f32(h2[b].x & 0xFFFFu));
+            const float o1 = fmaf(g, vi.y, bf16_bits_to_f32(h2[b].x >> 16));
+            const float o2 = fmaf(g, vi.z, bf16_bits_to_f32(h2[b].y & 0xFFFFu));
+            const float o3 = fmaf(g, vi.w, bf16_bits_to_f32(h2[b].y >> 16));
+            ht[(int64_t)b * n4 + i] = make_uint2(bf16x2_pack_rn(o0, o1), bf16x2_pack_rn(o2, o3));
+        }
 }
 
 // Thirty-two registers a thread (eight CTAs per SM): latency is hidden by
@@ -652,15 +680,18 @@ cudaError_t launch_gate_sums(const Geometry& g, const float* partials, int group
                              cudaStream_t s) {
     if (T == 0) return cudaSuccess;
     if (g.hc > 8 || g.d % kBN != 0 || groups < 1) return cudaErrorInvalidValue;
-    // about one float4 of v per thread: parts x 256 threads x 4 columns ~ d
-    const int parts = std::max(1, g.d / (4 * kGateSumsThreads));
+    // at most one float4 of v per thread
+    const int parts = (g.d / 4 + kGateSumsThreads - 1) / kGateSumsThreads;
     if (T * parts > INT32_MAX) return cudaErrorInvalidValue;
+    const size_t smem = (size_t)g.hc * (g.d / kBN) * groups * 3 * sizeof(float);
+    if (smem > 48 * 1024) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.gridDim = dim3((unsigned)(T * parts));
     cfg.blockDim = dim3(kGateSumsThreads);
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
@@ -697,7 +728,8 @@ cudaError_t launch_wkv_to_f16_tiles(const uint16_t* src, uint16_t* dst, uint64_t
 cudaError_t launch_gather_stage(const HashParams& hp, const uint4* windows, int64_t T, int row_dim,
                                 const uint8_t* table, const uint8_t* scales, uint64_t nrows,
                                 bool table_bf16, bool f16, int exp_shift, uint16_t* e,
-                                uint32_t* err, uint32_t* clear, int n_clear, cudaStream_t s) {
+                                uint32_t* err, uint32_t* clear, int n_clear, uint32_t* block_text,
+                                cudaStream_t s) {
     if (T == 0) return cudaSuccess;
     if (table_bf16 && f16) return cudaErrorInvalidValue;  // BF16 rows feed BF16 operands
     const int threads = 256;
@@ -718,15 +750,16 @@ cudaError_t launch_gather_stage(const HashParams& hp, const uint4* windows, int6
     if (f16)
         return cudaLaunchKernelEx(&cfg, k_gather_stage<true, false>, hp, windows, T, row_dim, table,
                                   scales, nrows, exp_shift, 0, e, err, clear, n_clear, no_rows,
-                                  no_raw);
+                                  no_raw, block_text);
     return cudaLaunchKernelEx(&cfg, k_gather_stage<false, false>, hp, windows, T, row_dim, table,
                               scales, nrows, exp_shift, table_bf16 ? 1 : 0, e, err, clear, n_clear,
-                              no_rows, no_raw);
+                              no_rows, no_raw, block_text);
 }
 
 cudaError_t launch_stage_raw(const HashParams& hp, const uint32_t* rows_bm, const uint8_t* raw,
                              int64_t T, int row_dim, bool f16, int exp_shift, uint16_t* e,
-                             uint32_t* err, uint32_t* clear, int n_clear, cudaStream_t s) {
+                             uint32_t* err, uint32_t* clear, int n_clear, uint32_t* block_text,
+                             cudaStream_t s) {
     if (T == 0) return cudaSuccess;
     const int threads = 256;
     const int64_t rows_per_warp = 32 / (row_dim / 16);
@@ -745,10 +778,10 @@ cudaError_t launch_stage_raw(const HashParams& hp, const uint32_t* rows_bm, cons
     if (f16)
         return cudaLaunchKernelEx(&cfg, k_gather_stage<true, true>, hp, no_windows, T, row_dim,
                                   no_table, no_table, (uint64_t)0, exp_shift, 0, e, err, clear,
-                                  n_clear, rows_bm, raw);
+                                  n_clear, rows_bm, raw, block_text);
     return cudaLaunchKernelEx(&cfg, k_gather_stage<false, true>, hp, no_windows, T, row_dim,
                               no_table, no_table, (uint64_t)0, exp_shift, 0, e, err, clear, n_clear,
-                              rows_bm, raw);
+                              rows_bm, raw, block_text);
 }
 
 cudaError_t launch_shard_gather_raw(const uint32_t* ids, int64_t n, uint64_t row_lo, uint64_t nrows,

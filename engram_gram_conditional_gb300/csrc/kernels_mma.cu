@@ -771,6 +771,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
       const __grid_constant__ MmaArgs a) {
     constexpr int kKS = k_blocks_per_stage<kASrc, kF16>();
+    // the whole-tile gate epilogue, plain or over the units that hold text
+    constexpr bool kFwdWhole = kMode == kEpiForward || kMode == kEpiForwardCompact;
     using L = Layout<kASrc, kKS, kMode>;
     constexpr int kA = L::kA, kB = L::kB;
     constexpr bool kPair = L::kPair;
@@ -847,12 +849,22 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
 
     // work items: (M unit, N tile, split); a CTA pair shares one item sequence
     // and its M unit is two M blocks, this CTA's being 2 mu + rank
-    const int m_units = kPair ? (a.m_blocks + 1) / 2 : a.m_blocks;
-    const int total = m_units * a.n_tiles * a.k_splits;
+    int m_units = kPair ? (a.m_blocks + 1) / 2 : a.m_blocks;
+    int total = m_units * a.n_tiles * a.k_splits;
+    // Compaction (MmaArgs::block_text): the item sequence covers only the M
+    // units that hold a text row; bit u of units_on is unit u.  Set by
+    // compact_units() in every role alike, after pdl_wait.
+    uint64_t units_on = 0;
+    bool compact = false;
     const int item0 = kPair ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
     const int istep = kPair ? (int)(gridDim.x >> 1) : (int)gridDim.x;
     auto coords = [&](int tile, int& mb, int& nt, int& ks) {
         tile_coords(a, m_units, tile, mb, nt, ks);
+        if (compact) {  // the mb-th unit that holds text (__fns: n-th set bit)
+            const uint32_t lo = (uint32_t)units_on, hi = (uint32_t)(units_on >> 32);
+            const int nlo = __popc(lo);
+            mb = mb < nlo ? (int)__fns(lo, 0, mb + 1) : 32 + (int)__fns(hi, 0, mb - nlo + 1);
+        }
         if constexpr (kPair) mb = 2 * mb + (int)rank;
     };
     const int KB = a.K / kBK;
@@ -869,14 +881,12 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
     // sequence, one piece per tile the range touches.
     const int nst_tile = KB / kKS;
     const bool sk = (kMode == kEpiStoreKv && a.stream_k != 0) || kMode == kEpiForwardSk;
-    // the gate epilogue, on whole tiles (kEpiForward) or on stream-K pieces
-    constexpr bool kFwd = kMode == kEpiForward || kMode == kEpiForwardSk;
     const int64_t sk_total = (int64_t)m_units * a.n_tiles * nst_tile;
     auto sk_start = [&](int u) { return (int64_t)u * sk_total / istep; };
     const int64_t sk_g0 = sk_start(item0), sk_g1 = sk_start(item0 + 1);
     const int sk_j0 = (int)(sk_g0 / nst_tile);
-    const int n_items = sk ? (sk_g1 > sk_g0 ? (int)((sk_g1 - 1) / nst_tile) - sk_j0 + 1 : 0)
-                           : (item0 < total ? (total - item0 + istep - 1) / istep : 0);
+    int n_items = sk ? (sk_g1 > sk_g0 ? (int)((sk_g1 - 1) / nst_tile) - sk_j0 + 1 : 0)
+                     : (item0 < total ? (total - item0 + istep - 1) / istep : 0);
     // item i: output tile (mb, nt), split ks, k-blocks [kb_lo, kb_lo + nkb), and
     // its stage range [st_lo, st_hi) within the tile's nst_tile stages
     auto get_item = [&](int i, int& mb, int& nt, int& ks, int& kb_lo, int& nkb, int& st_lo,
@@ -903,6 +913,34 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
         atomicOr(a.err, kErrTimeout);
     };
 
+    // Compaction of a batch with long image spans (TMA-fed operand, whole
+    // tiles, at most 64 units): the units whose blocks hold only image rows
+    // get no items at all, so the work left stays evenly spread over the
+    // CTAs; those rows pass through and their gates are written as 0 (the
+    // epilogue, below).  Called by all 32 lanes of a warp, after pdl_wait:
+    // the staging kernel writes the flags.
+    const bool may_compact = kMode == kEpiForwardCompact && !kFusedA && !sk && a.k_splits == 1 &&
+                             a.block_text != nullptr && m_units <= 64;
+    auto compact_units = [&]() {
+        if (!may_compact) return;
+        uint64_t on = 0;
+        for (int base = 0; base < m_units; base += 32) {
+            const int u = base + lane;
+            bool text = false;
+            if (u < m_units) {
+                const int b0 = kPair ? 2 * u : u;
+                text = a.block_text[b0] != 0u ||
+                       (kPair && b0 + 1 < a.m_blocks && a.block_text[b0 + 1] != 0u);
+            }
+            on |= (uint64_t)__ballot_sync(0xFFFFFFFFu, text) << base;
+        }
+        units_on = on;
+        compact = true;
+        m_units = __popcll((long long)on);
+        total = m_units * a.n_tiles * a.k_splits;
+        n_items = item0 < total ? (total - item0 + istep - 1) / istep : 0;
+    };
+
     if (warp >= kWarpTma) {
         setmaxnreg_dec<kRegsCtl>();
     }
@@ -910,7 +948,8 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
         // TMA producers: warp 12 loads the wkv tiles, warp 14 the A tiles of
         // the TMA-fed variants, each running ahead on its own ring
         const bool do_b = warp == kWarpTma;
-        if (!do_b) pdl_wait();
+        if (!do_b || may_compact) pdl_wait();
+        compact_units();
         // with one M unit every wkv byte is read once per launch: its lines
         // are marked for early eviction, so that they do not push the
         // launch's outputs (the kv of a small batch) out of L2
@@ -995,6 +1034,8 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
             return kPair ? mbar_wait_cluster(bar, parity, abort_flag, lim)
                          : mbar_wait(bar, parity, abort_flag, lim);
         };
+        if (may_compact) pdl_wait();
+        compact_units();
         if (lane == 0 && issuer) {
             int it = 0, tc = 0;
             bool ok = true;
@@ -1190,22 +1231,34 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
         constexpr int kCStep = kG;
         const int eslot = kWideEpi ? warp : q;
         const int m = q * 32 + lane;
+        compact_units();
+        if (compact && a.gates && grp == 0) {
+            // units of image rows only (no items): their rows' gates are 0,
+            // written by the CTA (pair) that unit index u % istep names
+            for (int u = item0; u < (kPair ? (a.m_blocks + 1) / 2 : a.m_blocks); u += istep) {
+                if ((units_on >> u) & 1u) continue;
+                const int mb = kPair ? 2 * u + (int)rank : u;
+                const int64_t t = (int64_t)mb * kBM + m;
+                if (mb < a.m_blocks && t < a.T)
+                    for (int b = 0; b < a.hc; ++b) a.gates[t * a.hc + b] = 0.0f;
+            }
+        }
         int tc = 0;
-        // the hidden slices an item's gate epilogue reads travel to L2 while the
-        // item before it is finished (a stream-K piece that only parks reads none)
-        auto prefetch_item = [&](int i) {
-            int mb2, nt2, ks2, kb2, nkb2, lo2, hi2;
-            get_item(i, mb2, nt2, ks2, kb2, nkb2, lo2, hi2);
-            // (kEpiForwardSk: a value tile only stores v and reads no hidden)
-            const bool value2 = (a.n_tile_begin + nt2) * kBN >= a.hc * a.d;
-            if (mb2 < a.m_blocks && !(sk && lo2 > 0) && !(kMode == kEpiForwardSk && value2))
-                prefetch_hidden(a, mb2, nt2, m);
-        };
-        if (kFwd && n_items > 0 && grp == 0) prefetch_item(0);
+        if (kFwdWhole && item0 < total && grp == 0) {
+            int mb, nt, ks;
+            coords(item0, mb, nt, ks);
+            if (mb < a.m_blocks) prefetch_hidden(a, mb, nt, m);
+        }
         for (; tc < n_items; ++tc) {
+            const int tile = item0 + tc * istep;  // (without stream K)
             int mb, nt, ks, kb_lo, nkb, st_lo, st_hi;
             get_item(tc, mb, nt, ks, kb_lo, nkb, st_lo, st_hi);
-            if (kFwd && tc + 1 < n_items && grp == 0) prefetch_item(tc + 1);
+            // the next tile's hidden slices travel to L2 while this one is finished
+            if (kFwdWhole && tile + istep < total && grp == 0) {
+                int mb2, nt2, ks2;
+                coords(tile + istep, mb2, nt2, ks2);
+                if (mb2 < a.m_blocks) prefetch_hidden(a, mb2, nt2, m);
+            }
             const int acc = tc & 1;
             const uint32_t aph = (uint32_t)(tc >> 1) & 1u;
             int full_ok = 1;
@@ -1221,7 +1274,7 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
             const int n0 = (a.n_tile_begin + nt) * kBN;
             // an odd pair CTA past the last M block has no rows to write
             int holds_sum = mb < a.m_blocks ? 1 : 0;
-            if (holds_sum && kFwd && a.k_splits > 1) {
+            if (holds_sum && kFwdWhole && a.k_splits > 1) {
                 holds_sum = split_k_quadrant(a, mb, nt, ks, q, lane, taddr, abort_flag, lim);
                 if (holds_sum < 0) {
                     if (lane == 0) fail();
@@ -1230,7 +1283,7 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
             }
             if (!holds_sum) {
                 // partial parked for the split that arrives last
-            } else if (sk && st_lo > 0) {
+            } else if ((kMode == kEpiStoreKv || kMode == kEpiForwardSk) && sk && st_lo > 0) {
                 // stream K, a piece after the tile's first: park the raw
                 // accumulator in this CTA's slot ([quadrant][chunk][float4][lane],
                 // 512 contiguous bytes per warp store) and raise the quadrant's flag
@@ -1251,12 +1304,11 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
                 __threadfence();
                 __syncwarp();
                 if (lane == 0) st_release_u32(a.sk_flags + cta * kSkFlagsPerCta + eslot, 1u);
-            } else {
-                // The piece that finishes the tile.  With stream K, when it is
-                // the tile's first piece but not all of it, the later stages lie
-                // in the ranges of the next units (each holds one of them as its
-                // first piece, parked in its slot): wait (bounded) for those and
-                // add them in unit order, which is k order.
+            } else if (kMode == kEpiStoreKv || kMode == kEpiForwardSk) {
+                // Stream K, the tile's first piece but not all of it: the later
+                // stages lie in the ranges of the next units (each holds one of
+                // them as its first piece, parked in its slot); wait (bounded) for
+                // those and add them in unit order, which is k order.
                 int u_last = item0;
                 if (sk && st_hi < nst_tile) {
                     const int64_t g_end = (int64_t)(sk_j0 + tc) * nst_tile + nst_tile - 1;
@@ -1285,13 +1337,87 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
                     }
                     __threadfence();
                 }
-                // Columns [32 c, 32 c + 32) of this lane's row of the tile: the
-                // TMEM accumulator plus the later ranges' parked pieces, in range
-                // order, scaled back to kv.
-                auto acc_chunk = [&](int c, float (&v)[32]) {
+                // kEpiForwardSk: a key tile publishes its gate sums; a value
+                // tile stores its 256 columns of v into kv = v [T][d]
+                const int kv_col0 = kMode == kEpiForwardSk ? a.hc * a.d : 0;
+                if (kMode == kEpiForwardSk && n0 < a.hc * a.d) {
+                    const int branch = n0 / a.d;
+                    const int col0 = n0 - branch * a.d;
+                    const bool text = t < a.T && a.windows[t].x != kDead;
+                    const uint16_t* hrow = a.hidden + (t * a.hc + branch) * (int64_t)a.d + col0;
+                    const float* wqkr = a.wqk + (int64_t)branch * a.d + col0;
+                    float skk = 0.f, shh = 0.f, shk = 0.f;
+#pragma unroll 1
+                    for (int c = c_first; c < kBN / 32; c += kCStep) {
+                        uint32_t r[32];
+                        tmem_ld32(taddr + (uint32_t)(c * 32), r);
+                        uint4 hv[4];
+                        if (text) {
+#pragma unroll
+                            for (int i = 0; i < 4; ++i)
+                                hv[i] = __ldg(reinterpret_cast<const uint4*>(hrow + c * 32) + i);
+                        }
+                        tmem_wait_ld();
+                        float v[32];
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+#pragma unroll 1
+                        for (int u = item0 + 1; u <= u_last; ++u) {
+                            if (sk_start(u) == sk_start(u + 1)) continue;
+                            const float4* src = reinterpret_cast<const float4*>(a.sk_slots) +
+                                                (int64_t)(kPair ? 2 * u + (int)rank : u) * (kBM * kBN / 4) +
+                                                q * (kBN / 4) * 32 + c * 8 * 32 + lane;
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) {
+                                const float4 x = __ldcg(src + i * 32);
+                                v[4 * i] += x.x;
+                                v[4 * i + 1] += x.y;
+                                v[4 * i + 2] += x.z;
+                                v[4 * i + 3] += x.w;
+                            }
+                        }
+                        if (text) {
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                const float4 p0 = __ldg(reinterpret_cast<const float4*>(wqkr + c * 32) + 2 * i);
+                                const float4 p1 = __ldg(reinterpret_cast<const float4*>(wqkr + c * 32) + 2 * i + 1);
+                                const float wqk[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+                                const uint32_t hw[4] = {hv[i].x, hv[i].y, hv[i].z, hv[i].w};
+#pragma unroll
+                                for (int e = 0; e < 8; ++e) {
+                                    const float h = (e & 1) ? bf16_hi(hw[e >> 1]) : bf16_lo(hw[e >> 1]);
+                                    const float k = v[8 * i + e] * a.out_scale;
+                                    skk = fmaf(k, k, skk);
+                                    shh = fmaf(h, h, shh);
+                                    shk = fmaf(h * wqk[e], k, shk);
+                                }
+                            }
+                        }
+                    }
+                    if (text) {
+                        // [token][branch][column tile][group][3]
+                        const int P = a.d / kBN;
+                        float* pp =
+                            a.partials + (((t * a.hc + branch) * P + col0 / kBN) * kG + grp) * 3;
+                        pp[0] = skk;
+                        pp[1] = shh;
+                        pp[2] = shk;
+                    }
+                } else {
+                // A lane holds 32 columns of its own row.  An 8 x 8 transpose of
+                // float4 within each group of 8 lanes (three butterfly rounds of
+                // shuffles) gives lane 8 g + j the float4 j of rows 8 g .. 8 g + 7,
+                // so that each store writes four whole 128-byte row segments
+                // instead of 32 scattered 16-byte pieces.
+                const int g8 = lane & ~7, j8 = lane & 7;
+                float* const kv0 = a.kv + ks * a.kv_split_stride + (n0 - kv_col0) + j8 * 4;
+                const int64_t row0 = (int64_t)mb * kBM + q * 32 + g8;
+#pragma unroll 1
+                for (int c = c_first; c < kBN / 32; c += kCStep) {
                     uint32_t r[32];
                     tmem_ld32(taddr + (uint32_t)(c * 32), r);
                     tmem_wait_ld();
+                    float v[32];
 #pragma unroll
                     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 #pragma unroll 1
@@ -1311,23 +1437,6 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
                     }
 #pragma unroll
                     for (int i = 0; i < 32; ++i) v[i] *= a.out_scale;
-                };
-                // kEpiForwardSk: a value tile stores its 256 columns of v into
-                // kv = v [T][d] (its gate runs later, from the key tiles' sums)
-                const int kv_col0 = kMode == kEpiForwardSk ? a.hc * a.d : 0;
-                if (kMode == kEpiStoreKv || (kMode == kEpiForwardSk && n0 >= a.hc * a.d)) {
-                // A lane holds 32 columns of its own row.  An 8 x 8 transpose of
-                // float4 within each group of 8 lanes (three butterfly rounds of
-                // shuffles) gives lane 8 g + j the float4 j of rows 8 g .. 8 g + 7,
-                // so that each store writes four whole 128-byte row segments
-                // instead of 32 scattered 16-byte pieces.
-                const int g8 = lane & ~7, j8 = lane & 7;
-                float* const kv0 = a.kv + ks * a.kv_split_stride + (n0 - kv_col0) + j8 * 4;
-                const int64_t row0 = (int64_t)mb * kBM + q * 32 + g8;
-#pragma unroll 1
-                for (int c = c_first; c < kBN / 32; c += kCStep) {
-                    float v[32];
-                    acc_chunk(c, v);
                     if (a.kv_bf16) {
                         // kv rounded once to BF16: the lane's 64 bytes are four
                         // 16-byte pieces; a 4 x 4 transpose within each group of 4
@@ -1393,7 +1502,8 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
                                 make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
                     }
                 }
-            } else if (kFwd && n0 < a.hc * a.d) {
+                }  // kv store
+            } else if (kFwdWhole && n0 < a.hc * a.d) {
                 const int branch = n0 / a.d;
                 const int col0 = n0 - branch * a.d;
                 const bool text = t < a.T && a.windows[t].x != kDead;
@@ -1402,15 +1512,15 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
                 float skk = 0.f, shh = 0.f, shk = 0.f;
 #pragma unroll 1
                 for (int c = c_first; c < kBN / 32; c += kCStep) {
-                    // the hidden slice's loads go out before the accumulator is read
+                    uint32_t r[32];
+                    tmem_ld32(taddr + (uint32_t)(c * 32), r);
                     uint4 hv[4];
                     if (text) {
 #pragma unroll
                         for (int i = 0; i < 4; ++i)
                             hv[i] = __ldg(reinterpret_cast<const uint4*>(hrow + c * 32) + i);
                     }
-                    float kv[32];
-                    acc_chunk(c, kv);  // warp-collective: every lane, text row or not
+                    tmem_wait_ld();
                     if (text) {
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
@@ -1421,7 +1531,7 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
 #pragma unroll
                             for (int e = 0; e < 8; ++e) {
                                 const float h = (e & 1) ? bf16_hi(hw[e >> 1]) : bf16_lo(hw[e >> 1]);
-                                const float k = kv[8 * i + e];
+                                const float k = __uint_as_float(r[8 * i + e]) * a.out_scale;
                                 skk = fmaf(k, k, skk);
                                 shh = fmaf(h, h, shh);
                                 shk = fmaf(h * wqk[e], k, shk);
@@ -1438,7 +1548,7 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
                     pp[1] = shh;
                     pp[2] = shk;
                 }
-                if (kMode == kEpiForward) {
+                if (kFwdWhole) {
                     // publish the warp's sums and count them in for its quadrant;
                     // the quadrant's last key tile turns the sums into gates and
                     // raises the quadrant's gates-ready flag
@@ -1464,8 +1574,8 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
                         if (lane == 0) st_release_u32(cnt + 1, 1u);
                     }
                 }
-            } else {  // value tile (kEpiForward)
-                if (kMode == kEpiForward) {
+            } else {  // value tile
+                if (kFwdWhole) {
                     // wait (bounded) for the gates of this M block quadrant
                     if (lane == 0) {
                         const uint64_t t0 = globaltimer();
@@ -1505,8 +1615,9 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
                 uint16_t* const hrow = a.hidden + t * a.hc * (int64_t)a.d + cv;
 #pragma unroll 1
                 for (int c = c_first; c < kBN / 32; c += kCStep) {
-                    float vv[32];
-                    acc_chunk(c, vv);
+                    uint32_t r[32];
+                    tmem_ld32(taddr + (uint32_t)(c * 32), r);
+                    tmem_wait_ld();
                     if (text) {
 #pragma unroll
                         for (int b0 = 0; b0 < 8; b0 += 2) {
@@ -1533,8 +1644,8 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
                                             uint32_t o[4];
 #pragma unroll
                                             for (int e2 = 0; e2 < 4; ++e2) {
-                                                const float v0 = vv[8 * i + 2 * e2];
-                                                const float v1 = vv[8 * i + 2 * e2 + 1];
+                                                const float v0 = __uint_as_float(r[8 * i + 2 * e2]) * a.out_scale;
+                                                const float v1 = __uint_as_float(r[8 * i + 2 * e2 + 1]) * a.out_scale;
                                                 o[e2] = bf16x2_pack_rn(fmaf(gb, v0, bf16_lo(hw[e2])),
                                                                        fmaf(gb, v1, bf16_hi(hw[e2])));
                                             }
@@ -1546,7 +1657,6 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
                     }
                 }
             }
-            }  // the piece that finishes the tile
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {
@@ -1594,13 +1704,14 @@ cudaError_t launch(const MmaArgs& a, const CUtensorMap& tmA, const CUtensorMap& 
     }
     // work units: the (tile, split)s, or with stream K the (tile, stage)s
     constexpr int kKS = k_blocks_per_stage<kASrc, kF16>();
-    // stream K: the kv-store epilogue, or the gate epilogue of kEpiForwardSk
-    // (which always runs it), on the TMA-fed operand, one split
+    // stream K: the kv-store epilogue, or the gate-sum epilogue of kEpiForwardSk
+    // (which always runs it), on a TMA-fed operand, one split
     if ((kMode == kEpiForwardSk) != (a.stream_k && kMode != kEpiStoreKv)) return cudaErrorInvalidValue;
     if (a.stream_k && (kMode == kEpiForward || a.k_splits != 1 || (a.K / kBK) % kKS != 0 ||
                        (kMode == kEpiForwardSk && kASrc != kASrcTma && kASrc != kASrcTmaPair)))
         return cudaErrorInvalidValue;
-    if ((kMode == kEpiForward || kMode == kEpiForwardSk) && a.epi_groups != epilogue_groups<kASrc>())
+    if ((kMode == kEpiForward || kMode == kEpiForwardSk || kMode == kEpiForwardCompact) &&
+        a.epi_groups != epilogue_groups<kASrc>())
         return cudaErrorInvalidValue;
     const int stages = a.stream_k ? (a.K / kBK) / kKS : a.k_splits;
     if (kASrc == kASrcTmaPair) {
@@ -1696,12 +1807,18 @@ cudaError_t launch_project_tma_pair(const MmaArgs& a, bool f16, const CUtensorMa
 
 cudaError_t launch_forward_tma_pair(const MmaArgs& a, bool f16, const CUtensorMap& tmA,
                                    const CUtensorMap& tmB_half, cudaStream_t s) {
+    if (a.block_text)  // compacted over the units that hold text
+        return f16 ? launch<kASrcTmaPair, true, kEpiForwardCompact>(a, tmA, tmB_half, s)
+                   : launch<kASrcTmaPair, false, kEpiForwardCompact>(a, tmA, tmB_half, s);
     if (f16) return launch<kASrcTmaPair, true, kEpiForward>(a, tmA, tmB_half, s);
     return launch<kASrcTmaPair, false, kEpiForward>(a, tmA, tmB_half, s);
 }
 
 cudaError_t launch_forward_tma(const MmaArgs& a, bool f16, const CUtensorMap& tmA,
                                const CUtensorMap& tmB, cudaStream_t s) {
+    if (a.block_text)
+        return f16 ? launch<kASrcTma, true, kEpiForwardCompact>(a, tmA, tmB, s)
+                   : launch<kASrcTma, false, kEpiForwardCompact>(a, tmA, tmB, s);
     if (f16) return launch<kASrcTma, true, kEpiForward>(a, tmA, tmB, s);
     return launch<kASrcTma, false, kEpiForward>(a, tmA, tmB, s);
 }

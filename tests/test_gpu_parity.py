@@ -391,6 +391,31 @@ def test_staged_pairs_with_an_odd_block_count(flags):
         s.close()
 
 
+@pytest.mark.parametrize("T,span", [(2048, (256, 768)), (2048, (0, 2048)), (5400, (512, 3072)),
+                                    (5400, (300, 4700)), (5400, (0, 5400))])
+def test_staged_with_long_image_spans(prefill, T, span):
+    # A batch longer than one chunk (about 4,864 tokens here) runs chunk by
+    # chunk, and each chunk's GEMM runs only its 256-token units that hold a
+    # text row (those of image rows only get no items and their gates are
+    # written as 0); a single chunk runs every unit.  Either way every row
+    # matches the oracle: image rows bit for bit with gates 0, text rows
+    # (the first after a span too) within tolerance.
+    win, _, _ = prefill_windows(prefill, 1, T, spans=[span])
+    hidden = synth.hidden_bf16(prefill.w, T)
+    h, gates = run_forward(prefill, win, hidden, staged=True)
+    image = win[:, 0] == eg.DEAD
+    assert image.sum() == min(span[1], T - span[0])
+    assert np.array_equal(h[image], hidden[image]) and (gates[image] == 0).all()
+    assert not np.isnan(gates).any()
+    lo, n = span
+    sample = np.unique(np.clip(np.array([0, lo - 1, lo, lo + 255, lo + n - 1, lo + n, lo + n + 1,
+                                         lo + n + 2, T - 1, 1500, 100, 4863, 4864, 5000]), 0, T - 1))
+    ref = O.forward(geom(prefill.w), prefill.w.table_seeds[0], prefill.oparams[0], prefill.W[0],
+                    prefill.wq[0], prefill.wk[0], win, hidden, sample, nthreads=16)
+    check_hidden(h[sample], ref["h_bf16"], f"image span {span}")
+    assert np.abs(gates[sample] - ref["gates"]).max() <= 1e-3
+
+
 def test_forward_edge_cases(tiny):
     ctx = tiny.model.ctx
     eg.engram_forward(ctx, 0, None, 0, None, None)  # T = 0
