@@ -69,6 +69,9 @@ def parse_args():
     ap.add_argument("--decode-small", action="store_true",
                     help="profiling case of the decode step: 256 sessions, full wkv, a "
                          "4.8M-row table; prints one line with its ms per step")
+    ap.add_argument("--long-small", action="store_true",
+                    help="profiling case of the long prefill: 50,032 tokens through two layers "
+                         "of 4.8M-row tables; prints one line with its ms per layer")
     return ap.parse_args()
 
 
@@ -287,6 +290,9 @@ def main():
         return
     if args.gather_small:
         gather_small(args)
+        return
+    if args.long_small:
+        long_small(args)
         return
     import torch
 
@@ -786,11 +792,31 @@ def extras(args, w, W, wq, wk, tmap, win0, d_win0, model, peaks, dev, sptr, stre
     return out
 
 
-def long_prefill(tmap, peaks, dev, stream):
+def long_small(args):
+    """The long prefill's kernels on 4.8M-row tables, for ncu: same batch,
+    chunks and launches, a table the capture can hold."""
+    import torch
+
+    from engram_gram_conditional_gb300 import build
+
+    build.build()
+    import synth
+
+    dev = torch.device("cuda", 0)
+    wl = synth.WORKLOADS["prefill_50k_2layer"]
+    tmap = synth.token_map(wl.vocab, wl.vc, wl.seed)
+    out = long_prefill(tmap, load_peaks(), dev, torch.cuda.current_stream(), small=True,
+                       steps=args.steps)
+    print(json.dumps({"case": "long_small", **out}), flush=True)
+
+
+def long_prefill(tmap, peaks, dev, stream, small=False, steps=6):
     """The long-prefill workload: one history of 50,032 tokens with three image
     spans of 1,024 tokens, appended once and run through layers L1 and L14
     (64M-row tables, primes of L14 after L1's, random-init wkv per layer) with
     the staged forward.  FLOPs count the 46,960 text rows."""
+    import dataclasses
+
     import torch
 
     import engram_gram_conditional_gb300 as eg
@@ -798,6 +824,8 @@ def long_prefill(tmap, peaks, dev, stream):
     from engram_gram_conditional_gb300.layer import EngramLayerSet
 
     wl = synth.WORKLOADS["prefill_50k_2layer"]
+    if small:
+        wl = dataclasses.replace(wl, bucket_bases=[200_000, 200_000])
     lm = EngramLayerSet.from_workload(wl, tmap, device=dev)
     try:
         Ws = []
@@ -821,15 +849,16 @@ def long_prefill(tmap, peaks, dev, stream):
         for l in range(2):
             eg.engram_forward_staged(lm.ctx, l, d_win, T, d_h, ws, None, sptr)
         ms = timed(lambda i: eg.engram_forward_staged(lm.ctx, i % 2, d_win, T, d_h, ws, None, sptr),
-                   6, stream)
+                   steps, stream)
         eg.engram_sync(lm.ctx, sptr)
         fl = 2.0 * wl.N * wl.K * text
         out = {"tokens": T, "text_tokens": text, "layers": 2,
                "table_rows": [lm.rows(0), lm.rows(1)],
                "ms_per_layer": ms, "tokens_per_s_per_layer": T / (ms / 1000.0),
                "tflops": fl / ms / 1e9, "tc_frac": fl / ms / 1e9 / peaks["bf16"]}
-        queue_oracle(out, wl, 0, *Ws[0], win,
-                     f"positions of the long prefill, layer L1 ({lm.rows(0):,}-row table)")
+        if not small:
+            queue_oracle(out, wl, 0, *Ws[0], win,
+                         f"positions of the long prefill, layer L1 ({lm.rows(0):,}-row table)")
         return out
     finally:
         lm.close()

@@ -381,18 +381,22 @@ constexpr int kGateBranchThreads = 256;
 
 // The gate's second half after the stream-K GEMM whose key tiles published
 // their sums (Σk², Σh², Σh w_q w_k k per (token, branch, column tile, epilogue
-// group)) and whose value tiles stored v [T][d].  CTA (t, part) takes columns
-// [part d / parts, (part + 1) d / parts) of token t for every branch: it
-// turns the branch sums into gates (added in (tile, group) order, as the
-// whole-tile gate epilogue adds them), then hidden_b += g_b v with one BF16
-// rounding, v read once for all branches.  Image rows pass through.  Each
-// thread owns at most one float4 of columns (parts = ceil(d / 4 / threads)),
-// and every load is issued at once: the thread's v and hidden, and all of
-// the token's sums (hc x d / 256 x groups x 3 floats, staged in shared
-// memory by the whole CTA) before the gates are added up, so the kernel
-// waits for memory about once.
-constexpr int kGateSumsThreads = 256;
-__global__ void __launch_bounds__(kGateSumsThreads)
+// group)) and whose value tiles stored v [T][d].  CTA (t, part) takes
+// kGateSumsCols float4 columns of token t for every branch: it turns the
+// branch sums into gates (added in (tile, group) order, as the whole-tile gate
+// epilogue adds them), then hidden_b += g_b v with one BF16 rounding, v read
+// once for all branches.  Image rows pass through.  Every load is issued at
+// once: the thread's v and hidden columns, and all of the token's sums
+// (hc x d / 256 x groups x 3 floats, staged in shared memory by the whole CTA)
+// before the gates are added up, so the kernel waits for memory about once.
+// Small CTAs of two float4 columns a thread: a decode batch (256 tokens, d =
+// 5,120) is 1,280 CTAs, all resident at once (nine per SM).  kMaxHc bounds
+// hc, so that a thread holds registers for the branches there are.
+constexpr int kGateSumsThreads = 128;
+constexpr int kGateSumsPer = 2;  // float4 columns a thread
+constexpr int kGateSumsCols = kGateSumsThreads * kGateSumsPer;
+template <int kMaxHc>
+__global__ void __launch_bounds__(kGateSumsThreads, 9)
 k_gate_sums(const float* __restrict__ partials, int groups, const float* __restrict__ v,
             const uint4* __restrict__ windows, int hc, int d, float eps, int parts,
             uint16_t* __restrict__ hidden, float* __restrict__ gates) {
@@ -407,16 +411,19 @@ k_gate_sums(const float* __restrict__ partials, int groups, const float* __restr
         return;
     }
     const int n4 = d / 4;
-    const int i = part * kGateSumsThreads + (int)threadIdx.x;  // this thread's float4 column
-    const bool live = i < n4;
     uint2* const ht = reinterpret_cast<uint2*>(hidden + t * hc * (int64_t)d);
-    float4 vi = make_float4(0.f, 0.f, 0.f, 0.f);
-    uint2 h2[8];
-    if (live) {
-        vi = __ldcg(reinterpret_cast<const float4*>(v + t * (int64_t)d) + i);
+    const float4* const vt = reinterpret_cast<const float4*>(v + t * (int64_t)d);
+    float4 vi[kGateSumsPer];
+    uint2 h2[kGateSumsPer][kMaxHc];
 #pragma unroll
-        for (int b = 0; b < 8; ++b)
-            if (b < hc) h2[b] = ht[(int64_t)b * n4 + i];
+    for (int c = 0; c < kGateSumsPer; ++c) {
+        const int i = part * kGateSumsCols + c * kGateSumsThreads + (int)threadIdx.x;
+        if (i < n4) {
+            vi[c] = __ldcg(vt + i);
+#pragma unroll
+            for (int b = 0; b < kMaxHc; ++b)
+                if (b < hc) h2[c][b] = ht[(int64_t)b * n4 + i];
+        }
     }
     const int P = d / 256 * groups;
     const int nsum = hc * P * 3;
@@ -436,17 +443,21 @@ k_gate_sums(const float* __restrict__ partials, int groups, const float* __restr
         if (gates && part == 0) gates[t * hc + threadIdx.x] = g;
     }
     __syncthreads();
-    if (!live) return;
 #pragma unroll
-    for (int b = 0; b < 8; ++b)
-        if (b < hc) {
-            const float g = gsh[b];
-            const float o0 = fmaf(g, vi.x, bf16_bits_to_f32(h2[b].x & 0xFFFFu));
-            const float o1 = fmaf(g, vi.y, bf16_bits_to_f32(h2[b].x >> 16));
-            const float o2 = fmaf(g, vi.z, bf16_bits_to_f32(h2[b].y & 0xFFFFu));
-            const float o3 = fmaf(g, vi.w, bf16_bits_to_f32(h2[b].y >> 16));
-            ht[(int64_t)b * n4 + i] = make_uint2(bf16x2_pack_rn(o0, o1), bf16x2_pack_rn(o2, o3));
-        }
+    for (int c = 0; c < kGateSumsPer; ++c) {
+        const int i = part * kGateSumsCols + c * kGateSumsThreads + (int)threadIdx.x;
+        if (i >= n4) continue;
+#pragma unroll
+        for (int b = 0; b < kMaxHc; ++b)
+            if (b < hc) {
+                const float g = gsh[b];
+                const float o0 = fmaf(g, vi[c].x, bf16_bits_to_f32(h2[c][b].x & 0xFFFFu));
+                const float o1 = fmaf(g, vi[c].y, bf16_bits_to_f32(h2[c][b].x >> 16));
+                const float o2 = fmaf(g, vi[c].z, bf16_bits_to_f32(h2[c][b].y & 0xFFFFu));
+                const float o3 = fmaf(g, vi[c].w, bf16_bits_to_f32(h2[c][b].y >> 16));
+                ht[(int64_t)b * n4 + i] = make_uint2(bf16x2_pack_rn(o0, o1), bf16x2_pack_rn(o2, o3));
+            }
+    }
 }
 
 // Thirty-two registers a thread (eight CTAs per SM): latency is hidden by
@@ -680,8 +691,7 @@ cudaError_t launch_gate_sums(const Geometry& g, const float* partials, int group
                              cudaStream_t s) {
     if (T == 0) return cudaSuccess;
     if (g.hc > 8 || g.d % kBN != 0 || groups < 1) return cudaErrorInvalidValue;
-    // at most one float4 of v per thread
-    const int parts = (g.d / 4 + kGateSumsThreads - 1) / kGateSumsThreads;
+    const int parts = (g.d / 4 + kGateSumsCols - 1) / kGateSumsCols;
     if (T * parts > INT32_MAX) return cudaErrorInvalidValue;
     const size_t smem = (size_t)g.hc * (g.d / kBN) * groups * 3 * sizeof(float);
     if (smem > 48 * 1024) return cudaErrorInvalidValue;
@@ -695,7 +705,10 @@ cudaError_t launch_gate_sums(const Geometry& g, const float* partials, int group
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, k_gate_sums, partials, groups, v, windows, g.hc, g.d, g.eps,
+    if (g.hc <= 4)
+        return cudaLaunchKernelEx(&cfg, k_gate_sums<4>, partials, groups, v, windows, g.hc, g.d,
+                                  g.eps, parts, hidden, gates);
+    return cudaLaunchKernelEx(&cfg, k_gate_sums<8>, partials, groups, v, windows, g.hc, g.d, g.eps,
                               parts, hidden, gates);
 }
 

@@ -876,22 +876,38 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
     auto k_rotation = [&](int nt, int nkb) { return kFusedA ? 0 : (nt * 13) % nkb; };
 
     // Work items of this CTA (a pair shares them).  Without stream K: the
-    // (tile, split)s item0, item0 + istep, ...  With stream K: the pieces of
-    // this unit's contiguous range [g0, g1) of the launch's (tile, stage)
-    // sequence, one piece per tile the range touches.
+    // (tile, split)s item0, item0 + istep, ...  With stream K: first the
+    // pieces of this unit's contiguous range [g0, g1) of the (tile, stage)
+    // sequence of the launch's first sk_tiles tiles, one piece per tile the
+    // range touches; then whole tiles sk_tiles + k istep + unit, k = 0 ..
+    // dp_waves - 1.  sk_tiles is what is left of the tiles after whole waves
+    // of one tile per unit (all of them when there are fewer tiles than
+    // units), so every unit gets the same number of stages, and each unit's
+    // last item is a whole tile: the pieces that wait for parked partials
+    // finish while the whole tiles' MMAs run, not after the last MMA.
     const int nst_tile = KB / kKS;
     const bool sk = (kMode == kEpiStoreKv && a.stream_k != 0) || kMode == kEpiForwardSk;
-    const int64_t sk_total = (int64_t)m_units * a.n_tiles * nst_tile;
+    const int tiles_all = m_units * a.n_tiles;
+    const int dp_waves = sk ? tiles_all / istep : 0;
+    const int sk_tiles = tiles_all - dp_waves * istep;
+    const int64_t sk_total = (int64_t)sk_tiles * nst_tile;
     auto sk_start = [&](int u) { return (int64_t)u * sk_total / istep; };
     const int64_t sk_g0 = sk_start(item0), sk_g1 = sk_start(item0 + 1);
     const int sk_j0 = (int)(sk_g0 / nst_tile);
-    int n_items = sk ? (sk_g1 > sk_g0 ? (int)((sk_g1 - 1) / nst_tile) - sk_j0 + 1 : 0)
+    const int n_sk_items = sk_g1 > sk_g0 ? (int)((sk_g1 - 1) / nst_tile) - sk_j0 + 1 : 0;
+    int n_items = sk ? n_sk_items + dp_waves
                      : (item0 < total ? (total - item0 + istep - 1) / istep : 0);
     // item i: output tile (mb, nt), split ks, k-blocks [kb_lo, kb_lo + nkb), and
     // its stage range [st_lo, st_hi) within the tile's nst_tile stages
     auto get_item = [&](int i, int& mb, int& nt, int& ks, int& kb_lo, int& nkb, int& st_lo,
                         int& st_hi) {
-        if (sk) {
+        if (sk && i >= n_sk_items) {  // a whole tile
+            coords(sk_tiles + (i - n_sk_items) * istep + item0, mb, nt, ks);
+            st_lo = 0;
+            st_hi = nst_tile;
+            kb_lo = 0;
+            nkb = KB;
+        } else if (sk) {
             const int j = sk_j0 + i;
             coords(j, mb, nt, ks);
             const int64_t base = (int64_t)j * nst_tile;
@@ -1261,6 +1277,120 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
             }
             const int acc = tc & 1;
             const uint32_t aph = (uint32_t)(tc >> 1) & 1u;
+            const int64_t t = (int64_t)mb * kBM + m;
+            const int n0 = (a.n_tile_begin + nt) * kBN;
+            // Stream K, the tile's first piece (this range's last item, or a
+            // whole tile): the tile's later stages, if any, lie in the ranges
+            // of the next units, each of which holds one of them as its first
+            // piece, parked in its slot long before.  Their flags are waited
+            // for (bounded), and the first chunk's operands loaded, while the
+            // MMAs of this item still run; each later chunk's operands load
+            // while the chunk before it is finished.
+            constexpr bool kSkEpi = kMode == kEpiStoreKv || kMode == kEpiForwardSk;
+            const bool sk_finish = kSkEpi && sk && st_lo == 0 && mb < a.m_blocks;
+            int u_last = item0;
+            if (sk_finish && st_hi < nst_tile) {
+                const int64_t g_end = (int64_t)(sk_j0 + tc) * nst_tile + nst_tile - 1;
+                u_last = (int)(((g_end + 1) * istep - 1) / sk_total);
+                int ready = 1;
+                if (lane == 0) {
+                    const uint64_t t0 = globaltimer();
+                    for (int u = item0 + 1; u <= u_last && ready; ++u) {
+                        if (sk_start(u) == sk_start(u + 1)) continue;  // an empty range
+                        const uint32_t* f = a.sk_flags +
+                                            (kPair ? 2 * u + (int)rank : u) * kSkFlagsPerCta + eslot;
+                        uint32_t n = 0;
+                        while (ld_acquire_u32(f) == 0u) {
+                            if ((++n & 63u) == 0u &&
+                                ((long long)(globaltimer() - t0) > lim || *abort_flag)) {
+                                ready = 0;
+                                break;
+                            }
+                        }
+                    }
+                }
+                ready = __shfl_sync(0xFFFFFFFFu, ready, 0);
+                if (!ready) {
+                    if (lane == 0) fail();
+                    break;
+                }
+                // the warp's later loads of the parked pieces are ordered after
+                // lane 0's acquire (a full fence here would first wait for the
+                // stores of the item before)
+                __syncwarp();
+            }
+            // The parked pieces to add, in unit order (which is k order): the
+            // first (u1; -1 for none) is loaded with the chunk's other operands,
+            // any later ones (u_rest .. u_last: ranges shorter than a tile) one
+            // after another.
+            int u1 = -1, u_rest = u_last + 1;
+            for (int u = item0 + 1; u <= u_last; ++u) {
+                if (sk_start(u) == sk_start(u + 1)) continue;  // an empty range
+                if (u1 < 0) {
+                    u1 = u;
+                } else {
+                    u_rest = u;
+                    break;
+                }
+            }
+            auto slot_src = [&](int u, int c) {
+                return reinterpret_cast<const float4*>(a.sk_slots) +
+                       (int64_t)(kPair ? 2 * u + (int)rank : u) * (kBM * kBN / 4) + q * (kBN / 4) * 32 +
+                       c * 8 * 32 + lane;
+            };
+            // v[0..31] += the parked pieces of chunk c (x1 loaded already)
+            auto add_parked = [&](float* v, const float4* x1, int c) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    if (u1 >= 0) {
+                        v[4 * i] += x1[i].x;
+                        v[4 * i + 1] += x1[i].y;
+                        v[4 * i + 2] += x1[i].z;
+                        v[4 * i + 3] += x1[i].w;
+                    }
+                }
+#pragma unroll 1
+                for (int u = u_rest; u <= u_last; ++u) {
+                    if (sk_start(u) == sk_start(u + 1)) continue;
+                    const float4* src = slot_src(u, c);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const float4 x = __ldcg(src + i * 32);
+                        v[4 * i] += x.x;
+                        v[4 * i + 1] += x.y;
+                        v[4 * i + 2] += x.z;
+                        v[4 * i + 3] += x.w;
+                    }
+                }
+            };
+            // kEpiForwardSk key tile: the rows' hidden slice of this branch
+            const bool key_tile = kMode == kEpiForwardSk && n0 < a.hc * a.d;
+            const int branch = key_tile ? n0 / a.d : 0;
+            const int col0 = n0 - branch * a.d;
+            const bool text = key_tile && t < a.T && a.windows[t].x != kDead;
+            const uint16_t* hrow = text ? a.hidden + (t * a.hc + branch) * (int64_t)a.d + col0 : nullptr;
+            // Operands of chunk c: the hidden slice (key tiles of text rows),
+            // w_q w_k of column 32 c + lane (passed round the warp by shuffles)
+            // and the parked piece u1.  The first chunk's are loaded before
+            // the accumulator is ready, each later chunk's while the chunk
+            // before it is finished.
+            const float* wqkr = key_tile ? a.wqk + (int64_t)branch * a.d + col0 : nullptr;
+            uint4 hv_n[4];
+            float wq_n = 0.f;
+            float4 x_n[8];
+            auto issue = [&](int c) {
+                if (key_tile) wq_n = __ldg(wqkr + c * 32 + lane);
+                if (text) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) hv_n[i] = __ldg(reinterpret_cast<const uint4*>(hrow + c * 32) + i);
+                }
+                if (u1 >= 0) {
+                    const float4* src = slot_src(u1, c);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) x_n[i] = __ldcg(src + i * 32);
+                }
+            };
+            if (sk_finish) issue(c_first);
             int full_ok = 1;
             if (lane == 0) full_ok = mbar_wait(tfull(acc), aph, abort_flag, lim);
             full_ok = __shfl_sync(0xFFFFFFFFu, full_ok, 0);
@@ -1270,8 +1400,6 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
             }
             tc_fence_after();
             const uint32_t taddr = tmem_base + (uint32_t)(acc * kBN) + ((uint32_t)(q * 32) << 16);
-            const int64_t t = (int64_t)mb * kBM + m;
-            const int n0 = (a.n_tile_begin + nt) * kBN;
             // an odd pair CTA past the last M block has no rows to write
             int holds_sum = mb < a.m_blocks ? 1 : 0;
             if (holds_sum && kFwdWhole && a.k_splits > 1) {
@@ -1304,92 +1432,39 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
                 __threadfence();
                 __syncwarp();
                 if (lane == 0) st_release_u32(a.sk_flags + cta * kSkFlagsPerCta + eslot, 1u);
-            } else if (kMode == kEpiStoreKv || kMode == kEpiForwardSk) {
-                // Stream K, the tile's first piece but not all of it: the later
-                // stages lie in the ranges of the next units (each holds one of
-                // them as its first piece, parked in its slot); wait (bounded) for
-                // those and add them in unit order, which is k order.
-                int u_last = item0;
-                if (sk && st_hi < nst_tile) {
-                    const int64_t g_end = (int64_t)(sk_j0 + tc) * nst_tile + nst_tile - 1;
-                    u_last = (int)(((g_end + 1) * istep - 1) / sk_total);
-                    int ready = 1;
-                    if (lane == 0) {
-                        const uint64_t t0 = globaltimer();
-                        for (int u = item0 + 1; u <= u_last && ready; ++u) {
-                            if (sk_start(u) == sk_start(u + 1)) continue;  // an empty range
-                            const uint32_t* f = a.sk_flags +
-                                                (kPair ? 2 * u + (int)rank : u) * kSkFlagsPerCta + eslot;
-                            uint32_t n = 0;
-                            while (ld_acquire_u32(f) == 0u) {
-                                if ((++n & 63u) == 0u &&
-                                    ((long long)(globaltimer() - t0) > lim || *abort_flag)) {
-                                    ready = 0;
-                                    break;
-                                }
-                            }
-                        }
-                    }
-                    ready = __shfl_sync(0xFFFFFFFFu, ready, 0);
-                    if (!ready) {
-                        if (lane == 0) fail();
-                        break;
-                    }
-                    __threadfence();
-                }
+            } else if (kSkEpi) {
                 // kEpiForwardSk: a key tile publishes its gate sums; a value
                 // tile stores its 256 columns of v into kv = v [T][d]
                 const int kv_col0 = kMode == kEpiForwardSk ? a.hc * a.d : 0;
-                if (kMode == kEpiForwardSk && n0 < a.hc * a.d) {
-                    const int branch = n0 / a.d;
-                    const int col0 = n0 - branch * a.d;
-                    const bool text = t < a.T && a.windows[t].x != kDead;
-                    const uint16_t* hrow = a.hidden + (t * a.hc + branch) * (int64_t)a.d + col0;
-                    const float* wqkr = a.wqk + (int64_t)branch * a.d + col0;
+                if (key_tile) {
                     float skk = 0.f, shh = 0.f, shk = 0.f;
 #pragma unroll 1
                     for (int c = c_first; c < kBN / 32; c += kCStep) {
+                        uint4 hv[4];
+                        const float wq = wq_n;
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) hv[i] = hv_n[i];
                         uint32_t r[32];
                         tmem_ld32(taddr + (uint32_t)(c * 32), r);
-                        uint4 hv[4];
-                        if (text) {
-#pragma unroll
-                            for (int i = 0; i < 4; ++i)
-                                hv[i] = __ldg(reinterpret_cast<const uint4*>(hrow + c * 32) + i);
-                        }
                         tmem_wait_ld();
                         float v[32];
 #pragma unroll
                         for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-#pragma unroll 1
-                        for (int u = item0 + 1; u <= u_last; ++u) {
-                            if (sk_start(u) == sk_start(u + 1)) continue;
-                            const float4* src = reinterpret_cast<const float4*>(a.sk_slots) +
-                                                (int64_t)(kPair ? 2 * u + (int)rank : u) * (kBM * kBN / 4) +
-                                                q * (kBN / 4) * 32 + c * 8 * 32 + lane;
+                        add_parked(v, x_n, c);
+                        if (c + kCStep < kBN / 32) issue(c + kCStep);  // hv_n, x_n are free again
 #pragma unroll
-                            for (int i = 0; i < 8; ++i) {
-                                const float4 x = __ldcg(src + i * 32);
-                                v[4 * i] += x.x;
-                                v[4 * i + 1] += x.y;
-                                v[4 * i + 2] += x.z;
-                                v[4 * i + 3] += x.w;
-                            }
-                        }
-                        if (text) {
+                        for (int i = 0; i < 4; ++i) {
+                            const uint32_t hw[4] = {hv[i].x, hv[i].y, hv[i].z, hv[i].w};
 #pragma unroll
-                            for (int i = 0; i < 4; ++i) {
-                                const float4 p0 = __ldg(reinterpret_cast<const float4*>(wqkr + c * 32) + 2 * i);
-                                const float4 p1 = __ldg(reinterpret_cast<const float4*>(wqkr + c * 32) + 2 * i + 1);
-                                const float wqk[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
-                                const uint32_t hw[4] = {hv[i].x, hv[i].y, hv[i].z, hv[i].w};
-#pragma unroll
-                                for (int e = 0; e < 8; ++e) {
+                            for (int e = 0; e < 8; ++e) {
+                                // every lane takes part in the shuffle; image rows add nothing
+                                const float wqk = __shfl_sync(0xFFFFFFFFu, wq, 8 * i + e);
+                                if (text) {
                                     const float h = (e & 1) ? bf16_hi(hw[e >> 1]) : bf16_lo(hw[e >> 1]);
                                     const float k = v[8 * i + e] * a.out_scale;
                                     skk = fmaf(k, k, skk);
                                     shh = fmaf(h, h, shh);
-                                    shk = fmaf(h * wqk[e], k, shk);
+                                    shk = fmaf(h * wqk, k, shk);
                                 }
                             }
                         }
@@ -1420,21 +1495,8 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
                     float v[32];
 #pragma unroll
                     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-#pragma unroll 1
-                    for (int u = item0 + 1; u <= u_last; ++u) {
-                        if (sk_start(u) == sk_start(u + 1)) continue;
-                        const float4* src = reinterpret_cast<const float4*>(a.sk_slots) +
-                                            (int64_t)(kPair ? 2 * u + (int)rank : u) * (kBM * kBN / 4) +
-                                            q * (kBN / 4) * 32 + c * 8 * 32 + lane;
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            const float4 x = __ldcg(src + i * 32);
-                            v[4 * i] += x.x;
-                            v[4 * i + 1] += x.y;
-                            v[4 * i + 2] += x.z;
-                            v[4 * i + 3] += x.w;
-                        }
-                    }
+                    add_parked(v, x_n, c);
+                    if (c + kCStep < kBN / 32) issue(c + kCStep);  // x_n is free again
 #pragma unroll
                     for (int i = 0; i < 32; ++i) v[i] *= a.out_scale;
                     if (a.kv_bf16) {
