@@ -408,20 +408,24 @@ def main():
     # ---- e2e through the C ABI with host buffers ----
     # Every step appends its tokens on the host, copies its windows and hidden
     # from pinned host memory, runs the forward and copies the updated hidden
-    # back.  Three streams and two buffer sets pipeline the steps: step i's
+    # back.  Three streams and three buffer sets pipeline the steps: step i's
     # upload and step i-1's download (opposite directions of the host link)
-    # overlap step i-1's and i's compute.
+    # overlap each other and the compute.  With two sets, step i's upload
+    # would wait for step i-2's download, and upload, compute and download
+    # would take turns over two steps; with three, the link's two directions
+    # bound the step.
+    NB = 3
     s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
-    h_win = [torch.empty((T, 4), dtype=torch.int32, pin_memory=True) for _ in range(2)]
+    h_win = [torch.empty((T, 4), dtype=torch.int32, pin_memory=True) for _ in range(NB)]
     h_hid_in = [torch.from_numpy(x.view(np.int16)).pin_memory() for x in hid_h[:2]]
     h_hid_out = [torch.empty((T, w.hc, w.d), dtype=torch.int16, pin_memory=True)
-                 for _ in range(2)]
-    e_win = [torch.empty((T, 4), dtype=torch.int32, device=dev) for _ in range(2)]
-    e_hid = [torch.empty((T, w.hc, w.d), dtype=torch.int16, device=dev) for _ in range(2)]
-    ev_in = [torch.cuda.Event() for _ in range(2)]
-    ev_comp = [torch.cuda.Event() for _ in range(2)]
-    ev_out = [torch.cuda.Event() for _ in range(2)]
-    for j in range(2):  # recorded once so that the first waits return at once
+                 for _ in range(NB)]
+    e_win = [torch.empty((T, 4), dtype=torch.int32, device=dev) for _ in range(NB)]
+    e_hid = [torch.empty((T, w.hc, w.d), dtype=torch.int16, device=dev) for _ in range(NB)]
+    ev_in = [torch.cuda.Event() for _ in range(NB)]
+    ev_comp = [torch.cuda.Event() for _ in range(NB)]
+    ev_out = [torch.cuda.Event() for _ in range(NB)]
+    for j in range(NB):  # recorded once so that the first waits return at once
         ev_in[j].record(s_in)
         ev_comp[j].record(stream)
         ev_out[j].record(s_out)
@@ -429,12 +433,12 @@ def main():
     h_win_np = [x.numpy().view(np.uint32) for x in h_win]
 
     def e2e_step(i):
-        j = i % 2
-        ev_in[j].synchronize()  # step i - 2's upload has read h_win[j]
+        j = i % NB
+        ev_in[j].synchronize()  # step i - NB's upload has read h_win[j]
         s = eg.engram_session_create(ctx)
         eg.engram_session_append(s, tok_h[i % 2], None, h_win_np[j])
         eg.engram_session_destroy(s)
-        s_in.wait_event(ev_comp[j])  # step i - 2's forward is done with e_win/e_hid[j]
+        s_in.wait_event(ev_comp[j])  # step i - NB's forward is done with e_win/e_hid[j]
         s_in.wait_event(ev_out[j])   # ... and its download has read e_hid[j]
         with torch.cuda.stream(s_in):
             e_win[j].copy_(h_win[j], non_blocking=True)

@@ -232,6 +232,12 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy() {
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
     return p;
 }
+// A policy that keeps the lines it brings into L2 longest.
+__device__ __forceinline__ uint64_t l2_evict_last_policy() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
 __device__ __forceinline__ void fence_proxy_async() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -971,6 +977,9 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
         // launch's outputs (the kv of a small batch) out of L2
         const bool wkv_once = m_units == 1;
         const uint64_t policy = l2_evict_first_policy();
+        // the operand matrix is read once per N tile: its lines stay in L2
+        // before any wkv line is evicted for them
+        const uint64_t policy_a = l2_evict_last_policy();
         if (lane == 0) {
             int it = 0;
             bool ok = true;
@@ -1035,10 +1044,11 @@ k_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorM
                         const int ay = a.a_tiled ? (mb * KB + kb) * 128 : mb * kBM;
                         if constexpr (kPair) {
                             if (issuer) mbar_expect_tx(a_full(sa), 2 * L::kAStageBytes);
-                            tma_load_2d_pair(a_stage(sa), &tmA, map_rank(a_full(sa), 0), ax, ay);
+                            tma_load_2d_pair_hint(a_stage(sa), &tmA, map_rank(a_full(sa), 0), ax, ay,
+                                                  policy_a);
                         } else {
                             mbar_expect_tx(a_full(sa), L::kAStageBytes);
-                            tma_load_2d(a_stage(sa), &tmA, a_full(sa), ax, ay);
+                            tma_load_2d_hint(a_stage(sa), &tmA, a_full(sa), ax, ay, policy_a);
                         }
                     }
                 }
