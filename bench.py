@@ -926,6 +926,15 @@ def host_pipeline(model, W, wq, wk, tmap, peaks, dev, stream):
                 dbuf.copy_(hbuf, non_blocking=True)
             ms_h2d = timed(lambda i: dbuf.copy_(hbuf, non_blocking=True), 5, stream)
         del hbuf, dbuf
+        # the link read through UVA: a kernel (the E8M0 scan of the bind) reading
+        # the host table's scale bytes in order, up to 2 GiB
+        scales = hm.tensors[0]["scales"]
+        n_uva = int(min(scales.nbytes, 2 << 30))
+        eg.engram_scale_range(hm.ctx, scales, n_uva)
+        t_u0 = time.perf_counter()
+        for _ in range(3):
+            eg.engram_scale_range(hm.ctx, scales, n_uva)
+        uva_gbs = 3 * n_uva / (time.perf_counter() - t_u0) / 1e9
 
         def stage(i, st):
             eg.engram_stage_rows(hm.ctx, 0, wins[i % nbatch], T, ws[i % 2], st)
@@ -974,8 +983,10 @@ def host_pipeline(model, W, wq, wk, tmap, peaks, dev, stream):
         out = {"tokens_per_step": T, "table_rows": hm.rows(0), "table": "pinned host, UVA",
                "table_bytes": hm.rows(0) * 264, "table_choice": why,
                "h2d_GB_per_s": (1 << 30) / ms_h2d / 1e6,
+               "uva_read_GB_per_s": uva_gbs,
                "stage_ms": ms_stage, "stage_link_GB_per_s": link_bytes / ms_stage / 1e6,
                "stage_frac_of_link": (link_bytes / ms_stage / 1e6) / ((1 << 30) / ms_h2d / 1e6),
+               "stage_frac_of_uva_read": (link_bytes / ms_stage / 1e6) / uva_gbs,
                "gemm_ms": ms_gemm, "serial_ms_per_step": ms_serial,
                "pipelined_ms_per_step": ms_pipe,
                "pipelined_tokens_per_s": T / (ms_pipe / 1000.0)}
