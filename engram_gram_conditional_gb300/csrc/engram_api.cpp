@@ -312,9 +312,10 @@ size_t forward_workspace_bytes(const engram_ctx* ctx, int64_t T, int max_splits)
 }
 
 // Points the forward epilogue's fields of `a` into the workspace and zeroes
-// its counters on `s`.
+// its counters on `s` (unless zero is false: the staging kernel before the
+// GEMM zeroed them, so that no memset stands between the two launches).
 cudaError_t forward_bind_ws(const engram_ctx* ctx, int64_t T, int max_splits, int groups,
-                            void* ws, MmaArgs& a, cudaStream_t s) {
+                            void* ws, MmaArgs& a, cudaStream_t s, bool zero) {
     const ForwardWs w = forward_ws(ctx, T, max_splits, groups);
     a.epi_groups = groups;
     char* base = static_cast<char*>(ws);
@@ -330,7 +331,8 @@ cudaError_t forward_bind_ws(const engram_ctx* ctx, int64_t T, int max_splits, in
         a.split_counters = a.counters + 8 * (size_t)a.m_blocks;
         a.split_partials = reinterpret_cast<float*>(base + w.part + w.gbuf + w.counters);
     }
-    return cudaMemsetAsync(a.counters, 0, w.counter_words * sizeof(uint32_t), s);
+    return zero ? cudaMemsetAsync(a.counters, 0, w.counter_words * sizeof(uint32_t), s)
+                : cudaSuccess;
 }
 
 }  // namespace engram
@@ -371,7 +373,8 @@ engram_status forward_fused(const engram_ctx* ctx, int layer, const uint32_t* d_
     a.n_tiles = ctx->N / kBN;
     // one launch: key tiles publish their sums and count in per M block; a
     // value tile's epilogue waits for its block's count before gating
-    cudaError_t e = forward_bind_ws(ctx, T, max_splits, 1, d_workspace, a, (cudaStream_t)stream);
+    cudaError_t e =
+        forward_bind_ws(ctx, T, max_splits, 1, d_workspace, a, (cudaStream_t)stream, true);
     if (e != cudaSuccess) return cuda_fail(e, "forward counters");
     e = launch_forward_phase(a, kEpiForward, L.f16, L.bucket_gather, tmB, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "forward launch");
@@ -1074,11 +1077,15 @@ static void staged_clear(const engram_ctx* ctx, int64_t T, void* d_workspace, ui
                          int& n_clear) {
     clear = nullptr;
     n_clear = 0;
+    char* const rest = static_cast<char*>(d_workspace) + staged_e_bytes(ctx, T);
     if (staged_stream_k(ctx, T)) {
         const StreamKWs w = stream_k_ws(ctx, T);
-        clear = reinterpret_cast<uint32_t*>(static_cast<char*>(d_workspace) +
-                                            staged_e_bytes(ctx, T) + w.part + w.v + w.slots);
+        clear = reinterpret_cast<uint32_t*>(rest + w.part + w.v + w.slots);
         n_clear = (int)(w.flags / sizeof(uint32_t));
+    } else {  // the forward epilogue's counters
+        const ForwardWs w = forward_ws(ctx, T, 8, 2);
+        clear = reinterpret_cast<uint32_t*>(rest + w.part + w.gbuf);
+        n_clear = (int)w.counter_words;
     }
 }
 
@@ -1235,7 +1242,7 @@ static engram_status staged_rows(const engram_ctx* ctx, int layer, const uint32_
         if (e != cudaSuccess) return cuda_fail(e, "gate launch");
         return ok();
     }
-    e = forward_bind_ws(ctx, T, 8, 2, rest, a, s);
+    e = forward_bind_ws(ctx, T, 8, 2, rest, a, s, !flags_clear);
     // the staging wrote which blocks hold text: the GEMM runs only the units
     // that hold some (a unit of image rows only passes through)
     a.block_text = compact ? staged_block_text(ctx, T, d_workspace) : nullptr;
