@@ -898,8 +898,23 @@ def host_pipeline(model, W, wq, wk, tmap, peaks, dev, stream):
         return {"skipped": "less than 48 GB of host memory available for the pinned table"}
     wh = dataclasses.replace(synth.WORKLOADS["host_table_8x1024"], bucket_bases=bases)
     hm = EngramLayerSet.from_workload(wh, tmap, device=dev)
+
+    def anon_huge() -> int:
+        with open("/proc/meminfo") as f:
+            for ln in f:
+                if ln.startswith("AnonHugePages:"):
+                    return int(ln.split()[1]) * 1024
+        return 0
+
     try:
+        with open("/sys/kernel/mm/transparent_hugepage/enabled") as f:
+            thp_mode = f.read().strip()
+    except OSError:
+        thp_mode = "unknown"
+    try:
+        huge0 = anon_huge()
         hm.bind(0, wh.table_seeds[0], model.tensors[0]["wkv"], wq, wk, host_table=True)
+        huge_gb = (anon_huge() - huge0) / 2**30
         T = wh.sessions * wh.tokens_per_session
         nbatch = 4
         wins, hids = [], []
@@ -982,6 +997,9 @@ def host_pipeline(model, W, wq, wk, tmap, peaks, dev, stream):
         link_bytes = T * wh.nb * 264  # codes and scales read over the link per step
         out = {"tokens_per_step": T, "table_rows": hm.rows(0), "table": "pinned host, UVA",
                "table_bytes": hm.rows(0) * 264, "table_choice": why,
+               # the table's backing: transparent huge pages gained by the bind
+               # (2 MB pages shorten the GPU's translation of random host rows)
+               "thp_mode": thp_mode, "huge_pages_GB": huge_gb,
                "h2d_GB_per_s": (1 << 30) / ms_h2d / 1e6,
                "uva_read_GB_per_s": uva_gbs,
                "stage_ms": ms_stage, "stage_link_GB_per_s": link_bytes / ms_stage / 1e6,
