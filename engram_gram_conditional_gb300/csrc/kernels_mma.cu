@@ -70,10 +70,7 @@ constexpr int kSkFlagsPerCta = 16;
 constexpr int kAStage = kBM * kBK * 2;  // 16 KB
 constexpr int kBStage = kBN * kBK * 2;  // 32 KB
 constexpr int kRowStride = kMaxBuckets + 1;  // row-index table stride (odd: no bank conflicts)
-#ifndef ENGRAM_PREFETCH
-#define ENGRAM_PREFETCH 3
-#endif
-constexpr int kPrefetch = ENGRAM_PREFETCH;   // k-blocks of row slices in flight per lane
+constexpr int kPrefetch = 3;   // k-blocks of row slices in flight per lane
 constexpr int kTmemCols = 2 * kBN;
 
 // Source of the A operand.
