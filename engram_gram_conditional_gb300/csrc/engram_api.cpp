@@ -7,6 +7,9 @@
 #include <cuda_runtime.h>
 #include <string.h>
 #include <sys/mman.h>
+#include <unistd.h>
+
+#include <cstdio>
 
 #include <math.h>
 
@@ -767,8 +770,27 @@ engram_status engram_table_fill_bf16(const engram_ctx* ctx, uint64_t seed, uint1
 engram_status engram_host_table_alloc(uint64_t bytes, void** out) {
     if (!out || bytes == 0) return fail(ENGRAM_EINVAL, "bytes > 0 and an output pointer");
     *out = nullptr;
-    void* p = mmap(nullptr, bytes, PROT_READ | PROT_WRITE, MAP_PRIVATE | MAP_ANONYMOUS, -1, 0);
-    if (p == MAP_FAILED) return fail(ENGRAM_ENOMEM, "mmap of the host table");
+    // The mapping starts on a huge-page boundary (the transparent huge page
+    // size the kernel reports, else 2 MB), so that every whole huge page of
+    // the table can be one: the GPU translates random rows of a 100 GB table
+    // far faster through huge pages.
+    uint64_t huge = 2ull << 20;
+    if (FILE* f = fopen("/sys/kernel/mm/transparent_hugepage/hpage_pmd_size", "r")) {
+        unsigned long long v = 0;
+        if (fscanf(f, "%llu", &v) == 1 && v >= 4096 && (v & (v - 1)) == 0 && v <= (1ull << 30))
+            huge = v;
+        fclose(f);
+    }
+    void* raw = mmap(nullptr, bytes + huge, PROT_READ | PROT_WRITE, MAP_PRIVATE | MAP_ANONYMOUS,
+                     -1, 0);
+    if (raw == MAP_FAILED) return fail(ENGRAM_ENOMEM, "mmap of the host table");
+    const uint64_t r0 = reinterpret_cast<uint64_t>(raw);
+    const uint64_t a0 = (r0 + huge - 1) & ~(huge - 1);
+    if (a0 > r0) munmap(raw, a0 - r0);
+    const uint64_t page = (uint64_t)sysconf(_SC_PAGESIZE);
+    const uint64_t tail = (a0 + bytes + page - 1) & ~(page - 1);  // first page past the table
+    if (r0 + bytes + huge > tail) munmap(reinterpret_cast<void*>(tail), r0 + bytes + huge - tail);
+    void* p = reinterpret_cast<void*>(a0);
     // a hint: the kernel may back the mapping with transparent huge pages
     // (ignored where it offers none)
     (void)madvise(p, bytes, MADV_HUGEPAGE);
