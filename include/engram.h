@@ -294,14 +294,19 @@ engram_status engram_forward(const engram_ctx* ctx, int layer, const uint32_t* d
  * matrix e [T][K] in d_workspace; step 2 is the forward GEMM with its A
  * operand read from e by TMA and the same gate epilogue (kv stays on chip).
  * Unlike engram_forward, the 6,144-vectors pass through device memory (an
- * L2-resident scratch of 12 KB per token for moderate T); in exchange each
- * table row is read once per call instead of once per output tile.  A batch
- * whose output tiles (128 tokens x 256 outputs) do not fill the GPU twice
- * (decode) runs step 2 as a stream-K projection into an fp32 kv [T][N] in
- * the workspace, followed by the gate kernel of engram_gate: the launch's
- * (tile, k-block) sequence is cut into one contiguous range per CTA (or CTA
- * pair), and a tile that two ranges share is summed, in k order, by the range
- * that holds its first k-block.  The result is deterministic on a given
+ * L2-resident scratch of 12 KB per token); in exchange each table row is
+ * read once per call instead of once per output tile.  A batch longer than
+ * about 4,864 tokens (on 152 SMs) runs in chunks of that many on the same
+ * workspace, so that each chunk's e stays in L2, and each chunk's GEMM runs
+ * only its 256-token units that hold a text row.  A batch whose output tiles
+ * (128 tokens x 256 outputs) do not fill the GPU twice (decode) runs step 2
+ * with stream K: the tiles left after whole waves of one tile per CTA pair
+ * have their (tile, stage) sequence cut into one contiguous range per pair,
+ * each pair runs its range and then its whole tiles, and a tile that two
+ * ranges share is summed, in k order, by the range that holds its first
+ * stage.  Its epilogue stores the gate's partial sums of the key tiles and
+ * the value v [T][d] (fp32, in the workspace); a third kernel turns the sums
+ * into gates and updates hidden.  The result is deterministic on a given
  * device (the ranges depend on its SM count).
  * d_workspace: engram_forward_staged_workspace_bytes(ctx, T) bytes. */
 size_t engram_forward_staged_workspace_bytes(const engram_ctx* ctx, int64_t T);
