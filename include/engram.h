@@ -197,13 +197,16 @@ engram_status engram_table_fill_bf16(const engram_ctx* ctx, uint64_t seed, uint1
 
 /* Host memory for a table read through UVA (vLLM "Engram" wiki, "CPU 오프로드":
  * the table in pinned host memory, read by the GPU).  bytes of an anonymous
- * mapping, advised to use transparent huge pages where the kernel offers them,
- * zeroed (every page touched, in parallel) and registered with CUDA, mapped
- * into the device address space; *out is both its host and its device
- * address.  Random row reads from a table this large are bound by address
- * translation, which huge pages reduce: on GB300 (64 KB base pages, 512 MB
- * huge pages), gathering 8,192 tokens x 24 rows from a 101 GB table took
- * 12.8 ms from cudaHostAlloc memory and 5.3 ms from this.  The caller owns the
+ * mapping that starts on a transparent-huge-page boundary, advised to use
+ * huge pages where the kernel offers them, zeroed (every page touched, in
+ * parallel) and registered with CUDA, mapped into the device address space;
+ * *out is both its host and its device address.  Random row reads from a
+ * table this large are bound by address translation, which huge pages
+ * reduce: on GB300 (64 KB base pages, 512 MB huge pages), gathering 8,192
+ * tokens x 24 rows from a 101 GB table took 12.8 ms from cudaHostAlloc
+ * memory and 5.3-5.4 ms from this (how much of the table huge pages cover
+ * depends on the host's free memory; with little of it covered the same
+ * gather took 37.6 ms).  The caller owns the
  * memory and releases it with engram_host_table_free(p, bytes) once no layer
  * is bound to it. */
 engram_status engram_host_table_alloc(uint64_t bytes, void** out);
