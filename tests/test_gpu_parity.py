@@ -392,14 +392,15 @@ def test_staged_pairs_with_an_odd_block_count(flags):
 
 
 @pytest.mark.parametrize("T,span", [(2048, (256, 768)), (2048, (0, 2048)), (5400, (512, 3072)),
-                                    (5400, (300, 4700)), (5400, (0, 5400))])
+                                    (5400, (300, 4700)), (5400, (0, 5400)), (5000, (4800, 100))])
 def test_staged_with_long_image_spans(prefill, T, span):
     # A batch longer than one chunk (about 4,864 tokens here) runs chunk by
     # chunk, and each chunk's GEMM runs only its 256-token units that hold a
     # text row (those of image rows only get no items and their gates are
-    # written as 0); a single chunk runs every unit.  Either way every row
-    # matches the oracle: image rows bit for bit with gates 0, text rows
-    # (the first after a span too) within tolerance.
+    # written as 0); a single chunk runs every unit, and a short last chunk
+    # (136 tokens at 5,000) runs the small-batch path with stream K.  Either
+    # way every row matches the oracle: image rows bit for bit with gates 0,
+    # text rows (the first after a span too) within tolerance.
     win, _, _ = prefill_windows(prefill, 1, T, spans=[span])
     hidden = synth.hidden_bf16(prefill.w, T)
     h, gates = run_forward(prefill, win, hidden, staged=True)
